@@ -1,0 +1,514 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+One decode step of the long-context workload (write the new token of every
+sequence through slot_mapping, then paged decode with split-KV over 16K-40K
+cached keys; batch 8, GQA 16/8, head_dim 128, block 256, bf16) is the headline
+(decode KV GB/s); the same run also measures one chunked-prefill step of the
+varlen workload (write 16 requests' new tokens, then causal varlen prefill over
+cached + new keys; TFLOP/s of the visible query-key pairs).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  With torchrun (N > 1) every rank runs its own replica of
+the workload on its own GPU (no collective on the data path; "replicas only"),
+and timing is the max over ranks.  ``--impl reference`` times the CPU oracle (the
+reference arm of this build) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode KV GB/s & % HBM peak; varlen prefill TFLOP/s & % bf16 peak"
+DECODE_CFG, PREFILL_CFG = 3, 4
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefill", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work of the workloads
+# ---------------------------------------------------------------------------
+def decode_kernel_bytes(step) -> int:
+    """Bytes paged_decode must move: K and V of every visible key, q, out,
+    the block-table entries of every page touched, and cache_seqlens."""
+    L = step.cache_seqlens.astype(np.int64)
+    kv = int(L.sum()) * step.kv_dim * step.elt * 2
+    qo = 2 * step.n_decode * step.hq * step.d * step.elt
+    table = int(np.sum(-(-L // step.block_size))) * 4
+    return kv + qo + table + step.n_decode * 4
+
+
+def write_bytes(step) -> int:
+    """slot_mapping build (token_seq, token_pos read, slot written) and the
+    K/V rows of every non-padding token read and written once."""
+    n_rows = len(step.token_seq)
+    n_real = int((step.token_seq >= 0).sum())
+    return n_rows * 12 + n_real * 4 + n_real * step.kv_dim * step.elt * 2 * 2 + n_rows * 4
+
+
+def prefill_pairs(step) -> int:
+    q = np.diff(step.cu_q).astype(np.int64)
+    k = np.diff(step.cu_k).astype(np.int64)
+    tot = 0
+    for qq, kk in zip(q, k):
+        i = np.arange(qq)
+        tot += int(np.clip(i + kk - qq + 1, 0, kk).sum()) if step.causal else int(qq * kk)
+    return tot
+
+
+def prefill_flops(step) -> int:
+    return 4 * step.d * step.hq * prefill_pairs(step)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class Clocks:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# device-side workload
+# ---------------------------------------------------------------------------
+def to_dev(a: np.ndarray) -> torch.Tensor:
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def pinned(a: np.ndarray) -> torch.Tensor:
+    if a.dtype == np.uint16:
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.pin_memory()
+
+
+class DeviceStep:
+    """Device-resident copy of a synthetic step and the calls of one pass."""
+
+    def __init__(self, step, pkv):
+        self.s, self.pkv = step, pkv
+        self.table = to_dev(step.table)
+        self.k_cache = to_dev(step.k_cache)
+        self.v_cache = to_dev(step.v_cache)
+        self.new_k, self.new_v = to_dev(step.new_k), to_dev(step.new_v)
+        self.token_seq, self.token_pos = to_dev(step.token_seq), to_dev(step.token_pos)
+        self.slots = torch.empty(len(step.token_seq), dtype=torch.int32, device="cuda")
+        if step.n_decode:
+            self.q = to_dev(step.q_decode)
+            self.seqlens = to_dev(step.cache_seqlens)
+            self.dtable = self.table[: step.n_decode].contiguous()
+            self.out = torch.empty_like(self.q)
+            self.ws = torch.empty(max(1, pkv.paged_decode_workspace_size(
+                step.n_decode, step.hq, self.k_cache)), dtype=torch.uint8, device="cuda")
+        if step.n_prefill:
+            self.q = to_dev(step.q_prefill)
+            self.cu_q, self.cu_k = to_dev(step.cu_q), to_dev(step.cu_k)
+            self.ptable = self.table[step.n_decode:].contiguous()
+            self.out = torch.empty_like(self.q)
+            need = pkv.paged_varlen_prefill_workspace_size(step.n_prefill, step.max_seqlen_q,
+                                                          step.hq, self.k_cache)
+            self.ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
+
+    def write(self):
+        pkv, s = self.pkv, self.s
+        pkv.paged_build_slot_mapping(self.table, self.token_seq, self.token_pos, s.block_size,
+                                     out=self.slots)
+        pkv.paged_kv_write(self.new_k, self.new_v, self.slots, self.k_cache, self.v_cache)
+
+    def attend(self):
+        pkv, s = self.pkv, self.s
+        if s.n_decode:
+            pkv.paged_decode(self.q, self.k_cache, self.v_cache, self.dtable, self.seqlens,
+                             s.scale, out=self.out, workspace=self.ws)
+        else:
+            pkv.paged_varlen_prefill(self.q, self.k_cache, self.v_cache, self.cu_q, self.cu_k,
+                                     s.max_seqlen_q, s.max_seqlen_k, self.ptable,
+                                     causal=s.causal, scale=s.scale, out=self.out,
+                                     workspace=self.ws)
+
+
+def time_steps(dev: DeviceStep, steps: int, warmup: int, flush: torch.Tensor | None, world: int):
+    """Warm up, then time `steps` passes (write + attend) with CUDA events on
+    the current stream.  Returns (total ms of the passes, mean ms of attend)."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        dev.write()
+        dev.attend()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(i & 0xff)  # evict the previous pass from L2 (not timed)
+        starts[i].record(stream)
+        dev.write()
+        mids[i].record(stream)
+        dev.attend()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    total = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    attend = [m.elapsed_time(e) for m, e in zip(mids, ends)]
+    return total, float(np.mean(attend)), float(np.median(attend))
+
+
+def time_e2e(step, dev: DeviceStep, steps: int, warmup: int, world: int):
+    """The same pass through the public API from pinned HOST buffers: every
+    step copies its inputs host->device and reads the output back."""
+    s = step
+    host_in = {"new_k": pinned(s.new_k), "new_v": pinned(s.new_v),
+               "token_seq": pinned(s.token_seq), "token_pos": pinned(s.token_pos),
+               "table": pinned(s.table)}
+    if s.n_decode:
+        host_in.update(q=pinned(s.q_decode), seqlens=pinned(s.cache_seqlens))
+    else:
+        host_in.update(q=pinned(s.q_prefill), cu_q=pinned(s.cu_q), cu_k=pinned(s.cu_k))
+    host_out = torch.empty(dev.out.shape, dtype=dev.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def one():
+        dev.new_k.copy_(host_in["new_k"], non_blocking=True)
+        dev.new_v.copy_(host_in["new_v"], non_blocking=True)
+        dev.token_seq.copy_(host_in["token_seq"], non_blocking=True)
+        dev.token_pos.copy_(host_in["token_pos"], non_blocking=True)
+        dev.table.copy_(host_in["table"], non_blocking=True)
+        dev.q.copy_(host_in["q"], non_blocking=True)
+        if s.n_decode:
+            dev.seqlens.copy_(host_in["seqlens"], non_blocking=True)
+            dev.dtable.copy_(dev.table[: s.n_decode])
+        else:
+            dev.cu_q.copy_(host_in["cu_q"], non_blocking=True)
+            dev.cu_k.copy_(host_in["cu_k"], non_blocking=True)
+            dev.ptable.copy_(dev.table[s.n_decode:])
+        dev.write()
+        dev.attend()
+        host_out.copy_(dev.out, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        one()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1), world) / steps
+    return ms, h2d, d2h
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_decode_sample(step, n_seqs: int):
+    """Oracle decode of the first n_seqs sequences; returns (seconds, bytes)."""
+    import oracle
+    sub = np.arange(n_seqs, dtype=np.int32)
+    t = time.perf_counter()
+    oracle.decode(step.q_decode, step.k_cache, step.v_cache, step.decode_table,
+                  step.cache_seqlens, step.scale, seq_subset=sub)
+    dt = time.perf_counter() - t
+    L = step.cache_seqlens[:n_seqs].astype(np.int64)
+    return dt, int(L.sum()) * step.kv_dim * step.elt * 2
+
+
+def oracle_prefill_sample(step, every: int):
+    """Oracle prefill of every `every`-th query row; returns (seconds, flops)."""
+    import oracle
+    rows = np.arange(0, int(step.cu_q[-1]), every, dtype=np.int32)
+    t = time.perf_counter()
+    oracle.prefill(step.q_prefill, step.k_cache, step.v_cache, step.cu_q, step.cu_k, step.scale,
+                   causal=step.causal, block_table=step.prefill_table,
+                   block_size=step.block_size, row_subset=rows)
+    dt = time.perf_counter() - t
+    q = np.diff(step.cu_q)
+    k = np.diff(step.cu_k)
+    req = np.searchsorted(step.cu_q, rows, side="right") - 1
+    i = rows - step.cu_q[req]
+    vis = np.clip(i + k[req] - q[req] + 1, 0, k[req]).astype(np.int64)
+    return dt, int(4 * step.d * step.hq * vis.sum())
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the CPU oracle on a bounded sample of the decode workload."""
+    from paged_kv_cache_70_gb300 import workloads as W
+    import oracle
+    if rank != 0:
+        return
+    step = W.config(DECODE_CFG)
+    n_seqs = 1
+    for _ in range(args.warmup):
+        oracle_decode_sample(step, n_seqs)
+    times, nbytes = [], 0
+    for _ in range(args.steps):
+        dt, nbytes = oracle_decode_sample(step, n_seqs)
+        times.append(dt)
+    sec = sum(times) / len(times)
+    value = nbytes / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": W.CONFIG_NAMES[DECODE_CFG], "sample": f"{n_seqs} of 8 sequences",
+                   "seed": 1000 + DECODE_CFG},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"decode of sequence 0 (all 16 heads, "
+                                   f"{int(step.cache_seqlens[0])} keys) per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def main():
+    args = parse_args()
+    world, rank = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    import paged_kv_cache_70_gb300 as pkv
+    from paged_kv_cache_70_gb300 import workloads as W
+    hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
+
+    # ---------------- decode (headline) ----------------
+    dstep = W.config(DECODE_CFG)
+    ddev = DeviceStep(dstep, pkv)
+    clocks = Clocks(torch.cuda.current_device())
+    clocks.start()
+    total_ms, dec_mean, dec_med = time_steps(ddev, args.steps, args.warmup, None, world)
+    clk = clocks.stop()
+    total_ms = max_over_ranks(total_ms, world)
+    ms_step = total_ms / args.steps
+    dbytes = decode_kernel_bytes(dstep)
+    wbytes = write_bytes(dstep)
+    step_bytes = dbytes + wbytes
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    # workspace traffic of the split (partials written and read back)
+    ctas = torch.cuda.get_device_properties(0).multi_processor_count
+    part = (ctas + dstep.n_decode) * dstep.hq * (dstep.d + 2) * 4 * 2
+    achieved = dbytes / (dec_mean * 1e-3) / 1e9
+    e2e_ms, h2d, d2h = time_e2e(dstep, ddev, args.steps, args.warmup, world)
+    flags = pkv.paged_error_flags()
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": W.CONFIG_NAMES[DECODE_CFG] + "; step = slot_mapping build + "
+                               "new-token write + paged decode (split-KV + combine)",
+                   "batch": dstep.n_decode, "seq_lens_total": int(dstep.cache_seqlens.sum()),
+                   "block_size": dstep.block_size, "num_heads": dstep.hq,
+                   "num_kv_heads": dstep.hkv, "head_dim": dstep.d, "seed": 1000 + DECODE_CFG,
+                   "bytes_per_step": step_bytes,
+                   "l2": "inputs larger than L2 (%.0f MB of K/V per step)" % (dbytes / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "paged_decode (split kernel + combine)",
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
+                     "traffic": None, "algorithmic_bytes_per_launch": dbytes,
+                     "workspace_bytes_per_launch": part,
+                     "mean_ms": round(dec_mean, 5), "median_ms": round(dec_med, 5)},
+        "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+        "error_flags": flags,
+    }
+    del ddev
+    torch.cuda.empty_cache()
+
+    # ---------------- prefill ----------------
+    if not args.no_prefill:
+        pstep = W.config(PREFILL_CFG)
+        pdev = DeviceStep(pstep, pkv)
+        try:
+            pdev.attend()
+            ok = True
+        except pkv.PagedKVError as e:
+            ok = False
+            line["prefill"] = {"unavailable": str(e)}
+        if ok:
+            flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+            clocks = Clocks(torch.cuda.current_device())
+            clocks.start()
+            ptotal, pmean, pmed = time_steps(pdev, args.steps, args.warmup, flush, world)
+            pclk = clocks.stop()
+            ptotal = max_over_ranks(ptotal, world)
+            flops = prefill_flops(pstep)
+            p_ms = ptotal / args.steps
+            tflops = flops / (pmean * 1e-3) / 1e12
+            pe2e_ms, ph2d, pd2h = time_e2e(pstep, pdev, args.steps, args.warmup, world)
+            line["prefill"] = {
+                "metric": "varlen prefill TFLOP/s", "workload": W.CONFIG_NAMES[PREFILL_CFG],
+                "value": round(world * flops / (p_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(p_ms, 5),
+                "step": "slot_mapping build + write of 16 requests' new K/V + causal varlen "
+                        "prefill (L2 flushed between steps, not timed)",
+                "flops_per_step": flops, "visible_pairs": prefill_pairs(pstep),
+                "roofline": {"bound": "tensor", "kernel": "paged_varlen_prefill",
+                             "achieved": round(tflops, 1), "peak": bf16_peak,
+                             "unit": "TFLOP/s", "frac": round(tflops / bf16_peak, 4),
+                             "peak_source": peak_src + " (bf16 burst)", "traffic": None,
+                             "mean_ms": round(pmean, 5), "median_ms": round(pmed, 5)},
+                "e2e": {"value": round(world * flops / (pe2e_ms * 1e-3) / 1e12, 2),
+                        "unit": "TFLOP/s", "ms_per_step": round(pe2e_ms, 5),
+                        "h2d_bytes_per_step": ph2d, "d2h_bytes_per_step": pd2h},
+                "clocks": pclk,
+            }
+            line["gpu_launches"] += 3 * args.steps
+            line["error_flags"] |= pkv.paged_error_flags()
+        del pdev
+        torch.cuda.empty_cache()
+
+    # ---------------- CPU baseline (oracle, rank 0, N=1) ----------------
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        n_seqs = 8
+        dt, nb = oracle_decode_sample(dstep, n_seqs)
+        line["cpu_baseline"] = {
+            "value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 oracle decode of all {n_seqs} sequences x 16 heads of the decode "
+                      f"workload ({dt:.1f} s)"}
+        if "prefill" in line and "value" in line["prefill"]:
+            pstep = W.config(PREFILL_CFG)
+            dt, fl = oracle_prefill_sample(pstep, 64)
+            line["prefill"]["cpu_baseline"] = {
+                "value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s",
+                "cores": oracle.num_threads(), "kind": "oracle",
+                "sample": f"every 64th query row of the prefill workload ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,183 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 (sm_103a) paged KV-cache attention library
+ * (libpagedkv.so).
+ *
+ * The library implements the data-parallel hot path of paged attention:
+ *   - the slot_mapping KV-cache write (new K/V rows scattered into the paged
+ *     pool, negative slots skipped);
+ *   - one-query-per-sequence decode that reads K/V through a block table and
+ *     merges blocks with the online-softmax rule (split over the keys of long
+ *     sequences, partial states merged by the same rule);
+ *   - causal varlen prefill over cu_seqlens_q / cu_seqlens_k that reads the
+ *     paged prior context (prefix cache / chunked prefill) on the tensor cores.
+ *
+ * Sources: "11. Paged attention 与 online softmax" (dilfish.github.io), §11.1
+ * block table and offset equation, §11.2 boxed merge equation;
+ * "从零开始写Qwen3（六）PagedAttention" (mlqm.cn), sections "fast-attn 库的使用"
+ * (the varlen / kvcache call shapes and their parameters) and "自己来实现一个"
+ * (the slot_mapping write kernel); "Sayfalı dikkat" (Hugging Face transformers
+ * docs), varlen path (cu_seq_lens) and decode path (block_table, cache_seqlens).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Memory.  Every pointer argument is a DEVICE pointer unless stated otherwise
+ * (pkv_geom is read on the host).  The caller owns every buffer; the library
+ * allocates no device memory.  Calls are asynchronous on `stream` and never
+ * synchronise the host, except paged_error_flags.
+ * Layouts (row-major, contiguous):
+ *   K/V pools  [num_blocks, block_size, num_kv_heads, head_dim]; the element
+ *              offset of logical position p of a sequence whose block-table row
+ *              is t is (t[p / B] * B + p % B) * kvDim, kvDim = Hkv * head_dim.
+ *   block_table [rows, max_blocks_per_seq] int32; entries past a sequence's
+ *              length are never read and may hold -1.
+ *   q / out    decode [batch, Hq, head_dim]; prefill [total_q, Hq, head_dim].
+ *   index arrays are int32.
+ * GQA: query head h reads KV head h / (Hq / Hkv).
+ * dtype: q, out and both pools share pkv_geom.dtype.
+ * Return codes: PKV_OK, or a negative PKV_ERR_* (no work is enqueued then).
+ * Device-side checks: an out-of-range block id, slot or sequence length found
+ * while a kernel runs is skipped (never dereferenced) and recorded in a
+ * per-device error word read by paged_error_flags.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types */
+typedef enum pkv_dtype { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* status codes */
+#define PKV_OK 0
+#define PKV_ERR_INVALID (-1)     /* null pointer, bad size, Hq % Hkv != 0, misaligned */
+#define PKV_ERR_UNSUPPORTED (-2) /* valid but not implemented (dtype/head_dim/GQA combo) */
+#define PKV_ERR_WORKSPACE (-3)   /* workspace missing or smaller than the *_workspace_size */
+#define PKV_ERR_CUDA (-4)        /* a CUDA runtime call or kernel launch failed */
+
+/* device error-word bits (paged_error_flags) */
+#define PKV_FLAG_BAD_BLOCK (1u << 0)   /* block-table entry outside [0, num_blocks) */
+#define PKV_FLAG_BAD_SLOT (1u << 1)    /* slot_mapping entry >= num_blocks * block_size */
+#define PKV_FLAG_BAD_LENGTH (1u << 2)  /* length < 0 or beyond max_blocks_per_seq * B */
+#define PKV_FLAG_BAD_SEQ (1u << 3)     /* token sequence index >= num_seqs */
+#define PKV_FLAG_TIMEOUT (1u << 4)     /* a pipeline wait gave up (kernel returned early) */
+
+/* Geometry of one paged pool (one layer's K pool and V pool). */
+typedef struct pkv_geom {
+    int32_t num_heads;    /* Hq, query heads */
+    int32_t num_kv_heads; /* Hkv, KV heads; Hq % Hkv == 0 */
+    int32_t head_dim;     /* d */
+    int32_t block_size;   /* B, tokens per physical block (page) */
+    int64_t num_blocks;   /* physical blocks in each pool */
+    int32_t dtype;        /* pkv_dtype of q, out and the pools */
+} pkv_geom;
+
+/*
+ * paged_build_slot_mapping -- address translation for the new tokens of a step.
+ * ("11. Paged attention 与 online softmax" §11.1: logical block p / B, slot
+ * p mod B, phys = table[p / B]; "自己来实现一个": the per-token index is
+ * computed once and reused by every layer.)
+ *   slot_mapping[n] = block_table[s][p / B] * B + p % B with s = token_seq[n],
+ *   p = token_pos[n]; token_seq[n] < 0 marks a padding row -> -1.
+ *   block_table [num_seqs, max_blocks_per_seq]; token_seq, token_pos,
+ *   slot_mapping [num_tokens].  Out-of-range s, p or table entries give -1 and
+ *   set PKV_FLAG_BAD_SEQ / _BAD_LENGTH / _BAD_BLOCK.
+ */
+int paged_build_slot_mapping(const int32_t* block_table, int32_t max_blocks_per_seq,
+                             int32_t num_seqs, const int32_t* token_seq,
+                             const int32_t* token_pos, int64_t num_tokens, int32_t block_size,
+                             int32_t* slot_mapping, cudaStream_t stream);
+
+/*
+ * paged_kv_write -- the slot_mapping cache write ("自己来实现一个",
+ * _update_paged_kv_cache_kernel).  For every token n with s = slot_mapping[n]
+ * >= 0: k_cache[s*kvDim + j] = cast(k[n*kvDim + j]) and likewise for v,
+ * j < kvDim; s < 0 writes nothing.  k, v [num_tokens, Hkv, d] of kv_dtype; the
+ * pools of geom->dtype.  fp32 -> bf16 rounds to nearest even; equal dtypes
+ * copy bits.  Duplicate non-negative slots are a caller error (the surviving
+ * row is unspecified).  s >= num_blocks*B is skipped and sets PKV_FLAG_BAD_SLOT.
+ */
+int paged_kv_write(const void* k, const void* v, int32_t kv_dtype, const int32_t* slot_mapping,
+                   int64_t num_tokens, void* k_cache, void* v_cache, const pkv_geom* geom,
+                   cudaStream_t stream);
+
+/*
+ * paged_decode_workspace_size -- bytes of device scratch paged_decode needs for
+ * `batch` sequences on the CURRENT device (the split plan depends on its SM
+ * count).  Returns 0 for invalid arguments.
+ */
+size_t paged_decode_workspace_size(int32_t batch, const pkv_geom* geom);
+
+/*
+ * paged_decode -- paged attention of one query token per sequence ("Sayfalı
+ * dikkat" decode path; "11. Paged attention 与 online softmax" §11.1-§11.2).
+ * Sequence b attends over exactly cache_seqlens[b] keys (positions 0 ..
+ * cache_seqlens[b]-1, read through block_table row b), i.e. the new token's
+ * K/V must already have been written with paged_kv_write.
+ *   out[b,h,:] = sum_j softmax_j(scale * q[b,h,:] . k_j) v_j  over those keys,
+ *   0 when cache_seqlens[b] == 0.
+ * The keys of all sequences are cut into equal shares, one per CTA; each CTA
+ * keeps the (m, l, o) online-softmax state of its share and a second kernel
+ * merges the shares of each sequence with the same rule and normalises.
+ * Supported: head_dim 64 or 128; fp32 or bf16; Hq/Hkv in {1, 2, 4}; Hkv in
+ * {1, 2, 4, 8} or a multiple of 8; any block_size >= 1; batch <= 4096.
+ * workspace: device scratch of at least paged_decode_workspace_size(batch, geom)
+ * bytes, 256-byte aligned, contents irrelevant on entry; it must not be used by
+ * another call that runs concurrently.
+ */
+int paged_decode(const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* block_table, int32_t max_blocks_per_seq,
+                 const int32_t* cache_seqlens, int32_t batch, float scale, void* out,
+                 void* workspace, size_t workspace_bytes, const pkv_geom* geom,
+                 cudaStream_t stream);
+
+/*
+ * paged_varlen_prefill_workspace_size -- bytes of device scratch
+ * paged_varlen_prefill needs (0 when it needs none).  Returns 0 for invalid
+ * arguments as well.
+ */
+size_t paged_varlen_prefill_workspace_size(int32_t batch, int32_t max_seqlen_q,
+                                           const pkv_geom* geom);
+
+/*
+ * paged_varlen_prefill -- causal varlen prefill over a paged cache
+ * ("从零开始写Qwen3（六）PagedAttention", "fast-attn 库的使用": prefix cache and
+ * chunked prefill read the cache through block_table; "Sayfalı dikkat" varlen
+ * path).  Request r owns query rows [cu_seqlens_q[r], cu_seqlens_q[r+1]) of q
+ * and keys 0 .. k_len-1, k_len = cu_seqlens_k[r+1] - cu_seqlens_k[r], read
+ * through block_table row r (the new tokens' K/V must already be written).
+ * With causal != 0 query i of a request with q_len queries sees key j iff
+ * j <= i + k_len - q_len (bottom-right alignment: the queries are the last
+ * q_len positions); a row that sees no key outputs 0.
+ * max_seqlen_q / max_seqlen_k are host-side upper bounds of the per-request
+ * lengths (they size the launch).  q, out [total_q, Hq, d].
+ * Supported: bf16, head_dim 128, Hq/Hkv in {1, 2, 4, 8, ...}, any block_size
+ * that is a multiple of 16 or divides 128.
+ */
+int paged_varlen_prefill(const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
+                         int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t* block_table,
+                         int32_t max_blocks_per_seq, int32_t causal, float scale, void* out,
+                         void* workspace, size_t workspace_bytes, const pkv_geom* geom,
+                         cudaStream_t stream);
+
+/*
+ * paged_error_flags -- read (and with clear != 0, reset) the device error word
+ * of the current device: an OR of PKV_FLAG_* bits set by kernels since the
+ * last clear.  Synchronises with the device.  *flags (host pointer) receives
+ * the word.
+ */
+int paged_error_flags(uint32_t* flags, int32_t clear);
+
+/* paged_status_string -- static text for a PKV_* status code. */
+const char* paged_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGEDKV_H */

@@ -1,0 +1,257 @@
+"""ctypes binding of libpagedkv.so (include/pagedkv.h).
+
+Argument marshalling only: shapes and dtypes are read from torch tensors,
+device pointers and the current CUDA stream are passed to the C ABI, and a
+non-zero status raises :class:`PagedKVError`.  Every step of the computation
+runs in the library's CUDA kernels; there is no fallback path.  PyTorch is used
+for device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libpagedkv.so")
+
+PKV_F32, PKV_BF16 = 0, 1
+PKV_FLAG_BAD_BLOCK = 1 << 0
+PKV_FLAG_BAD_SLOT = 1 << 1
+PKV_FLAG_BAD_LENGTH = 1 << 2
+PKV_FLAG_BAD_SEQ = 1 << 3
+PKV_FLAG_TIMEOUT = 1 << 4
+
+# every extern "C" entry point of include/pagedkv.h
+EXPORTED = (
+    "paged_build_slot_mapping",
+    "paged_kv_write",
+    "paged_decode_workspace_size",
+    "paged_decode",
+    "paged_varlen_prefill_workspace_size",
+    "paged_varlen_prefill",
+    "paged_error_flags",
+    "paged_status_string",
+)
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, func: str, status: int, msg: str):
+        super().__init__(f"{func} failed with status {status}: {msg}")
+        self.status = status
+
+
+class Geom(ctypes.Structure):
+    _fields_ = [
+        ("num_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int64),
+        ("dtype", ctypes.c_int32),
+    ]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: str | None = None):
+    """Load libpagedkv.so (built in-tree by ``paged_kv_cache_70_gb300.build``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"libpagedkv.so not found at {p}; build it with "
+                "`python -m paged_kv_cache_70_gb300.build` (needs nvcc)")
+        lib = ctypes.CDLL(p)
+        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        gp = ctypes.POINTER(Geom)
+        lib.paged_build_slot_mapping.argtypes = [vp, i32, i32, vp, vp, i64, i32, vp, vp]
+        lib.paged_build_slot_mapping.restype = ctypes.c_int
+        lib.paged_kv_write.argtypes = [vp, vp, i32, vp, i64, vp, vp, gp, vp]
+        lib.paged_kv_write.restype = ctypes.c_int
+        lib.paged_decode_workspace_size.argtypes = [i32, gp]
+        lib.paged_decode_workspace_size.restype = sz
+        lib.paged_decode.argtypes = [vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp, sz,
+                                     gp, vp]
+        lib.paged_decode.restype = ctypes.c_int
+        lib.paged_varlen_prefill_workspace_size.argtypes = [i32, i32, gp]
+        lib.paged_varlen_prefill_workspace_size.restype = sz
+        lib.paged_varlen_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp, i32, i32,
+                                             ctypes.c_float, vp, vp, sz, gp, vp]
+        lib.paged_varlen_prefill.restype = ctypes.c_int
+        lib.paged_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+        lib.paged_error_flags.restype = ctypes.c_int
+        lib.paged_status_string.argtypes = [ctypes.c_int]
+        lib.paged_status_string.restype = ctypes.c_char_p
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(func: str, status: int) -> None:
+    if status != 0:
+        msg = load_library().paged_status_string(status).decode()
+        raise PagedKVError(func, status, msg)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return PKV_F32
+    if t.dtype == torch.bfloat16:
+        return PKV_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _cuda_contig(name: str, t: torch.Tensor, dtype=None) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def geom_of(k_cache: torch.Tensor, num_heads: int) -> Geom:
+    """pkv_geom of a pool [num_blocks, block_size, num_kv_heads, head_dim]."""
+    nb, bs, hkv, d = k_cache.shape
+    return Geom(num_heads, hkv, d, bs, nb, _dtype_code(k_cache))
+
+
+def paged_build_slot_mapping(block_table: torch.Tensor, token_seq: torch.Tensor,
+                             token_pos: torch.Tensor, block_size: int,
+                             out: torch.Tensor | None = None) -> torch.Tensor:
+    """slot_mapping[n] = table[s][p // B] * B + p % B (-1 where token_seq < 0)."""
+    for n, t in (("block_table", block_table), ("token_seq", token_seq), ("token_pos", token_pos)):
+        _cuda_contig(n, t, torch.int32)
+    n_tok = token_seq.numel()
+    if out is None:
+        out = torch.empty(n_tok, dtype=torch.int32, device=token_seq.device)
+    _cuda_contig("out", out, torch.int32)
+    rows, width = block_table.shape
+    st = load_library().paged_build_slot_mapping(
+        _ptr(block_table), width, rows, _ptr(token_seq), _ptr(token_pos), n_tok, block_size,
+        _ptr(out), _stream(token_seq))
+    _check("paged_build_slot_mapping", st)
+    return out
+
+
+def paged_kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                   k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
+    """In-place write of k/v [N, Hkv, d] rows into the pools at slot_mapping."""
+    _cuda_contig("k", k)
+    _cuda_contig("v", v, k.dtype)
+    _cuda_contig("slot_mapping", slot_mapping, torch.int32)
+    _cuda_contig("k_cache", k_cache)
+    _cuda_contig("v_cache", v_cache, k_cache.dtype)
+    if k.shape != v.shape or k.shape[1:] != k_cache.shape[2:] or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between k/v rows and the pools")
+    if slot_mapping.numel() != k.shape[0]:
+        raise ValueError("slot_mapping must have one entry per token row")
+    g = geom_of(k_cache, k_cache.shape[2])
+    st = load_library().paged_kv_write(_ptr(k), _ptr(v), _dtype_code(k), _ptr(slot_mapping),
+                                       k.shape[0], _ptr(k_cache), _ptr(v_cache),
+                                       ctypes.byref(g), _stream(k))
+    _check("paged_kv_write", st)
+
+
+def paged_decode_workspace_size(batch: int, q_heads: int, k_cache: torch.Tensor) -> int:
+    g = geom_of(k_cache, q_heads)
+    with torch.cuda.device(k_cache.device):
+        return int(load_library().paged_decode_workspace_size(batch, ctypes.byref(g)))
+
+
+def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 block_table: torch.Tensor, cache_seqlens: torch.Tensor,
+                 scale: float | None = None, out: torch.Tensor | None = None,
+                 workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """One query token per sequence over its cache_seqlens[b] cached keys."""
+    _cuda_contig("q", q, k_cache.dtype)
+    _cuda_contig("k_cache", k_cache)
+    _cuda_contig("v_cache", v_cache, k_cache.dtype)
+    _cuda_contig("block_table", block_table, torch.int32)
+    _cuda_contig("cache_seqlens", cache_seqlens, torch.int32)
+    batch, hq, d = q.shape
+    if d != k_cache.shape[3] or block_table.shape[0] < batch or cache_seqlens.numel() < batch:
+        raise ValueError("shape mismatch")
+    g = geom_of(k_cache, hq)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        need = int(lib.paged_decode_workspace_size(batch, ctypes.byref(g)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, q.dtype)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    with torch.cuda.device(q.device):
+        st = lib.paged_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                              block_table.shape[1], _ptr(cache_seqlens), batch, scale, _ptr(out),
+                              _ptr(workspace), workspace.numel(), ctypes.byref(g), _stream(q))
+    _check("paged_decode", st)
+    return out
+
+
+def paged_varlen_prefill_workspace_size(batch: int, max_seqlen_q: int, q_heads: int,
+                                        k_cache: torch.Tensor) -> int:
+    g = geom_of(k_cache, q_heads)
+    return int(load_library().paged_varlen_prefill_workspace_size(batch, max_seqlen_q,
+                                                                 ctypes.byref(g)))
+
+
+def paged_varlen_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                         cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
+                         max_seqlen_q: int, max_seqlen_k: int, block_table: torch.Tensor,
+                         causal: bool = True, scale: float | None = None,
+                         out: torch.Tensor | None = None,
+                         workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Causal varlen prefill of q [total_q, Hq, d] over the paged cache."""
+    _cuda_contig("q", q, k_cache.dtype)
+    _cuda_contig("k_cache", k_cache)
+    _cuda_contig("v_cache", v_cache, k_cache.dtype)
+    _cuda_contig("cu_seqlens_q", cu_seqlens_q, torch.int32)
+    _cuda_contig("cu_seqlens_k", cu_seqlens_k, torch.int32)
+    _cuda_contig("block_table", block_table, torch.int32)
+    batch = cu_seqlens_q.numel() - 1
+    total_q, hq, d = q.shape
+    g = geom_of(k_cache, hq)
+    lib = load_library()
+    need = int(lib.paged_varlen_prefill_workspace_size(batch, max_seqlen_q, ctypes.byref(g)))
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, q.dtype)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    with torch.cuda.device(q.device):
+        st = lib.paged_varlen_prefill(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch,
+            int(max_seqlen_q), int(max_seqlen_k), _ptr(block_table), block_table.shape[1],
+            1 if causal else 0, scale, _ptr(out), _ptr(workspace),
+            0 if workspace is None else workspace.numel(), ctypes.byref(g), _stream(q))
+    _check("paged_varlen_prefill", st)
+    return out
+
+
+def paged_error_flags(clear: bool = True) -> int:
+    """Device error word of the current device (PKV_FLAG_* bits)."""
+    v = ctypes.c_uint32(0)
+    _check("paged_error_flags", load_library().paged_error_flags(ctypes.byref(v), 1 if clear else 0))
+    return int(v.value)

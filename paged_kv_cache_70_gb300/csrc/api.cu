@@ -1,0 +1,211 @@
+// api.cu -- the extern "C" entry points of libpagedkv (declared in
+// include/pagedkv.h): argument validation, per-device state (SM count,
+// shared-memory limit, error word) and dispatch to the kernel launchers.
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace pkv {
+
+// One error word per device (each device holds its own copy of this variable).
+__device__ unsigned int g_error_word = 0;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+bool g_have[kMaxDevices];
+DeviceInfo g_info[kMaxDevices];
+}  // namespace
+
+cudaError_t current_device_info(DeviceInfo* info) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_have[dev]) {
+        DeviceInfo d{};
+        d.device = dev;
+        e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        int smem = 0;
+        e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        d.max_smem_optin = (size_t)smem;
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_error_word);
+        if (e != cudaSuccess) return e;
+        d.err = static_cast<unsigned int*>(p);
+        g_info[dev] = d;
+        g_have[dev] = true;
+    }
+    *info = g_info[dev];
+    return cudaSuccess;
+}
+
+}  // namespace pkv
+
+using pkv::DeviceInfo;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int elt_size(int dtype) { return dtype == PKV_F32 ? 4 : (dtype == PKV_BF16 ? 2 : 0); }
+
+// common geometry checks; returns PKV_OK or an error code
+int check_geom(const pkv_geom* g) {
+    if (!g) return PKV_ERR_INVALID;
+    if (g->num_heads <= 0 || g->num_kv_heads <= 0 || g->head_dim <= 0 || g->block_size <= 0 ||
+        g->num_blocks < 0)
+        return PKV_ERR_INVALID;
+    if (g->num_heads % g->num_kv_heads) return PKV_ERR_INVALID;
+    if (!elt_size(g->dtype)) return PKV_ERR_INVALID;
+    // slot ids are int32
+    if ((double)g->num_blocks * g->block_size > 2147483647.0) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int paged_build_slot_mapping(const int32_t* block_table, int32_t max_blocks_per_seq,
+                             int32_t num_seqs, const int32_t* token_seq,
+                             const int32_t* token_pos, int64_t num_tokens, int32_t block_size,
+                             int32_t* slot_mapping, cudaStream_t stream) {
+    if (num_tokens < 0 || block_size <= 0 || max_blocks_per_seq < 0 || num_seqs < 0)
+        return PKV_ERR_INVALID;
+    if (num_tokens == 0) return PKV_OK;
+    if (!token_seq || !token_pos || !slot_mapping) return PKV_ERR_INVALID;
+    if (num_seqs > 0 && max_blocks_per_seq > 0 && !block_table) return PKV_ERR_INVALID;
+    DeviceInfo dev;
+    cudaError_t e = pkv::current_device_info(&dev);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    return cuda_status(pkv::launch_build_slot_mapping(block_table, max_blocks_per_seq, num_seqs,
+                                                      token_seq, token_pos, num_tokens,
+                                                      block_size, slot_mapping, dev.err, stream));
+}
+
+int paged_kv_write(const void* k, const void* v, int32_t kv_dtype, const int32_t* slot_mapping,
+                   int64_t num_tokens, void* k_cache, void* v_cache, const pkv_geom* geom,
+                   cudaStream_t stream) {
+    int st = check_geom(geom);
+    if (st != PKV_OK) return st;
+    if (!elt_size(kv_dtype) || num_tokens < 0) return PKV_ERR_INVALID;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID;
+    DeviceInfo dev;
+    if (pkv::current_device_info(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    const int64_t kv_dim = (int64_t)geom->num_kv_heads * geom->head_dim;
+    const int64_t num_slots = geom->num_blocks * geom->block_size;
+    return cuda_status(pkv::launch_kv_write(k, v, kv_dtype, slot_mapping, num_tokens, k_cache,
+                                            v_cache, geom->dtype, kv_dim, num_slots, dev.err,
+                                            stream));
+}
+
+size_t paged_decode_workspace_size(int32_t batch, const pkv_geom* geom) {
+    if (check_geom(geom) != PKV_OK || batch < 0) return 0;
+    DeviceInfo dev;
+    if (pkv::current_device_info(&dev) != cudaSuccess) return 0;
+    pkv::DecodePlan plan;
+    if (!pkv::plan_decode(dev, batch, geom->num_heads, geom->num_kv_heads, geom->head_dim,
+                          geom->block_size, elt_size(geom->dtype), &plan))
+        return 0;
+    return plan.ws_bytes;
+}
+
+int paged_decode(const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* block_table, int32_t max_blocks_per_seq,
+                 const int32_t* cache_seqlens, int32_t batch, float scale, void* out,
+                 void* workspace, size_t workspace_bytes, const pkv_geom* geom,
+                 cudaStream_t stream) {
+    int st = check_geom(geom);
+    if (st != PKV_OK) return st;
+    if (batch < 0 || max_blocks_per_seq < 0) return PKV_ERR_INVALID;
+    if (batch == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !cache_seqlens || !out)
+        return PKV_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+        return PKV_ERR_INVALID;
+    DeviceInfo dev;
+    if (pkv::current_device_info(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    pkv::DecodePlan plan;
+    if (!pkv::plan_decode(dev, batch, geom->num_heads, geom->num_kv_heads, geom->head_dim,
+                          geom->block_size, elt_size(geom->dtype), &plan))
+        return PKV_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256))
+        return PKV_ERR_WORKSPACE;
+    return cuda_status(pkv::launch_decode(plan, q, k_cache, v_cache, block_table,
+                                          max_blocks_per_seq, cache_seqlens, batch, scale, out,
+                                          workspace, geom->num_heads, geom->num_kv_heads,
+                                          geom->head_dim, geom->block_size, geom->num_blocks,
+                                          geom->dtype, dev.err, stream));
+}
+
+size_t paged_varlen_prefill_workspace_size(int32_t batch, int32_t max_seqlen_q,
+                                           const pkv_geom* geom) {
+    if (check_geom(geom) != PKV_OK || batch < 0 || max_seqlen_q < 0) return 0;
+    return pkv::prefill_workspace_bytes(batch, max_seqlen_q, geom->num_heads);
+}
+
+int paged_varlen_prefill(const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
+                         int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t* block_table,
+                         int32_t max_blocks_per_seq, int32_t causal, float scale, void* out,
+                         void* workspace, size_t workspace_bytes, const pkv_geom* geom,
+                         cudaStream_t stream) {
+    int st = check_geom(geom);
+    if (st != PKV_OK) return st;
+    if (batch < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || max_blocks_per_seq < 0)
+        return PKV_ERR_INVALID;
+    if (batch == 0 || max_seqlen_q == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !block_table || !out)
+        return PKV_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+        return PKV_ERR_INVALID;
+    if (geom->dtype != PKV_BF16 || geom->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    const size_t need = pkv::prefill_workspace_bytes(batch, max_seqlen_q, geom->num_heads);
+    if (need && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
+        return PKV_ERR_WORKSPACE;
+    DeviceInfo dev;
+    if (pkv::current_device_info(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    cudaError_t e = pkv::launch_prefill(
+        dev, q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, max_seqlen_k,
+        block_table, max_blocks_per_seq, causal, scale, out, workspace, geom->num_heads,
+        geom->num_kv_heads, geom->head_dim, geom->block_size, geom->num_blocks, dev.err, stream);
+    if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+    return cuda_status(e);
+}
+
+int paged_error_flags(uint32_t* flags, int32_t clear) {
+    if (!flags) return PKV_ERR_INVALID;
+    DeviceInfo dev;
+    if (pkv::current_device_info(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpy(&v, dev.err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (clear) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(dev.err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return PKV_ERR_CUDA;
+    }
+    *flags = v;
+    return PKV_OK;
+}
+
+const char* paged_status_string(int status) {
+    switch (status) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+        case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+        case PKV_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

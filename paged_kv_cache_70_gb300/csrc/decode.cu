@@ -1,0 +1,564 @@
+// decode.cu -- paged decode (one query token per sequence) for sm_103a.
+//
+// What it computes ("Sayfalı dikkat", decode path; "11. Paged attention 与
+// online softmax" §11.1-§11.2): for sequence b and query head h,
+//   out[b,h] = sum_j softmax_j(scale * q[b,h] . k_j) v_j,  j < cache_seqlens[b],
+// where key j is read from the paged pool through block_table row b
+// (phys = table[j / B], slot = j % B) and blocks are merged with the online
+// rule  m_new = max(m, m_b),  o = o e^(m - m_new) + o_b e^(m_b - m_new),
+// l likewise, out = o / l.
+//
+// GB300 design (HBM-bound: ~1 FMA per K/V byte for GQA group 2):
+//  * Work split.  The keys of every sequence are cut into tiles of R keys
+//    (R divides B, so a tile never crosses a page) and the concatenated tile
+//    list of all sequences is cut into equal contiguous shares, one per CTA
+//    (one CTA per SM).  A CTA therefore covers a piece of one long sequence or
+//    several short ones; each piece yields a partial (m, l, o) state that a
+//    second kernel merges with the same rule.  Load balance is within one tile
+//    whatever the length mix.
+//  * Data movement.  A producer warp streams each tile of K and V (all KV heads
+//    of the CTA; a tile is contiguous in the pool when the CTA owns every KV
+//    head) into a ring of shared-memory stages with cp.async.bulk, tracked by
+//    mbarriers; 5-6 stages of 32 KiB keep ~160 KiB in flight per SM.  The
+//    block-table entry is read once per tile.
+//  * Math.  Eight consumer warps; each warp owns one KV head and its G query
+//    heads (the K/V tile is shared across the GQA group).  Within a warp,
+//    groups of D/16 lanes each take a key row, every lane holding 16 of the D
+//    dimensions of q (pre-scaled by scale*log2 e) and of o; dot products are
+//    reduced with xor shuffles.  Each key updates the state element-wise
+//    (running max; the rescale of o is taken only when the max grows).
+//    Exponentials are base 2 on log2-scaled scores, which is the same merge.
+//  * Safety.  Block ids and lengths are range-checked before any address is
+//    formed; every mbarrier wait is time-limited (PKV_FLAG_TIMEOUT).
+#include <float.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace pkv {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxStages = 8;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DecodeArgs {
+    const void* q;
+    const unsigned char* k_cache;
+    const unsigned char* v_cache;
+    const int32_t* table;
+    const int32_t* seqlens;
+    float* part_o;     // [ctas + batch][hq][D]
+    float* part_ml;    // [ctas + batch][hq][2]
+    int32_t* tstart_out;  // [batch + 1]
+    unsigned int* err;
+    int64_t num_blocks;
+    float qscale;  // scale * log2(e)
+    int32_t max_blocks;
+    int32_t batch;
+    int32_t hq;
+    int32_t hkv;
+    int32_t hc;  // KV heads per CTA
+    int32_t block_size;
+    int32_t rows;  // R
+    int32_t stages;
+};
+
+__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+constexpr size_t kTstartBytes = align_up((kDecodeMaxBatch + 1) * sizeof(int32_t), 128);
+__host__ __device__ constexpr size_t merge_bytes(int G, int D) {
+    return align_up((size_t)kConsumerWarps * G * (D + 2) * sizeof(float), 128);
+}
+__host__ __device__ constexpr size_t decode_fixed_smem(int G, int D) {
+    return 128 + kTstartBytes + merge_bytes(G, D);
+}
+
+// load 8 consecutive elements as fp32
+template <bool BF16>
+__device__ __forceinline__ void load8_smem(const unsigned char* p, float* x) {
+    if constexpr (BF16) {
+        const uint4 w = *reinterpret_cast<const uint4*>(p);
+        x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
+        x[4] = bf16lo(w.z); x[5] = bf16hi(w.z); x[6] = bf16lo(w.w); x[7] = bf16hi(w.w);
+    } else {
+        const float4 a = *reinterpret_cast<const float4*>(p);
+        const float4 b = *reinterpret_cast<const float4*>(p + 16);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void load8_global(const void* base, int64_t elem, float* x) {
+    if constexpr (BF16) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + elem));
+        x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
+        x[4] = bf16lo(w.z); x[5] = bf16hi(w.z); x[6] = bf16lo(w.w); x[7] = bf16hi(w.w);
+    } else {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem);
+        const float4 a = __ldg(p), b = __ldg(p + 1);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
+}
+
+__device__ __forceinline__ int32_t clamp_len(int32_t L, int32_t cap) {
+    return L < 0 ? 0 : (L > cap ? cap : L);
+}
+
+// Exclusive scan of per-sequence tile counts into tstart[0..batch] (all threads).
+__device__ void scan_tiles(const DecodeArgs& a, int32_t* tstart) {
+    __shared__ int32_t warp_tot[kDecodeThreads / 32];
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int per = (a.batch + nthr - 1) / nthr;
+    const int lo = tid * per, hi = min(lo + per, a.batch);
+    const int32_t cap = a.max_blocks * a.block_size;
+    int32_t sum = 0;
+    for (int b = lo; b < hi; ++b) {
+        const int32_t L = clamp_len(a.seqlens[b], cap);
+        sum += (L + a.rows - 1) / a.rows;
+    }
+    // inclusive warp scan of the per-thread sums
+    const int lane = tid & 31, warp = tid >> 5;
+    int32_t inc = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += y;
+    }
+    if (lane == 31) warp_tot[warp] = inc;
+    __syncthreads();
+    int32_t base = 0;
+    for (int w = 0; w < warp; ++w) base += warp_tot[w];
+    int32_t run = base + inc - sum;  // exclusive prefix of this thread's first sequence
+    for (int b = lo; b < hi; ++b) {
+        tstart[b] = run;
+        const int32_t L = clamp_len(a.seqlens[b], cap);
+        run += (L + a.rows - 1) / a.rows;
+    }
+    if (tid == nthr - 1) tstart[a.batch] = base + inc;
+}
+
+// the sequence b with tstart[b] <= t < tstart[b+1]
+__device__ __forceinline__ int seq_of_tile(const int32_t* tstart, int batch, int32_t t) {
+    int lo = 0, hi = batch;  // first index in [0, batch] with tstart[idx] > t
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (tstart[mid] <= t) lo = mid + 1; else hi = mid;
+    }
+    return lo - 1;
+}
+
+template <int D, bool BF16, int G>
+__global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const DecodeArgs a) {
+    constexpr int ELT = BF16 ? 2 : 4;
+    constexpr int TG = D / 16;    // lanes per key row
+    constexpr int GPW = 32 / TG;  // key rows processed side by side by a warp
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kMaxStages;
+    int32_t* tstart = reinterpret_cast<int32_t*>(smem + 128);
+    float* mscratch = reinterpret_cast<float*>(smem + 128 + kTstartBytes);
+    unsigned char* stage_base = smem + decode_fixed_smem(G, D);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = a.stages, R = a.rows, HC = a.hc;
+    const size_t row_bytes = (size_t)HC * D * ELT;         // one key row of the CTA's heads
+    const size_t half_bytes = (size_t)R * row_bytes;       // K (or V) part of a stage
+    const int32_t cap = a.max_blocks * a.block_size;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    scan_tiles(a, tstart);
+    __syncthreads();
+
+    const int32_t total = tstart[a.batch];
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+        for (int b = threadIdx.x; b <= a.batch; b += blockDim.x) a.tstart_out[b] = tstart[b];
+        for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
+            const int32_t L = a.seqlens[b];
+            if (L < 0 || L > cap) flag_error(a.err, PKV_FLAG_BAD_LENGTH);
+        }
+    }
+    if (total == 0) return;
+    const int32_t chunk = (total + gridDim.x - 1) / gridDim.x;
+    const int32_t t0 = blockIdx.x * chunk;
+    const int32_t t1 = min(t0 + chunk, total);
+    if (t0 >= t1) return;
+    const int head0 = blockIdx.y * HC;  // first KV head of this CTA
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------ producer ------------------------------
+        if (lane != 0) return;
+        const uint64_t pol = l2_evict_first_policy();
+        int b = seq_of_tile(tstart, a.batch, t0);
+        int32_t L = clamp_len(a.seqlens[b], cap);
+        for (int32_t t = t0, k = 0; t < t1; ++t, ++k) {
+            while (t >= tstart[b + 1]) {
+                ++b;
+                L = clamp_len(a.seqlens[b], cap);
+            }
+            const int s = k % S;
+            if (!mbar_wait(&empty[s], ((k / S) & 1) ^ 1, a.err)) return;
+            const int32_t pos0 = (t - tstart[b]) * R;
+            const int32_t rows = min(R, L - pos0);
+            const int32_t phys = a.table[(int64_t)b * a.max_blocks + pos0 / a.block_size];
+            if (phys < 0 || phys >= a.num_blocks) {
+                flag_error(a.err, PKV_FLAG_BAD_BLOCK);
+                mbar_arrive(&full[s]);
+                continue;
+            }
+            const int64_t row0 = (int64_t)phys * a.block_size + pos0 % a.block_size;
+            unsigned char* kd = stage_base + (size_t)s * 2 * half_bytes;
+            unsigned char* vd = kd + half_bytes;
+            const uint32_t bytes = (uint32_t)(rows * row_bytes);
+            mbar_arrive_expect_tx(&full[s], 2 * bytes);
+            if (HC == a.hkv) {
+                const size_t off = (size_t)row0 * row_bytes;
+                bulk_g2s(kd, a.k_cache + off, bytes, &full[s], pol);
+                bulk_g2s(vd, a.v_cache + off, bytes, &full[s], pol);
+            } else {
+                const size_t pool_row = (size_t)a.hkv * D * ELT;
+                for (int r = 0; r < rows; ++r) {
+                    const size_t off = (size_t)(row0 + r) * pool_row + (size_t)head0 * D * ELT;
+                    bulk_g2s(kd + r * row_bytes, a.k_cache + off, (uint32_t)row_bytes, &full[s], pol);
+                    bulk_g2s(vd + r * row_bytes, a.v_cache + off, (uint32_t)row_bytes, &full[s], pol);
+                }
+            }
+        }
+        return;
+    }
+
+    // ------------------------------- consumers --------------------------------
+    const int hc = warp % HC;          // local KV head of this warp
+    const int wrank = warp / HC;       // rank among the warps sharing this head
+    const int WH = kConsumerWarps / HC;
+    const int grp = lane / TG, tl = lane % TG;
+    const int row_first = wrank * GPW + grp;
+    const int row_step = WH * GPW;
+    const int kvh = head0 + hc;
+    // this lane's dimensions: [c*TG*8 + tl*8, +8) for c = 0, 1
+    const int dim0 = tl * 8, dim1 = TG * 8 + tl * 8;
+
+    float qf[G][16], o[G][16], m[G], l[G];
+    int b = seq_of_tile(tstart, a.batch, t0);
+    int loaded = -1;
+    int32_t L = 0;
+
+    for (int32_t t = t0, k = 0; t < t1; ++t, ++k) {
+        while (t >= tstart[b + 1]) ++b;
+        if (b != loaded) {
+            loaded = b;
+            L = clamp_len(a.seqlens[b], cap);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const int64_t qb = ((int64_t)b * a.hq + (int64_t)kvh * G + g) * D;
+                load8_global<BF16>(a.q, qb + dim0, &qf[g][0]);
+                load8_global<BF16>(a.q, qb + dim1, &qf[g][8]);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    qf[g][e] *= a.qscale;
+                    o[g][e] = 0.f;
+                }
+                m[g] = -INFINITY;
+                l[g] = 0.f;
+            }
+        }
+        const int s = k % S;
+        if (!mbar_wait(&full[s], (k / S) & 1, a.err)) return;
+        const int32_t pos0 = (t - tstart[b]) * R;
+        const int32_t rows = min(R, L - pos0);
+        const int32_t phys = a.table[(int64_t)b * a.max_blocks + pos0 / a.block_size];
+        if (phys >= 0 && phys < a.num_blocks) {
+            const unsigned char* ks = stage_base + (size_t)s * 2 * half_bytes;
+            const unsigned char* vs = ks + half_bytes;
+            // warp-uniform loop: the warp continues while its first group has a row
+            for (int r = row_first; r - grp < rows; r += row_step) {
+                const bool valid = r < rows;
+                const int rr = valid ? r : rows - 1;
+                const unsigned char* kr = ks + ((size_t)rr * HC + hc) * D * ELT;
+                float kx[16];
+                load8_smem<BF16>(kr + dim0 * ELT, &kx[0]);
+                load8_smem<BF16>(kr + dim1 * ELT, &kx[8]);
+                float sc[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        s0 = fmaf(qf[g][e], kx[e], s0);
+                        s1 = fmaf(qf[g][8 + e], kx[8 + e], s1);
+                    }
+                    sc[g] = s0 + s1;
+                }
+#pragma unroll
+                for (int off = 1; off < TG; off <<= 1)
+#pragma unroll
+                    for (int g = 0; g < G; ++g) sc[g] += __shfl_xor_sync(0xffffffffu, sc[g], off);
+                if (valid) {
+                    const unsigned char* vr = vs + ((size_t)rr * HC + hc) * D * ELT;
+                    float vx[16];
+                    load8_smem<BF16>(vr + dim0 * ELT, &vx[0]);
+                    load8_smem<BF16>(vr + dim1 * ELT, &vx[8]);
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        if (sc[g] > m[g]) {  // running max grows: rescale the state
+                            const float c = ex2(m[g] - sc[g]);
+                            l[g] *= c;
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) o[g][e] *= c;
+                            m[g] = sc[g];
+                        }
+                        const float p = ex2(sc[g] - m[g]);
+                        l[g] += p;
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) o[g][e] = fmaf(p, vx[e], o[g][e]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+
+        // end of this CTA's piece of sequence b: merge and store the partial state
+        const bool seg_end = (t + 1 == t1) || (t + 1 >= tstart[b + 1]);
+        if (!seg_end) continue;
+        // merge the groups of the warp (lanes with equal tl hold the same dims)
+#pragma unroll
+        for (int off = TG; off < 32; off <<= 1) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float mo = __shfl_xor_sync(0xffffffffu, m[g], off);
+                const float lo = __shfl_xor_sync(0xffffffffu, l[g], off);
+                const float M = fmaxf(m[g], mo);
+                const float ca = (m[g] == -INFINITY) ? 0.f : ex2(m[g] - M);
+                const float cb = (mo == -INFINITY) ? 0.f : ex2(mo - M);
+                l[g] = l[g] * ca + lo * cb;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float oo = __shfl_xor_sync(0xffffffffu, o[g][e], off);
+                    o[g][e] = o[g][e] * ca + oo * cb;
+                }
+                m[g] = M;
+            }
+        }
+        if (WH > 1) {  // several warps share this KV head: merge through shared memory
+            float* my = mscratch + (size_t)warp * G * (D + 2);
+            if (grp == 0) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        my[g * (D + 2) + dim0 + e] = o[g][e];
+                        my[g * (D + 2) + dim1 + e] = o[g][8 + e];
+                    }
+                    if (tl == 0) {
+                        my[g * (D + 2) + D] = m[g];
+                        my[g * (D + 2) + D + 1] = l[g];
+                    }
+                }
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+            if (wrank == 0) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float M = -INFINITY;
+                    for (int w = 0; w < WH; ++w)
+                        M = fmaxf(M, mscratch[(size_t)(w * HC + hc) * G * (D + 2) + g * (D + 2) + D]);
+                    float lt = 0.f, ot[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) ot[e] = 0.f;
+                    for (int w = 0; w < WH; ++w) {
+                        const float* src = mscratch + (size_t)(w * HC + hc) * G * (D + 2) + g * (D + 2);
+                        const float mw = src[D];
+                        const float c = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+                        lt += src[D + 1] * c;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            ot[e] += src[dim0 + e] * c;
+                            ot[8 + e] += src[dim1 + e] * c;
+                        }
+                    }
+                    m[g] = M;
+                    l[g] = lt;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) o[g][e] = ot[e];
+                }
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+        }
+        if (wrank == 0 && grp == 0) {
+            const int64_t slot = (int64_t)blockIdx.x + b;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const int64_t qh = (int64_t)kvh * G + g;
+                float* dst = a.part_o + (slot * a.hq + qh) * D;
+                *reinterpret_cast<float4*>(dst + dim0) = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
+                *reinterpret_cast<float4*>(dst + dim0 + 4) = make_float4(o[g][4], o[g][5], o[g][6], o[g][7]);
+                *reinterpret_cast<float4*>(dst + dim1) = make_float4(o[g][8], o[g][9], o[g][10], o[g][11]);
+                *reinterpret_cast<float4*>(dst + dim1 + 4) = make_float4(o[g][12], o[g][13], o[g][14], o[g][15]);
+                if (tl == 0) {
+                    a.part_ml[(slot * a.hq + qh) * 2 + 0] = m[g];
+                    a.part_ml[(slot * a.hq + qh) * 2 + 1] = l[g];
+                }
+            }
+        }
+        loaded = -1;  // the next tile starts a new piece (re-load q, reset state)
+    }
+}
+
+// Merge the partial states of every sequence and normalise.  One CTA per
+// sequence; thread i handles 4 consecutive output elements of [hq][D].
+template <bool BF16>
+__global__ void decode_combine_kernel(const float* __restrict__ part_o,
+                                      const float* __restrict__ part_ml,
+                                      const int32_t* __restrict__ tstart, int32_t batch, int ctas,
+                                      int hq, int D, void* __restrict__ out) {
+    const int b = blockIdx.x;
+    const int32_t total = tstart[batch];
+    const int32_t tb0 = tstart[b], tb1 = tstart[b + 1];
+    const int n4 = hq * D / 4;
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const int h = (i * 4) / D;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float lt = 0.f;
+        if (tb1 > tb0) {
+            const int32_t chunk = (total + ctas - 1) / ctas;
+            const int c0 = tb0 / chunk, c1 = (tb1 - 1) / chunk;
+            float M = -INFINITY;
+            for (int c = c0; c <= c1; ++c) M = fmaxf(M, part_ml[(((int64_t)c + b) * hq + h) * 2]);
+            if (M != -INFINITY) {
+                for (int c = c0; c <= c1; ++c) {
+                    const int64_t slot = (int64_t)c + b;
+                    const float mc = part_ml[(slot * hq + h) * 2];
+                    const float w = (mc == -INFINITY) ? 0.f : ex2(mc - M);
+                    lt += part_ml[(slot * hq + h) * 2 + 1] * w;
+                    const float4 oc = *reinterpret_cast<const float4*>(part_o + slot * hq * D + i * 4);
+                    acc.x += oc.x * w; acc.y += oc.y * w; acc.z += oc.z * w; acc.w += oc.w * w;
+                }
+            }
+        }
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        const float r0 = acc.x * inv, r1 = acc.y * inv, r2 = acc.z * inv, r3 = acc.w * inv;
+        const int64_t oi = (int64_t)b * hq * D + (int64_t)i * 4;
+        if constexpr (BF16) {
+            uint2 pk = make_uint2(pack_bf16x2(r0, r1), pack_bf16x2(r2, r3));
+            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + oi) = pk;
+        } else {
+            *reinterpret_cast<float4*>(static_cast<float*>(out) + oi) = make_float4(r0, r1, r2, r3);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+static int largest_pow2_divisor(int x, int cap) {
+    int r = 1;
+    while (r * 2 <= cap && x % (r * 2) == 0) r *= 2;
+    return r;
+}
+
+bool plan_decode(const DeviceInfo& dev, int32_t batch, int hq, int hkv, int d, int block_size,
+                 int elt, DecodePlan* p) {
+    if (d != 64 && d != 128) return false;
+    if (hkv <= 0 || hq % hkv) return false;
+    const int G = hq / hkv;
+    if (G != 1 && G != 2 && G != 4) return false;
+    if (batch < 0 || batch > kDecodeMaxBatch) return false;
+    int HC;
+    if (hkv <= kConsumerWarps) {
+        if (kConsumerWarps % hkv) return false;
+        HC = hkv;
+    } else {
+        if (hkv % kConsumerWarps) return false;
+        HC = kConsumerWarps;
+    }
+    const size_t row_bytes = (size_t)HC * d * elt;
+    // ~32 KiB of K+V per stage
+    int cap_rows = (int)(32768 / (2 * row_bytes));
+    if (cap_rows < 1) cap_rows = 1;
+    if (cap_rows > 32) cap_rows = 32;
+    const int R = largest_pow2_divisor(block_size, cap_rows);
+    const size_t stage = 2 * (size_t)R * row_bytes;
+    const size_t fixed = decode_fixed_smem(G, d);
+    if (dev.max_smem_optin < fixed + 2 * stage) return false;
+    int stages = (int)((dev.max_smem_optin - fixed) / stage);
+    if (stages > kMaxStages) stages = kMaxStages;
+    p->heads_per_cta = HC;
+    p->head_groups = hkv / HC;
+    p->ctas = dev.num_sms / p->head_groups > 0 ? dev.num_sms / p->head_groups : 1;
+    p->rows_per_tile = R;
+    p->stages = stages;
+    p->smem_bytes = fixed + (size_t)stages * stage;
+    const size_t slots = (size_t)p->ctas + batch;
+    p->ws_bytes = align_up((size_t)(batch + 1) * 4, 256) + align_up(slots * hq * 2 * 4, 256) +
+                  align_up(slots * hq * d * 4, 256);
+    return true;
+}
+
+template <int D, bool BF16, int G>
+static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a, void* out,
+                                   cudaStream_t stream) {
+    auto kern = decode_split_kernel<D, BF16, G>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)plan.smem_bytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(plan.ctas, plan.head_groups);
+    kern<<<grid, kDecodeThreads, plan.smem_bytes, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    decode_combine_kernel<BF16><<<a.batch, 256, 0, stream>>>(a.part_o, a.part_ml, a.tstart_out,
+                                                             a.batch, plan.ctas, a.hq, D, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_cache,
+                          const void* v_cache, const int32_t* block_table, int32_t max_blocks,
+                          const int32_t* cache_seqlens, int32_t batch, float scale, void* out,
+                          void* workspace, int hq, int hkv, int d, int block_size,
+                          int64_t num_blocks, int dtype, unsigned int* err, cudaStream_t stream) {
+    if (batch == 0) return cudaSuccess;
+    DecodeArgs a;
+    a.q = q;
+    a.k_cache = static_cast<const unsigned char*>(k_cache);
+    a.v_cache = static_cast<const unsigned char*>(v_cache);
+    a.table = block_table;
+    a.seqlens = cache_seqlens;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    const size_t slots = (size_t)plan.ctas + batch;
+    a.tstart_out = reinterpret_cast<int32_t*>(ws);
+    ws += align_up((size_t)(batch + 1) * 4, 256);
+    a.part_ml = reinterpret_cast<float*>(ws);
+    ws += align_up(slots * hq * 2 * 4, 256);
+    a.part_o = reinterpret_cast<float*>(ws);
+    a.err = err;
+    a.num_blocks = num_blocks;
+    a.qscale = scale * kLog2e;
+    a.max_blocks = max_blocks;
+    a.batch = batch;
+    a.hq = hq;
+    a.hkv = hkv;
+    a.hc = plan.heads_per_cta;
+    a.block_size = block_size;
+    a.rows = plan.rows_per_tile;
+    a.stages = plan.stages;
+    const int G = hq / hkv;
+    const bool bf = dtype == PKV_BF16;
+#define PKV_DECODE_CASE(DD, BB, GG) \
+    if (d == DD && bf == BB && G == GG) return launch_decode_t<DD, BB, GG>(plan, a, out, stream);
+    PKV_DECODE_CASE(128, true, 1) PKV_DECODE_CASE(128, true, 2) PKV_DECODE_CASE(128, true, 4)
+    PKV_DECODE_CASE(128, false, 1) PKV_DECODE_CASE(128, false, 2) PKV_DECODE_CASE(128, false, 4)
+    PKV_DECODE_CASE(64, true, 1) PKV_DECODE_CASE(64, true, 2) PKV_DECODE_CASE(64, true, 4)
+    PKV_DECODE_CASE(64, false, 1) PKV_DECODE_CASE(64, false, 2) PKV_DECODE_CASE(64, false, 4)
+#undef PKV_DECODE_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv

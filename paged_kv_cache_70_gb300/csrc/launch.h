@@ -1,0 +1,68 @@
+// launch.h -- internal host-side launchers of libpagedkv's kernels.  The C ABI
+// layer (api.cu) validates arguments before calling any of these; each returns
+// the cudaError_t of its launch(es).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    size_t max_smem_optin;
+    unsigned int* err;  // device address of this device's error word
+};
+
+// Looks up (once per device) the SM count, shared-memory limit and the error
+// word's device address of the current device.
+cudaError_t current_device_info(DeviceInfo* info);
+
+cudaError_t launch_build_slot_mapping(const int32_t* block_table, int32_t max_blocks,
+                                      int32_t num_seqs, const int32_t* token_seq,
+                                      const int32_t* token_pos, int64_t num_tokens,
+                                      int32_t block_size, int32_t* slot_mapping,
+                                      unsigned int* err, cudaStream_t stream);
+
+cudaError_t launch_kv_write(const void* k, const void* v, int src_dtype, const int32_t* slots,
+                            int64_t num_tokens, void* k_cache, void* v_cache, int cache_dtype,
+                            int64_t kv_dim, int64_t num_slots, unsigned int* err,
+                            cudaStream_t stream);
+
+// ---- decode -----------------------------------------------------------------
+struct DecodePlan {
+    int heads_per_cta;   // KV heads one CTA handles (HC)
+    int head_groups;     // grid.y = Hkv / HC
+    int ctas;            // grid.x (CTAs along the key axis)
+    int rows_per_tile;   // R: keys per pipeline stage (divides block_size)
+    int stages;          // pipeline depth
+    size_t smem_bytes;   // dynamic shared memory per CTA
+    size_t ws_bytes;     // workspace bytes needed
+};
+
+constexpr int kDecodeMaxBatch = 4096;
+
+// Returns false when the geometry is not supported.
+bool plan_decode(const DeviceInfo& dev, int32_t batch, int hq, int hkv, int d, int block_size,
+                 int elt, DecodePlan* plan);
+
+cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_cache,
+                          const void* v_cache, const int32_t* block_table, int32_t max_blocks,
+                          const int32_t* cache_seqlens, int32_t batch, float scale, void* out,
+                          void* workspace, int hq, int hkv, int d, int block_size,
+                          int64_t num_blocks, int dtype, unsigned int* err, cudaStream_t stream);
+
+// ---- prefill ----------------------------------------------------------------
+size_t prefill_workspace_bytes(int32_t batch, int32_t max_seqlen_q, int hq);
+
+cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_cache,
+                           const void* v_cache, const int32_t* cu_q, const int32_t* cu_k,
+                           int32_t batch, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                           const int32_t* block_table, int32_t max_blocks, int causal,
+                           float scale, void* out, void* workspace, int hq, int hkv, int d,
+                           int block_size, int64_t num_blocks, unsigned int* err,
+                           cudaStream_t stream);
+
+}  // namespace pkv

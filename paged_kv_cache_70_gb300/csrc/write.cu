@@ -1,0 +1,186 @@
+// write.cu -- slot_mapping construction and the paged KV-cache write.
+//
+// "从零开始写Qwen3（六）PagedAttention", section "自己来实现一个": the slot of
+// every new token is computed once per step (shared by all layers), then each
+// token's K and V rows are copied to cache[slot * kvDim ...] with a cast to the
+// cache dtype; a negative slot is skipped.  Addressing follows
+// "11. Paged attention 与 online softmax" §11.1 (slot = table[p/B]*B + p%B).
+//
+// GB300 layout of the write: one warp per token row; each lane moves 16-byte
+// vectors of the K row and of the V row (2 KiB rows for Hkv=8, d=128, bf16), so
+// a warp issues fully coalesced 512-byte transactions.  The kernel is HBM-bound
+// (2 * kvDim * elt bytes read and written per token).
+#include "common.cuh"
+#include "launch.h"
+
+namespace pkv {
+
+__global__ void build_slot_mapping_kernel(const int32_t* __restrict__ table, int32_t max_blocks,
+                                          int32_t num_seqs, const int32_t* __restrict__ token_seq,
+                                          const int32_t* __restrict__ token_pos,
+                                          int64_t num_tokens, int32_t block_size,
+                                          int32_t* __restrict__ slots, unsigned int* err) {
+    int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (n >= num_tokens) return;
+    const int32_t s = token_seq[n];
+    const int32_t p = token_pos[n];
+    int32_t out = -1;
+    if (s >= 0) {
+        if (s >= num_seqs) {
+            flag_error(err, PKV_FLAG_BAD_SEQ);
+        } else if (p < 0 || p / block_size >= max_blocks) {
+            flag_error(err, PKV_FLAG_BAD_LENGTH);
+        } else {
+            const int32_t phys = table[(int64_t)s * max_blocks + p / block_size];
+            if (phys < 0) {
+                flag_error(err, PKV_FLAG_BAD_BLOCK);
+            } else {
+                out = phys * block_size + p % block_size;
+            }
+        }
+    }
+    slots[n] = out;
+}
+
+cudaError_t launch_build_slot_mapping(const int32_t* block_table, int32_t max_blocks,
+                                      int32_t num_seqs, const int32_t* token_seq,
+                                      const int32_t* token_pos, int64_t num_tokens,
+                                      int32_t block_size, int32_t* slot_mapping,
+                                      unsigned int* err, cudaStream_t stream) {
+    if (num_tokens == 0) return cudaSuccess;
+    const int threads = 256;
+    const int64_t blocks = (num_tokens + threads - 1) / threads;
+    build_slot_mapping_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
+        block_table, max_blocks, num_seqs, token_seq, token_pos, num_tokens, block_size,
+        slot_mapping, err);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// write kernels
+// ---------------------------------------------------------------------------
+constexpr int kWriteWarps = 8;
+
+// equal dtypes: 16-byte vector copy of row_bytes (a multiple of 16)
+__global__ void __launch_bounds__(kWriteWarps * 32)
+kv_write_copy_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                     const int32_t* __restrict__ slots, int64_t num_tokens,
+                     uint4* __restrict__ kc, uint4* __restrict__ vc, int64_t vec_per_row,
+                     int64_t num_slots, unsigned int* err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t n = (int64_t)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
+    if (n >= num_tokens) return;
+    const int32_t s = __ldg(slots + n);
+    if (s < 0) return;
+    if (s >= num_slots) {
+        if (lane == 0) flag_error(err, PKV_FLAG_BAD_SLOT);
+        return;
+    }
+    const uint4* ks = k + n * vec_per_row;
+    const uint4* vs = v + n * vec_per_row;
+    uint4* kd = kc + (int64_t)s * vec_per_row;
+    uint4* vd = vc + (int64_t)s * vec_per_row;
+    for (int64_t i = lane; i < vec_per_row; i += 32) {
+        const uint4 a = __ldcs(ks + i);
+        const uint4 b = __ldcs(vs + i);
+        kd[i] = a;
+        vd[i] = b;
+    }
+}
+
+// fp32 source -> bf16 cache (round to nearest even); groups of 8 elements
+__global__ void __launch_bounds__(kWriteWarps * 32)
+kv_write_f32_to_bf16_kernel(const float4* __restrict__ k, const float4* __restrict__ v,
+                            const int32_t* __restrict__ slots, int64_t num_tokens,
+                            uint4* __restrict__ kc, uint4* __restrict__ vc, int64_t groups8,
+                            int64_t num_slots, unsigned int* err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t n = (int64_t)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
+    if (n >= num_tokens) return;
+    const int32_t s = __ldg(slots + n);
+    if (s < 0) return;
+    if (s >= num_slots) {
+        if (lane == 0) flag_error(err, PKV_FLAG_BAD_SLOT);
+        return;
+    }
+    for (int64_t i = lane; i < groups8; i += 32) {
+        const float4 a0 = __ldcs(k + (n * groups8 + i) * 2);
+        const float4 a1 = __ldcs(k + (n * groups8 + i) * 2 + 1);
+        const float4 b0 = __ldcs(v + (n * groups8 + i) * 2);
+        const float4 b1 = __ldcs(v + (n * groups8 + i) * 2 + 1);
+        kc[(int64_t)s * groups8 + i] = make_uint4(pack_bf16x2(a0.x, a0.y), pack_bf16x2(a0.z, a0.w),
+                                                  pack_bf16x2(a1.x, a1.y), pack_bf16x2(a1.z, a1.w));
+        vc[(int64_t)s * groups8 + i] = make_uint4(pack_bf16x2(b0.x, b0.y), pack_bf16x2(b0.z, b0.w),
+                                                  pack_bf16x2(b1.x, b1.y), pack_bf16x2(b1.z, b1.w));
+    }
+}
+
+// generic element-wise path: any kvDim, any dtype pair
+__global__ void kv_write_scalar_kernel(const void* __restrict__ k, const void* __restrict__ v,
+                                       int src_dtype, const int32_t* __restrict__ slots,
+                                       int64_t num_tokens, void* __restrict__ kc,
+                                       void* __restrict__ vc, int cache_dtype, int64_t kv_dim,
+                                       int64_t num_slots, unsigned int* err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t n = (int64_t)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
+    if (n >= num_tokens) return;
+    const int32_t s = slots[n];
+    if (s < 0) return;
+    if (s >= num_slots) {
+        if (lane == 0) flag_error(err, PKV_FLAG_BAD_SLOT);
+        return;
+    }
+    for (int64_t j = lane; j < kv_dim; j += 32) {
+        const int64_t si = n * kv_dim + j, di = (int64_t)s * kv_dim + j;
+        float a, b;
+        if (src_dtype == PKV_F32) {
+            a = static_cast<const float*>(k)[si];
+            b = static_cast<const float*>(v)[si];
+        } else {
+            a = __uint_as_float((uint32_t) static_cast<const uint16_t*>(k)[si] << 16);
+            b = __uint_as_float((uint32_t) static_cast<const uint16_t*>(v)[si] << 16);
+        }
+        if (cache_dtype == PKV_F32) {
+            static_cast<float*>(kc)[di] = a;
+            static_cast<float*>(vc)[di] = b;
+        } else if (src_dtype == PKV_BF16) {  // bf16 -> bf16: bit copy
+            static_cast<uint16_t*>(kc)[di] = static_cast<const uint16_t*>(k)[si];
+            static_cast<uint16_t*>(vc)[di] = static_cast<const uint16_t*>(v)[si];
+        } else {
+            static_cast<uint16_t*>(kc)[di] = f32_to_bf16_bits(a);
+            static_cast<uint16_t*>(vc)[di] = f32_to_bf16_bits(b);
+        }
+    }
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaError_t launch_kv_write(const void* k, const void* v, int src_dtype, const int32_t* slots,
+                            int64_t num_tokens, void* k_cache, void* v_cache, int cache_dtype,
+                            int64_t kv_dim, int64_t num_slots, unsigned int* err,
+                            cudaStream_t stream) {
+    if (num_tokens == 0) return cudaSuccess;
+    const int64_t grid = (num_tokens + kWriteWarps - 1) / kWriteWarps;
+    const int threads = kWriteWarps * 32;
+    const bool all_aligned = aligned16(k) && aligned16(v) && aligned16(k_cache) &&
+                             aligned16(v_cache);
+    const int src_elt = src_dtype == PKV_F32 ? 4 : 2;
+    if (all_aligned && src_dtype == cache_dtype && (kv_dim * src_elt) % 16 == 0) {
+        kv_write_copy_kernel<<<(unsigned)grid, threads, 0, stream>>>(
+            static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens,
+            static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), kv_dim * src_elt / 16,
+            num_slots, err);
+    } else if (all_aligned && src_dtype == PKV_F32 && cache_dtype == PKV_BF16 && kv_dim % 8 == 0) {
+        kv_write_f32_to_bf16_kernel<<<(unsigned)grid, threads, 0, stream>>>(
+            static_cast<const float4*>(k), static_cast<const float4*>(v), slots, num_tokens,
+            static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), kv_dim / 8, num_slots,
+            err);
+    } else {
+        kv_write_scalar_kernel<<<(unsigned)grid, threads, 0, stream>>>(
+            k, v, src_dtype, slots, num_tokens, k_cache, v_cache, cache_dtype, kv_dim, num_slots,
+            err);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

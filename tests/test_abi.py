@@ -1,0 +1,67 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/pagedkv.h declares; host-side argument checks answer without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_70_gb300 as pkv
+from paged_kv_cache_70_gb300 import build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "pagedkv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\s*\*)\s+(\w+)\s*\(", text,
+                                 flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return pkv.load_library()
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for n in ("paged_kv_write", "paged_decode", "paged_varlen_prefill",
+              "paged_build_slot_mapping"):
+        assert n in names
+    assert set(names) == set(pkv.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert lib.paged_status_string(0) == b"ok"
+    assert lib.paged_status_string(-1) == b"invalid argument"
+    assert lib.paged_status_string(-3) == b"workspace missing or too small"
+
+
+def test_host_side_argument_checks(lib):
+    """Checks that fail before any CUDA call (no GPU needed)."""
+    g = pkv.Geom(16, 8, 128, 16, 100, pkv.PKV_BF16)
+    assert lib.paged_kv_write(None, None, 1, None, 1, None, None, None, None) == -1
+    bad = pkv.Geom(16, 6, 128, 16, 100, pkv.PKV_BF16)  # Hq % Hkv != 0
+    assert lib.paged_kv_write(None, None, 1, None, 1, None, None, ctypes.byref(bad), None) == -1
+    assert lib.paged_kv_write(None, None, 1, None, 0, None, None, ctypes.byref(g), None) == 0
+    assert lib.paged_decode(None, None, None, None, 4, None, 0, 1.0, None, None, 0,
+                            ctypes.byref(g), None) == 0  # empty batch
+    assert lib.paged_decode(None, None, None, None, 4, None, 2, 1.0, None, None, 0,
+                            ctypes.byref(g), None) == -1
+    assert lib.paged_build_slot_mapping(None, 4, 1, None, None, -1, 16, None, None) == -1
+    assert lib.paged_varlen_prefill_workspace_size(4, 100, None) == 0
+    huge = pkv.Geom(16, 8, 128, 256, 1 << 24, pkv.PKV_BF16)  # 2^32 slots > int32
+    assert lib.paged_kv_write(None, None, 1, None, 1, None, None, ctypes.byref(huge), None) == -2
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="not found"):
+        pkv.load_library(str(tmp_path / "missing.so"))

@@ -1,0 +1,163 @@
+"""GPU parity of paged decode (block-table reads + online-softmax merge +
+split-KV combine) against the fp64 oracle, through the C ABI."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_70_gb300 as pkv
+from paged_kv_cache_70_gb300 import workloads as W
+from gpu_helpers import DevStep, assert_close, oracle_write, to_dev, to_host, widen
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+@pytest.fixture(autouse=True)
+def _clear_flags():
+    pkv.paged_error_flags(clear=True)
+    yield
+
+
+def _oracle_decode(step, kc, vc):
+    return oracle.decode(step.q_decode, kc, vc, step.decode_table, step.cache_seqlens, step.scale)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 5])
+def test_config_step(cfg):
+    """The workload's step: write the new tokens, then decode over L+1 keys."""
+    step = W.config(cfg)
+    dev = DevStep(step)
+    dev.write()
+    out = dev.decode()
+    torch.cuda.synchronize()
+    _, kc, vc = oracle_write(step)
+    assert np.array_equal(to_host(dev.k_cache), kc)
+    want = _oracle_decode(step, kc, vc)
+    assert_close(widen(out), want, step.dtype, f"cfg{cfg}")
+    assert pkv.paged_error_flags() == 0
+
+
+def test_decode_example_state():
+    """Sayfalı dikkat decode example as printed: cache_seqlens [30,32,70],
+    B=32, table [[2,-1,-1,-1],[0,1,-1,-1],[3,5,6,-1]] (fp32, Hq=2, Hkv=1, d=64)."""
+    g = json.load(open(os.path.join(GOLDEN, "decode_example.json")))
+    rng = np.random.default_rng(1001)
+    kc = rng.standard_normal((8, 32, 1, 64)).astype(np.float32)
+    vc = rng.standard_normal((8, 32, 1, 64)).astype(np.float32)
+    q = rng.standard_normal((3, 2, 64)).astype(np.float32)
+    table = np.array(g["block_table"], np.int32)
+    lens = np.array(g["cache_seqlens"], np.int32)
+    out = pkv.paged_decode(to_dev(q), to_dev(kc), to_dev(vc), to_dev(table), to_dev(lens), 0.125)
+    want = oracle.decode(q, kc, vc, table, lens, 0.125)
+    assert_close(widen(out), want, "f32", "p4 example")
+
+
+CASES = [
+    # (dtype, hq, hkv, d, B, lens)
+    ("bf16", 16, 8, 128, 16, [0, 1, 15, 16, 17, 33, 1000]),
+    ("bf16", 16, 8, 128, 256, [255, 256, 257, 0, 5000]),
+    ("f32", 16, 8, 128, 32, [1, 31, 64, 100]),
+    ("bf16", 8, 8, 128, 64, [3, 130, 700]),        # G = 1
+    ("bf16", 32, 8, 128, 16, [77, 500, 1]),         # G = 4
+    ("f32", 4, 1, 64, 32, [30, 32, 70, 0]),         # Hkv = 1 (warps share a head)
+    ("bf16", 4, 2, 64, 48, [47, 48, 49, 200]),      # B not a power of two
+    ("bf16", 8, 4, 64, 1, [1, 2, 9]),               # B = 1
+    ("f32", 32, 16, 128, 16, [40, 300]),            # Hkv > 8: heads split across CTAs
+    ("bf16", 2, 2, 128, 3, [0, 0, 0]),              # all empty
+    ("bf16", 16, 8, 128, 16, [4096] * 3 + [0] * 500 + [17] * 200),  # many sequences
+]
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,d,B,lens", CASES)
+def test_decode_shapes(dtype, hq, hkv, d, B, lens):
+    step = W.make_step(name="edge", dtype=dtype, hq=hq, hkv=hkv, d=d, block_size=B,
+                       decode_lens=[max(L - 1, 0) for L in lens], seed=sum(lens) + hq + B)
+    step.cache_seqlens = np.asarray(lens, np.int32)  # attend over exactly these lengths
+    dev = DevStep(step)
+    out = dev.decode()
+    torch.cuda.synchronize()
+    want = _oracle_decode(step, step.k_cache, step.v_cache)
+    assert_close(widen(out), want, dtype, str(lens[:6]))
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert torch.count_nonzero(out[b]) == 0
+    assert pkv.paged_error_flags() == 0
+
+
+def test_single_key_returns_v0():
+    step = W.make_step(name="one", dtype="f32", hq=4, hkv=2, d=128, block_size=16,
+                       decode_lens=[0, 0], seed=3)
+    step.cache_seqlens = np.array([1, 1], np.int32)
+    out = DevStep(step).decode()
+    for b in range(2):
+        v0 = step.v_cache[step.table[b, 0], 0]  # [Hkv, d]
+        for h in range(4):
+            assert np.allclose(widen(out)[b, h], v0[h // 2], atol=1e-6, rtol=0)
+
+
+def test_physical_permutation_bitwise():
+    """Moving physical blocks (data + table) leaves the GPU output bit-identical:
+    the reduction order depends only on logical positions."""
+    step = W.config(2)
+    dev = DevStep(step)
+    a = to_host(dev.decode())
+    nb = step.num_blocks
+    perm = np.random.default_rng(9).permutation(nb)
+    inv = np.argsort(perm)
+    dev.k_cache = dev.k_cache[torch.from_numpy(inv).cuda()].contiguous()
+    dev.v_cache = dev.v_cache[torch.from_numpy(inv).cuda()].contiguous()
+    t = step.decode_table
+    dev.decode_table = to_dev(np.where(t >= 0, perm[np.maximum(t, 0)], -1).astype(np.int32))
+    b = to_host(dev.decode())
+    assert np.array_equal(a, b)
+
+
+def test_repeatable_and_out_buffer():
+    step = W.config(3)
+    dev = DevStep(step)
+    a = to_host(dev.decode())
+    out = torch.full_like(dev.q_decode, float("nan"))
+    ws = torch.empty(pkv.paged_decode_workspace_size(step.n_decode, step.hq, dev.k_cache),
+                     dtype=torch.uint8, device="cuda")
+    dev.decode(out=out, workspace=ws)
+    assert np.array_equal(a, to_host(out))
+
+
+def test_bad_block_id_is_flagged_not_read():
+    step = W.make_step(name="bad", dtype="bf16", hq=16, hkv=8, d=128, block_size=16,
+                       decode_lens=[40, 40], seed=5)
+    step.table[1, 1] = step.num_blocks + 1000  # out of range inside the valid length
+    dev = DevStep(step)
+    out = dev.decode()
+    torch.cuda.synchronize()
+    assert pkv.paged_error_flags() & pkv.PKV_FLAG_BAD_BLOCK
+    want = oracle.decode(step.q_decode[:1], step.k_cache, step.v_cache, step.decode_table[:1],
+                         step.cache_seqlens[:1], step.scale)
+    assert_close(widen(out)[:1], want, "bf16", "untouched sequence")
+
+
+def test_length_beyond_table_is_clamped_and_flagged():
+    step = W.make_step(name="long", dtype="bf16", hq=16, hkv=8, d=128, block_size=16,
+                       decode_lens=[20], seed=6, max_blocks=2)
+    step.cache_seqlens = np.array([10_000], np.int32)
+    DevStep(step).decode()
+    torch.cuda.synchronize()
+    assert pkv.paged_error_flags() & pkv.PKV_FLAG_BAD_LENGTH
+
+
+def test_workspace_and_support_errors():
+    step = W.make_step(name="ws", dtype="bf16", hq=16, hkv=8, d=128, block_size=16,
+                       decode_lens=[10], seed=8)
+    dev = DevStep(step)
+    with pytest.raises(pkv.PagedKVError) as e:
+        dev.decode(workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == -3
+    q = torch.zeros(1, 16, 96, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(4, 16, 8, 96, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pkv.PagedKVError) as e:
+        pkv.paged_decode(q, kc, kc, dev.decode_table, dev.cache_seqlens)
+    assert e.value.status == -2
