@@ -167,6 +167,36 @@ int paged_varlen_prefill(const void* q, const void* k_cache, const void* v_cache
                          cudaStream_t stream);
 
 /*
+ * paged_decode_noalloc -- paged_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart: this is a deployment variant of
+ * paged_decode that takes no workspace.
+ * Some callers cannot hand the library a scratch buffer: a plugin whose host
+ * framework owns every device allocation and offers no workspace hook, or a
+ * serving loop that must not call cudaMalloc because it can synchronise the
+ * device and stall other streams.  This call allocates nothing (no cudaMalloc,
+ * no cudaFree, no allocating library routine); its split-KV scratch is a fixed
+ * device array of PKV_NOALLOC_SCRATCH_BYTES inside the library, which every
+ * GPU that loads the library holds until the process exits.
+ *   - Same arguments, layouts, results and support matrix as paged_decode,
+ *     minus workspace / workspace_bytes.
+ *   - Returns PKV_ERR_WORKSPACE when the problem needs more scratch than the
+ *     array holds, i.e. when paged_decode_workspace_size(batch, geom) >
+ *     PKV_NOALLOC_SCRATCH_BYTES (about 1000 sequences for Hq=16, head_dim=128
+ *     on a 152-SM GPU).
+ *   - All calls share the one array, and it keeps the previous call's contents
+ *     (nothing in it needs to start at zero).  Calls that overlap on the GPU
+ *     race on it: order them on one stream or with events.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (8u << 20)
+int paged_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_table, int32_t max_blocks_per_seq,
+                         const int32_t* cache_seqlens, int32_t batch, float scale, void* out,
+                         const pkv_geom* geom, cudaStream_t stream);
+
+/*
  * paged_error_flags -- read (and with clear != 0, reset) the device error word
  * of the current device: an OR of PKV_FLAG_* bits set by kernels since the
  * last clear.  Synchronises with the device.  *flags (host pointer) receives

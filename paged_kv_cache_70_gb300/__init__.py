@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     load_library,
     paged_build_slot_mapping,
     paged_decode,
+    paged_decode_noalloc,
     paged_decode_workspace_size,
     paged_error_flags,
     paged_kv_write,

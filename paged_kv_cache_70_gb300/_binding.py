@@ -35,6 +35,7 @@ EXPORTED = (
     "paged_varlen_prefill",
     "paged_error_flags",
     "paged_status_string",
+    "paged_decode_noalloc",
 )
 
 
@@ -89,6 +90,9 @@ def load_library(path: str | None = None):
         lib.paged_varlen_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp, i32, i32,
                                              ctypes.c_float, vp, vp, sz, gp, vp]
         lib.paged_varlen_prefill.restype = ctypes.c_int
+        lib.paged_decode_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, vp,
+                                             gp, vp]
+        lib.paged_decode_noalloc.restype = ctypes.c_int
         lib.paged_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         lib.paged_error_flags.restype = ctypes.c_int
         lib.paged_status_string.argtypes = [ctypes.c_int]
@@ -206,6 +210,32 @@ def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                               block_table.shape[1], _ptr(cache_seqlens), batch, scale, _ptr(out),
                               _ptr(workspace), workspace.numel(), ctypes.byref(g), _stream(q))
     _check("paged_decode", st)
+    return out
+
+
+def paged_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                         block_table: torch.Tensor, cache_seqlens: torch.Tensor,
+                         scale: float | None = None,
+                         out: torch.Tensor | None = None) -> torch.Tensor:
+    """paged_decode without a workspace, for callers that cannot allocate
+    device memory: the library's built-in scratch array is used instead (see
+    include/pagedkv.h; calls that overlap on the GPU race on that array)."""
+    _cuda_contig("q", q, k_cache.dtype)
+    _cuda_contig("k_cache", k_cache)
+    _cuda_contig("v_cache", v_cache, k_cache.dtype)
+    _cuda_contig("block_table", block_table, torch.int32)
+    _cuda_contig("cache_seqlens", cache_seqlens, torch.int32)
+    batch, hq, d = q.shape
+    g = geom_of(k_cache, hq)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, q.dtype)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    with torch.cuda.device(q.device):
+        st = load_library().paged_decode_noalloc(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+            _ptr(cache_seqlens), batch, scale, _ptr(out), ctypes.byref(g), _stream(q))
+    _check("paged_decode_noalloc", st)
     return out
 
 
