@@ -1,0 +1,179 @@
+"""GPU parity of the causal varlen prefill (tcgen05/TMEM, paged K/V through
+the block table) against the fp64 oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_70_gb300 as pkv
+from paged_kv_cache_70_gb300 import workloads as W
+from gpu_helpers import DevStep, assert_close, oracle_write, to_dev, to_host, widen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clear_flags():
+    pkv.paged_error_flags(clear=True)
+    yield
+
+
+def _bf(x):
+    return W._to_dtype(np.asarray(x, np.float32), "bf16")
+
+
+def make_case(qlens, klens, B, hq=16, hkv=8, d=128, seed=0, extra_blocks=3):
+    """Pool + table holding each request's keys (any q/k lengths, k may be < q)."""
+    rng = np.random.default_rng(seed)
+    need = [-(-k // B) for k in klens]
+    nb = sum(need) + extra_blocks
+    order = rng.permutation(nb).astype(np.int32)
+    width = max(need + [1])
+    table = np.full((len(qlens), width), -1, np.int32)
+    nxt = 0
+    for r, n in enumerate(need):
+        table[r, :n] = order[nxt: nxt + n]
+        nxt += n
+    kc = _bf(rng.standard_normal((nb, B, hkv, d)))
+    vc = _bf(rng.standard_normal((nb, B, hkv, d)))
+    cq = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(klens)]).astype(np.int32)
+    q = _bf(rng.standard_normal((int(cq[-1]), hq, d)))
+    return dict(q=q, kc=kc, vc=vc, table=table, cq=cq, ck=ck, B=B, scale=1 / math.sqrt(d))
+
+
+def run_gpu(c, causal=True):
+    return pkv.paged_varlen_prefill(
+        to_dev(c["q"]), to_dev(c["kc"]), to_dev(c["vc"]), to_dev(c["cq"]), to_dev(c["ck"]),
+        int(np.diff(c["cq"]).max()), int(np.diff(c["ck"]).max()), to_dev(c["table"]),
+        causal=causal, scale=c["scale"])
+
+
+def run_oracle(c, causal=True, rows=None):
+    return oracle.prefill(c["q"], c["kc"], c["vc"], c["cq"], c["ck"], c["scale"], causal=causal,
+                          block_table=c["table"], block_size=c["B"], row_subset=rows)
+
+
+def test_varlen_example_lengths():
+    """Sayfalı dikkat varlen example lengths: q [10,3,1], k [0,1,7]; rows that
+    see no key (all of r0, rows 0-1 of r1) are 0."""
+    c = make_case([10, 3, 1], [0, 1, 7], B=16, seed=1)
+    out = run_gpu(c)
+    torch.cuda.synchronize()
+    got = widen(out)
+    assert np.all(got[:12] == 0)
+    assert_close(got, run_oracle(c), "bf16", "varlen example")
+    assert pkv.paged_error_flags() == 0
+
+
+@pytest.mark.parametrize("B", [8, 16, 32, 64, 128, 256, 512])
+def test_block_sizes(B):
+    qlens = [1, 127, 128, 129, 300]
+    cached = [0, 5, 256, 1000 % B + 3, 77]
+    c = make_case(qlens, [q + k for q, k in zip(qlens, cached)], B=B, seed=B)
+    out = run_gpu(c)
+    torch.cuda.synchronize()
+    assert_close(widen(out), run_oracle(c), "bf16", f"B={B}")
+    assert pkv.paged_error_flags() == 0
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (16, 4), (32, 4), (4, 1)])
+def test_gqa_groups(hq, hkv):
+    c = make_case([200, 64], [260, 64], B=64, hq=hq, hkv=hkv, seed=hq * 10 + hkv)
+    assert_close(widen(run_gpu(c)), run_oracle(c), "bf16", f"{hq}/{hkv}")
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_causal_flag(causal):
+    c = make_case([131, 7, 256], [131, 300, 600], B=32, seed=5)
+    assert_close(widen(run_gpu(c, causal)), run_oracle(c, causal), "bf16", str(causal))
+
+
+def test_single_query_equals_decode():
+    """q_len = 1 prefill (causal or not) equals paged decode over the same keys."""
+    lens = [1, 200, 513, 4096]
+    c = make_case([1] * 4, lens, B=16, seed=9)
+    dec = pkv.paged_decode(to_dev(c["q"]), to_dev(c["kc"]), to_dev(c["vc"]), to_dev(c["table"]),
+                           to_dev(np.array(lens, np.int32)), c["scale"])
+    for causal in (True, False):
+        pre = run_gpu(c, causal)
+        torch.cuda.synchronize()
+        err = np.abs(widen(pre) - widen(dec))
+        assert err.max() <= 2e-2 and err.mean() <= 2e-3
+
+
+@pytest.mark.parametrize("cfg", [5, 4])
+def test_config_prefill(cfg):
+    """Workload step: write the new tokens, then prefill.  Workload 5 is
+    compared on every row; workload 4 on sampled rows of every request (tile
+    edges, first/last rows and a stride) and every head."""
+    step = W.config(cfg)
+    dev = DevStep(step)
+    dev.write()
+    out = dev.prefill()
+    torch.cuda.synchronize()
+    _, kc, vc = oracle_write(step)
+    got = widen(out)
+    if cfg == 5:
+        rows = None
+    else:
+        rows = []
+        for r in range(step.n_prefill):
+            a, b = int(step.cu_q[r]), int(step.cu_q[r + 1])
+            cand = {a, b - 1, a + 1, b - 2} | set(range(a, b, 61))
+            cand |= {a + t for t in (127, 128, 255, 256, 1023, 1024) if a + t < b}
+            rows += sorted(x for x in cand if a <= x < b)
+        rows = np.array(rows, np.int32)
+    want = oracle.prefill(step.q_prefill, kc, vc, step.cu_q, step.cu_k, step.scale, causal=True,
+                          block_table=step.prefill_table, block_size=step.block_size,
+                          row_subset=rows)
+    assert_close(got if rows is None else got[rows], want, "bf16", f"cfg{cfg}")
+    assert pkv.paged_error_flags() == 0
+
+
+def test_physical_permutation_bitwise():
+    c = make_case([300, 90], [700, 90], B=16, seed=3)
+    a = to_host(run_gpu(c))
+    nb = c["kc"].shape[0]
+    perm = np.random.default_rng(4).permutation(nb)
+    inv = np.argsort(perm)
+    c2 = dict(c, kc=c["kc"][inv], vc=c["vc"][inv],
+              table=np.where(c["table"] >= 0, perm[np.maximum(c["table"], 0)], -1).astype(np.int32))
+    b = to_host(run_gpu(c2))
+    assert np.array_equal(a, b)
+
+
+def test_nonfinite_pool_padding_is_ignored():
+    """Pool slots past a request's keys hold NaN: they must not leak into the
+    output (p = 0 for those keys)."""
+    c = make_case([50, 3], [70, 3], B=64, seed=11)
+    kc, vc = c["kc"].copy(), c["vc"].copy()
+    for r, k in enumerate([70, 3]):
+        blk = c["table"][r, (k - 1) // 64]
+        kc[blk, k % 64:] = 0x7fc0  # bf16 NaN
+        vc[blk, k % 64:] = 0x7fc0
+    c2 = dict(c, kc=kc, vc=vc)
+    out = widen(run_gpu(c2))
+    assert np.all(np.isfinite(out))
+    assert_close(out, run_oracle(c), "bf16", "nan padding")
+
+
+def test_bad_block_id_is_flagged():
+    c = make_case([40], [300], B=64, seed=12)
+    c["table"][0, 2] = 10_000
+    run_gpu(c)
+    torch.cuda.synchronize()
+    assert pkv.paged_error_flags() & pkv.PKV_FLAG_BAD_BLOCK
+
+
+def test_unsupported_combinations():
+    c = make_case([4], [4], B=16, d=64, seed=1)
+    with pytest.raises(pkv.PagedKVError) as e:
+        run_gpu(c)
+    assert e.value.status == -2
+    c = make_case([4], [4], B=24, seed=1)
+    with pytest.raises(pkv.PagedKVError) as e:
+        run_gpu(c)
+    assert e.value.status == -2
