@@ -44,7 +44,9 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--only", choices=["all", "decode", "prefill"], default="all",
+                   help="measure one half only (profiling runs)")
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
     return p.parse_args()
 
 
@@ -136,7 +138,7 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
@@ -310,6 +312,24 @@ def time_e2e(step, dev: DeviceStep, steps: int, warmup: int, world: int):
     return ms, h2d, d2h
 
 
+def traffic_of(kernel: str):
+    """DRAM bytes per launch from the committed ncu capture of `kernel`, or None
+    when the kernel's source has changed since the capture."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src):
+        return None
+    if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != rec["source_sha256_16"]:
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -394,11 +414,32 @@ def main():
     from paged_kv_cache_70_gb300 import workloads as W
     hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
 
-    # ---------------- decode (headline) ----------------
+    line = {"metric": METRIC, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "gpu_launches": 0,
+            "error_flags": 0}
+    dstep = None
+    if args.only in ("all", "decode"):
+        dstep = run_decode(args, world, pkv, W, hbm_peak, peak_src, line)
+    if args.only in ("all", "prefill"):
+        run_prefill(args, world, pkv, W, bf16_peak, peak_src, line)
+    if args.only == "prefill":  # headline comes from the prefill half
+        line["metric"] = "varlen prefill TFLOP/s"
+        line["value"], line["unit"] = line["prefill"].get("value"), "TFLOP/s"
+        line["ms_per_step"] = line["prefill"].get("ms_per_step")
+    cpu_baseline(args, world, rank, W, dstep, line)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_decode(args, world, pkv, W, hbm_peak, peak_src, line):
     dstep = W.config(DECODE_CFG)
     ddev = DeviceStep(dstep, pkv)
     clocks = Clocks(torch.cuda.current_device())
-    clocks.start()
+    clocks.start()  # sampled from the warm-up on: the timed region is shorter than one period
     total_ms, dec_mean, dec_med = time_steps(ddev, args.steps, args.warmup, None, world)
     clk = clocks.stop()
     total_ms = max_over_ranks(total_ms, world)
@@ -411,14 +452,8 @@ def main():
     ctas = torch.cuda.get_device_properties(0).multi_processor_count
     part = (ctas + dstep.n_decode) * dstep.hq * (dstep.d + 2) * 4 * 2
     achieved = dbytes / (dec_mean * 1e-3) / 1e9
-    e2e_ms, h2d, d2h = time_e2e(dstep, ddev, args.steps, args.warmup, world)
-    flags = pkv.paged_error_flags()
-
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
+    line.update({
+        "value": round(value, 2), "ms_per_step": round(ms_step, 5),
         "config": {"workload": W.CONFIG_NAMES[DECODE_CFG] + "; step = slot_mapping build + "
                                "new-token write + paged decode (split-KV + combine)",
                    "batch": dstep.n_decode, "seq_lens_total": int(dstep.cache_seqlens.sum()),
@@ -430,66 +465,77 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "paged_decode (split kernel + combine)",
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
-                     "traffic": None, "algorithmic_bytes_per_launch": dbytes,
+                     "traffic": traffic_of("decode_split_kernel"),
+                     "algorithmic_bytes_per_launch": dbytes,
                      "workspace_bytes_per_launch": part,
                      "mean_ms": round(dec_mean, 5), "median_ms": round(dec_med, 5)},
-        "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * args.steps,
         "clocks": clk,
-        "error_flags": flags,
-    }
+    })
+    line["gpu_launches"] += 4 * args.steps
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = time_e2e(dstep, ddev, args.steps, args.warmup, world)
+        line["e2e"] = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2),
+                       "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    line["error_flags"] |= pkv.paged_error_flags()
     del ddev
     torch.cuda.empty_cache()
+    return dstep
 
-    # ---------------- prefill ----------------
-    if not args.no_prefill:
-        pstep = W.config(PREFILL_CFG)
-        pdev = DeviceStep(pstep, pkv)
-        try:
-            pdev.attend()
-            ok = True
-        except pkv.PagedKVError as e:
-            ok = False
-            line["prefill"] = {"unavailable": str(e)}
-        if ok:
-            flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-            clocks = Clocks(torch.cuda.current_device())
-            clocks.start()
-            ptotal, pmean, pmed = time_steps(pdev, args.steps, args.warmup, flush, world)
-            pclk = clocks.stop()
-            ptotal = max_over_ranks(ptotal, world)
-            flops = prefill_flops(pstep)
-            p_ms = ptotal / args.steps
-            tflops = flops / (pmean * 1e-3) / 1e12
+
+def run_prefill(args, world, pkv, W, bf16_peak, peak_src, line):
+    pstep = W.config(PREFILL_CFG)
+    pdev = DeviceStep(pstep, pkv)
+    try:
+        pdev.attend()
+        ok = True
+    except pkv.PagedKVError as e:
+        ok = False
+        line["prefill"] = {"unavailable": str(e)}
+    if ok:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        clocks = Clocks(torch.cuda.current_device())
+        clocks.start()
+        ptotal, pmean, pmed = time_steps(pdev, args.steps, args.warmup, flush, world)
+        pclk = clocks.stop()
+        ptotal = max_over_ranks(ptotal, world)
+        flops = prefill_flops(pstep)
+        p_ms = ptotal / args.steps
+        tflops = flops / (pmean * 1e-3) / 1e12
+        line["prefill"] = {
+            "metric": "varlen prefill TFLOP/s", "workload": W.CONFIG_NAMES[PREFILL_CFG],
+            "value": round(world * flops / (p_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(p_ms, 5),
+            "step": "slot_mapping build + write of 16 requests' new K/V + causal varlen "
+                    "prefill (L2 flushed between steps, not timed)",
+            "flops_per_step": flops, "visible_pairs": prefill_pairs(pstep),
+            "roofline": {"bound": "tensor", "kernel": "paged_varlen_prefill",
+                         "achieved": round(tflops, 1), "peak": bf16_peak,
+                         "unit": "TFLOP/s", "frac": round(tflops / bf16_peak, 4),
+                         "peak_source": peak_src + " (bf16 burst)",
+                         "traffic": traffic_of("prefill_tc_kernel"),
+                         "mean_ms": round(pmean, 5), "median_ms": round(pmed, 5)},
+            "clocks": pclk,
+        }
+        if not args.no_e2e:
             pe2e_ms, ph2d, pd2h = time_e2e(pstep, pdev, args.steps, args.warmup, world)
-            line["prefill"] = {
-                "metric": "varlen prefill TFLOP/s", "workload": W.CONFIG_NAMES[PREFILL_CFG],
-                "value": round(world * flops / (p_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                "ms_per_step": round(p_ms, 5),
-                "step": "slot_mapping build + write of 16 requests' new K/V + causal varlen "
-                        "prefill (L2 flushed between steps, not timed)",
-                "flops_per_step": flops, "visible_pairs": prefill_pairs(pstep),
-                "roofline": {"bound": "tensor", "kernel": "paged_varlen_prefill",
-                             "achieved": round(tflops, 1), "peak": bf16_peak,
-                             "unit": "TFLOP/s", "frac": round(tflops / bf16_peak, 4),
-                             "peak_source": peak_src + " (bf16 burst)", "traffic": None,
-                             "mean_ms": round(pmean, 5), "median_ms": round(pmed, 5)},
-                "e2e": {"value": round(world * flops / (pe2e_ms * 1e-3) / 1e12, 2),
-                        "unit": "TFLOP/s", "ms_per_step": round(pe2e_ms, 5),
-                        "h2d_bytes_per_step": ph2d, "d2h_bytes_per_step": pd2h},
-                "clocks": pclk,
-            }
-            line["gpu_launches"] += 3 * args.steps
-            line["error_flags"] |= pkv.paged_error_flags()
-        del pdev
-        torch.cuda.empty_cache()
+            line["prefill"]["e2e"] = {
+                "value": round(world * flops / (pe2e_ms * 1e-3) / 1e12, 2),
+                "unit": "TFLOP/s", "ms_per_step": round(pe2e_ms, 5),
+                "h2d_bytes_per_step": ph2d, "d2h_bytes_per_step": pd2h}
+        line["gpu_launches"] += 3 * args.steps
+        line["error_flags"] |= pkv.paged_error_flags()
+    del pdev
+    torch.cuda.empty_cache()
 
-    # ---------------- CPU baseline (oracle, rank 0, N=1) ----------------
+
+def cpu_baseline(args, world, rank, W, dstep, line):
+    """The oracle as it stands, on the host cores (rank 0, N=1 only)."""
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         n_seqs = 8
+        if dstep is None:
+            dstep = W.config(DECODE_CFG)
         dt, nb = oracle_decode_sample(dstep, n_seqs)
         line["cpu_baseline"] = {
             "value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
@@ -503,11 +549,6 @@ def main():
                 "value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s",
                 "cores": oracle.num_threads(), "kind": "oracle",
                 "sample": f"every 64th query row of the prefill workload ({dt:.1f} s)"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
 
 
 if __name__ == "__main__":
