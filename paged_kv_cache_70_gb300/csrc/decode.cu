@@ -19,15 +19,19 @@
 //  * Data movement.  A producer warp streams each tile of K and V (all KV heads
 //    of the CTA; a tile is contiguous in the pool when the CTA owns every KV
 //    head) into a ring of shared-memory stages with cp.async.bulk, tracked by
-//    mbarriers; 5-6 stages of 32 KiB keep ~160 KiB in flight per SM.  The
-//    block-table entry is read once per tile.
+//    mbarriers; ~128 KiB stay in flight per SM.  The block-table entry is read
+//    and range-checked once per tile, by the producer.
 //  * Math.  Eight consumer warps; each warp owns one KV head and its G query
 //    heads (the K/V tile is shared across the GQA group).  Within a warp,
-//    groups of D/16 lanes each take a key row, every lane holding 16 of the D
-//    dimensions of q (pre-scaled by scale*log2 e) and of o; dot products are
-//    reduced with xor shuffles.  Each key updates the state element-wise
-//    (running max; the rescale of o is taken only when the max grows).
+//    groups of D/16 lanes take key rows, every lane holding 16 of the D
+//    dimensions of q (pre-scaled by scale*log2 e) and of o as fp32 pairs; a
+//    group handles two key rows at a time with packed fp32x2 FMAs (four
+//    independent chains), dot products are reduced with xor shuffles, and each
+//    key updates the state (running max; o rescaled only when the max grows).
 //    Exponentials are base 2 on log2-scaled scores, which is the same merge.
+//  * The combine kernel (one warp per sequence and head) is launched as a
+//    programmatic dependent of the split kernel, so its launch overlaps the
+//    split kernel's tail.
 //  * Safety.  Block ids and lengths are range-checked before any address is
 //    formed; every mbarrier wait is time-limited (PKV_FLAG_TIMEOUT).
 #include <float.h>
@@ -48,8 +52,8 @@ struct DecodeArgs {
     const unsigned char* v_cache;
     const int32_t* table;
     const int32_t* seqlens;
-    float* part_o;     // [ctas + batch][hq][D]
-    float* part_ml;    // [ctas + batch][hq][2]
+    float* part_o;        // [ctas + batch][hq][D]
+    float* part_ml;       // [ctas + batch][hq][2]
     int32_t* tstart_out;  // [batch + 1]
     unsigned int* err;
     int64_t num_blocks;
@@ -70,36 +74,58 @@ constexpr size_t kTstartBytes = align_up((kDecodeMaxBatch + 1) * sizeof(int32_t)
 __host__ __device__ constexpr size_t merge_bytes(int G, int D) {
     return align_up((size_t)kConsumerWarps * G * (D + 2) * sizeof(float), 128);
 }
+// [barriers 128 B][stage valid flags 128 B][tile starts][merge scratch][stages]
 __host__ __device__ constexpr size_t decode_fixed_smem(int G, int D) {
-    return 128 + kTstartBytes + merge_bytes(G, D);
+    return 256 + kTstartBytes + merge_bytes(G, D);
 }
 
-// load 8 consecutive elements as fp32
+// ---- packed fp32x2 arithmetic (sm_100 family) ---------------------------------
+__device__ __forceinline__ unsigned long long f2u(float2 a) {
+    return (unsigned long long)__float_as_uint(a.x) |
+           ((unsigned long long)__float_as_uint(a.y) << 32);
+}
+__device__ __forceinline__ float2 u2f(unsigned long long u) {
+    return make_float2(__uint_as_float((uint32_t)u), __uint_as_float((uint32_t)(u >> 32)));
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)), "l"(f2u(c)));
+    return u2f(d);
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
+    return u2f(d);
+}
+// two bf16 packed in a word -> (element 2i, element 2i+1) as fp32 (exact)
+__device__ __forceinline__ float2 bf2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// 8 consecutive elements as 4 fp32 pairs
 template <bool BF16>
-__device__ __forceinline__ void load8_smem(const unsigned char* p, float* x) {
+__device__ __forceinline__ void load8_smem(const unsigned char* p, float2* x) {
     if constexpr (BF16) {
         const uint4 w = *reinterpret_cast<const uint4*>(p);
-        x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
-        x[4] = bf16lo(w.z); x[5] = bf16hi(w.z); x[6] = bf16lo(w.w); x[7] = bf16hi(w.w);
+        x[0] = bf2(w.x); x[1] = bf2(w.y); x[2] = bf2(w.z); x[3] = bf2(w.w);
     } else {
         const float4 a = *reinterpret_cast<const float4*>(p);
         const float4 b = *reinterpret_cast<const float4*>(p + 16);
-        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+        x[0] = make_float2(a.x, a.y); x[1] = make_float2(a.z, a.w);
+        x[2] = make_float2(b.x, b.y); x[3] = make_float2(b.z, b.w);
     }
 }
 
 template <bool BF16>
-__device__ __forceinline__ void load8_global(const void* base, int64_t elem, float* x) {
+__device__ __forceinline__ void load8_global(const void* base, int64_t elem, float2* x) {
     if constexpr (BF16) {
         const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + elem));
-        x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
-        x[4] = bf16lo(w.z); x[5] = bf16hi(w.z); x[6] = bf16lo(w.w); x[7] = bf16hi(w.w);
+        x[0] = bf2(w.x); x[1] = bf2(w.y); x[2] = bf2(w.z); x[3] = bf2(w.w);
     } else {
         const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem);
         const float4 a = __ldg(p), b = __ldg(p + 1);
-        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+        x[0] = make_float2(a.x, a.y); x[1] = make_float2(a.z, a.w);
+        x[2] = make_float2(b.x, b.y); x[3] = make_float2(b.z, b.w);
     }
 }
 
@@ -119,7 +145,6 @@ __device__ void scan_tiles(const DecodeArgs& a, int32_t* tstart) {
         const int32_t L = clamp_len(a.seqlens[b], cap);
         sum += (L + a.rows - 1) / a.rows;
     }
-    // inclusive warp scan of the per-thread sums
     const int lane = tid & 31, warp = tid >> 5;
     int32_t inc = sum;
 #pragma unroll
@@ -150,6 +175,24 @@ __device__ __forceinline__ int seq_of_tile(const int32_t* tstart, int batch, int
     return lo - 1;
 }
 
+// online-softmax update of one head's state with one key row (score s, V pairs)
+__device__ __forceinline__ void online_update(float s, const float2* v, float& m, float& l,
+                                              float2* o) {
+    if (s > m) {  // running max grows: rescale the state
+        const float c = ex2(m - s);
+        l *= c;
+        const float2 c2 = make_float2(c, c);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = fmul2(o[e], c2);
+        m = s;
+    }
+    const float p = ex2(s - m);
+    l += p;
+    const float2 p2 = make_float2(p, p);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = ffma2(p2, v[e], o[e]);
+}
+
 template <int D, bool BF16, int G>
 __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const DecodeArgs a) {
     constexpr int ELT = BF16 ? 2 : 4;
@@ -158,14 +201,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kMaxStages;
-    int32_t* tstart = reinterpret_cast<int32_t*>(smem + 128);
-    float* mscratch = reinterpret_cast<float*>(smem + 128 + kTstartBytes);
+    int32_t* stage_ok = reinterpret_cast<int32_t*>(smem + 128);
+    int32_t* tstart = reinterpret_cast<int32_t*>(smem + 256);
+    float* mscratch = reinterpret_cast<float*>(smem + 256 + kTstartBytes);
     unsigned char* stage_base = smem + decode_fixed_smem(G, D);
+
+    // the combine kernel may be scheduled now; it waits for this grid's results
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = a.stages, R = a.rows, HC = a.hc;
-    const size_t row_bytes = (size_t)HC * D * ELT;         // one key row of the CTA's heads
-    const size_t half_bytes = (size_t)R * row_bytes;       // K (or V) part of a stage
+    const size_t row_bytes = (size_t)HC * D * ELT;    // one key row of the CTA's heads
+    const size_t half_bytes = (size_t)R * row_bytes;  // K (or V) part of a stage
     const int32_t cap = a.max_blocks * a.block_size;
 
     if (threadIdx.x == 0) {
@@ -211,9 +258,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
             const int32_t phys = a.table[(int64_t)b * a.max_blocks + pos0 / a.block_size];
             if (phys < 0 || phys >= a.num_blocks) {
                 flag_error(a.err, PKV_FLAG_BAD_BLOCK);
+                stage_ok[s] = 0;
                 mbar_arrive(&full[s]);
                 continue;
             }
+            stage_ok[s] = 1;
             const int64_t row0 = (int64_t)phys * a.block_size + pos0 % a.block_size;
             unsigned char* kd = stage_base + (size_t)s * 2 * half_bytes;
             unsigned char* vd = kd + half_bytes;
@@ -236,17 +285,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
     }
 
     // ------------------------------- consumers --------------------------------
-    const int hc = warp % HC;          // local KV head of this warp
-    const int wrank = warp / HC;       // rank among the warps sharing this head
+    const int hc = warp % HC;     // local KV head of this warp
+    const int wrank = warp / HC;  // rank among the warps sharing this head
     const int WH = kConsumerWarps / HC;
     const int grp = lane / TG, tl = lane % TG;
-    const int row_first = wrank * GPW + grp;
-    const int row_step = WH * GPW;
+    const int warp_row0 = wrank * GPW;  // first row of the warp in a tile
+    const int row_step = WH * GPW;      // rows between a group's consecutive rows
     const int kvh = head0 + hc;
-    // this lane's dimensions: [c*TG*8 + tl*8, +8) for c = 0, 1
+    // this lane's dimensions: [tl*8, +8) and [TG*8 + tl*8, +8)
     const int dim0 = tl * 8, dim1 = TG * 8 + tl * 8;
 
-    float qf[G][16], o[G][16], m[G], l[G];
+    float2 q2[G][8], o2[G][8];
+    float m[G], l[G];
     int b = seq_of_tile(tstart, a.batch, t0);
     int loaded = -1;
     int32_t L = 0;
@@ -256,15 +306,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
         if (b != loaded) {
             loaded = b;
             L = clamp_len(a.seqlens[b], cap);
+            const float2 sc2 = make_float2(a.qscale, a.qscale);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const int64_t qb = ((int64_t)b * a.hq + (int64_t)kvh * G + g) * D;
-                load8_global<BF16>(a.q, qb + dim0, &qf[g][0]);
-                load8_global<BF16>(a.q, qb + dim1, &qf[g][8]);
+                load8_global<BF16>(a.q, qb + dim0, &q2[g][0]);
+                load8_global<BF16>(a.q, qb + dim1, &q2[g][4]);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    qf[g][e] *= a.qscale;
-                    o[g][e] = 0.f;
+                for (int e = 0; e < 8; ++e) {
+                    q2[g][e] = fmul2(q2[g][e], sc2);
+                    o2[g][e] = make_float2(0.f, 0.f);
                 }
                 m[g] = -INFINITY;
                 l[g] = 0.f;
@@ -272,54 +323,57 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
         }
         const int s = k % S;
         if (!mbar_wait(&full[s], (k / S) & 1, a.err)) return;
-        const int32_t pos0 = (t - tstart[b]) * R;
-        const int32_t rows = min(R, L - pos0);
-        const int32_t phys = a.table[(int64_t)b * a.max_blocks + pos0 / a.block_size];
-        if (phys >= 0 && phys < a.num_blocks) {
+        const int32_t rows = min(R, L - (t - tstart[b]) * R);
+        if (stage_ok[s]) {
             const unsigned char* ks = stage_base + (size_t)s * 2 * half_bytes;
             const unsigned char* vs = ks + half_bytes;
-            // warp-uniform loop: the warp continues while its first group has a row
-            for (int r = row_first; r - grp < rows; r += row_step) {
-                const bool valid = r < rows;
-                const int rr = valid ? r : rows - 1;
-                const unsigned char* kr = ks + ((size_t)rr * HC + hc) * D * ELT;
-                float kx[16];
-                load8_smem<BF16>(kr + dim0 * ELT, &kx[0]);
-                load8_smem<BF16>(kr + dim1 * ELT, &kx[8]);
-                float sc[G];
+            // warp-uniform loop over pairs of rows (ra, rb = ra + row_step)
+            for (int base = warp_row0; base < rows; base += 2 * row_step) {
+                const int ra = base + grp, rb = ra + row_step;
+                const bool va = ra < rows, vb = rb < rows;
+                const int ia = va ? ra : 0, ib = vb ? rb : 0;
+                const unsigned char* kra = ks + ((size_t)ia * HC + hc) * D * ELT;
+                const unsigned char* krb = ks + ((size_t)ib * HC + hc) * D * ELT;
+                float2 ka[8], kb[8];
+                load8_smem<BF16>(kra + dim0 * ELT, &ka[0]);
+                load8_smem<BF16>(kra + dim1 * ELT, &ka[4]);
+                load8_smem<BF16>(krb + dim0 * ELT, &kb[0]);
+                load8_smem<BF16>(krb + dim1 * ELT, &kb[4]);
+                float sa[G], sb[G];
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    float s0 = 0.f, s1 = 0.f;
+                    float2 acca = make_float2(0.f, 0.f), accb = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        s0 = fmaf(qf[g][e], kx[e], s0);
-                        s1 = fmaf(qf[g][8 + e], kx[8 + e], s1);
+                        acca = ffma2(q2[g][e], ka[e], acca);
+                        accb = ffma2(q2[g][e], kb[e], accb);
                     }
-                    sc[g] = s0 + s1;
+                    sa[g] = acca.x + acca.y;
+                    sb[g] = accb.x + accb.y;
                 }
 #pragma unroll
-                for (int off = 1; off < TG; off <<= 1)
-#pragma unroll
-                    for (int g = 0; g < G; ++g) sc[g] += __shfl_xor_sync(0xffffffffu, sc[g], off);
-                if (valid) {
-                    const unsigned char* vr = vs + ((size_t)rr * HC + hc) * D * ELT;
-                    float vx[16];
-                    load8_smem<BF16>(vr + dim0 * ELT, &vx[0]);
-                    load8_smem<BF16>(vr + dim1 * ELT, &vx[8]);
+                for (int off = 1; off < TG; off <<= 1) {
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
-                        if (sc[g] > m[g]) {  // running max grows: rescale the state
-                            const float c = ex2(m[g] - sc[g]);
-                            l[g] *= c;
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) o[g][e] *= c;
-                            m[g] = sc[g];
-                        }
-                        const float p = ex2(sc[g] - m[g]);
-                        l[g] += p;
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) o[g][e] = fmaf(p, vx[e], o[g][e]);
+                        sa[g] += __shfl_xor_sync(0xffffffffu, sa[g], off);
+                        sb[g] += __shfl_xor_sync(0xffffffffu, sb[g], off);
                     }
+                }
+                if (va) {
+                    const unsigned char* vr = vs + ((size_t)ia * HC + hc) * D * ELT;
+                    float2 vx[8];
+                    load8_smem<BF16>(vr + dim0 * ELT, &vx[0]);
+                    load8_smem<BF16>(vr + dim1 * ELT, &vx[4]);
+#pragma unroll
+                    for (int g = 0; g < G; ++g) online_update(sa[g], vx, m[g], l[g], o2[g]);
+                }
+                if (vb) {
+                    const unsigned char* vr = vs + ((size_t)ib * HC + hc) * D * ELT;
+                    float2 vx[8];
+                    load8_smem<BF16>(vr + dim0 * ELT, &vx[0]);
+                    load8_smem<BF16>(vr + dim1 * ELT, &vx[4]);
+#pragma unroll
+                    for (int g = 0; g < G; ++g) online_update(sb[g], vx, m[g], l[g], o2[g]);
                 }
             }
         }
@@ -341,9 +395,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
                 const float cb = (mo == -INFINITY) ? 0.f : ex2(mo - M);
                 l[g] = l[g] * ca + lo * cb;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float oo = __shfl_xor_sync(0xffffffffu, o[g][e], off);
-                    o[g][e] = o[g][e] * ca + oo * cb;
+                for (int e = 0; e < 8; ++e) {
+                    const float ox = __shfl_xor_sync(0xffffffffu, o2[g][e].x, off);
+                    const float oy = __shfl_xor_sync(0xffffffffu, o2[g][e].y, off);
+                    o2[g][e] = make_float2(o2[g][e].x * ca + ox * cb, o2[g][e].y * ca + oy * cb);
                 }
                 m[g] = M;
             }
@@ -354,9 +409,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        my[g * (D + 2) + dim0 + e] = o[g][e];
-                        my[g * (D + 2) + dim1 + e] = o[g][8 + e];
+                    for (int e = 0; e < 4; ++e) {
+                        my[g * (D + 2) + dim0 + 2 * e] = o2[g][e].x;
+                        my[g * (D + 2) + dim0 + 2 * e + 1] = o2[g][e].y;
+                        my[g * (D + 2) + dim1 + 2 * e] = o2[g][4 + e].x;
+                        my[g * (D + 2) + dim1 + 2 * e + 1] = o2[g][4 + e].y;
                     }
                     if (tl == 0) {
                         my[g * (D + 2) + D] = m[g];
@@ -371,24 +428,27 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
                     float M = -INFINITY;
                     for (int w = 0; w < WH; ++w)
                         M = fmaxf(M, mscratch[(size_t)(w * HC + hc) * G * (D + 2) + g * (D + 2) + D]);
-                    float lt = 0.f, ot[16];
+                    float lt = 0.f;
+                    float2 ot[8];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) ot[e] = 0.f;
+                    for (int e = 0; e < 8; ++e) ot[e] = make_float2(0.f, 0.f);
                     for (int w = 0; w < WH; ++w) {
                         const float* src = mscratch + (size_t)(w * HC + hc) * G * (D + 2) + g * (D + 2);
                         const float mw = src[D];
                         const float c = (mw == -INFINITY) ? 0.f : ex2(mw - M);
                         lt += src[D + 1] * c;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            ot[e] += src[dim0 + e] * c;
-                            ot[8 + e] += src[dim1 + e] * c;
+                        for (int e = 0; e < 4; ++e) {
+                            ot[e].x += src[dim0 + 2 * e] * c;
+                            ot[e].y += src[dim0 + 2 * e + 1] * c;
+                            ot[4 + e].x += src[dim1 + 2 * e] * c;
+                            ot[4 + e].y += src[dim1 + 2 * e + 1] * c;
                         }
                     }
                     m[g] = M;
                     l[g] = lt;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) o[g][e] = ot[e];
+                    for (int e = 0; e < 8; ++e) o2[g][e] = ot[e];
                 }
             }
             asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
@@ -399,10 +459,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
             for (int g = 0; g < G; ++g) {
                 const int64_t qh = (int64_t)kvh * G + g;
                 float* dst = a.part_o + (slot * a.hq + qh) * D;
-                *reinterpret_cast<float4*>(dst + dim0) = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
-                *reinterpret_cast<float4*>(dst + dim0 + 4) = make_float4(o[g][4], o[g][5], o[g][6], o[g][7]);
-                *reinterpret_cast<float4*>(dst + dim1) = make_float4(o[g][8], o[g][9], o[g][10], o[g][11]);
-                *reinterpret_cast<float4*>(dst + dim1 + 4) = make_float4(o[g][12], o[g][13], o[g][14], o[g][15]);
+                *reinterpret_cast<float4*>(dst + dim0) =
+                    make_float4(o2[g][0].x, o2[g][0].y, o2[g][1].x, o2[g][1].y);
+                *reinterpret_cast<float4*>(dst + dim0 + 4) =
+                    make_float4(o2[g][2].x, o2[g][2].y, o2[g][3].x, o2[g][3].y);
+                *reinterpret_cast<float4*>(dst + dim1) =
+                    make_float4(o2[g][4].x, o2[g][4].y, o2[g][5].x, o2[g][5].y);
+                *reinterpret_cast<float4*>(dst + dim1 + 4) =
+                    make_float4(o2[g][6].x, o2[g][6].y, o2[g][7].x, o2[g][7].y);
                 if (tl == 0) {
                     a.part_ml[(slot * a.hq + qh) * 2 + 0] = m[g];
                     a.part_ml[(slot * a.hq + qh) * 2 + 1] = l[g];
@@ -413,46 +477,58 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
     }
 }
 
-// Merge the partial states of every sequence and normalise.  One CTA per
-// sequence; thread i handles 4 consecutive output elements of [hq][D].
-template <bool BF16>
-__global__ void decode_combine_kernel(const float* __restrict__ part_o,
-                                      const float* __restrict__ part_ml,
-                                      const int32_t* __restrict__ tstart, int32_t batch, int ctas,
-                                      int hq, int D, void* __restrict__ out) {
-    const int b = blockIdx.x;
+// Merge the partial states of every (sequence, head) and normalise.  One warp
+// per (sequence, head); lane i owns dims [i*D/32, (i+1)*D/32).
+template <int D, bool BF16>
+__global__ void __launch_bounds__(128)
+decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
+                      const int32_t* __restrict__ tstart, int32_t batch, int ctas, int hq,
+                      void* __restrict__ out) {
+    constexpr int DPL = D / 32;
+    // wait until the split kernel's partials are complete and visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (w >= (int64_t)batch * hq) return;
+    const int b = (int)(w / hq), h = (int)(w % hq);
     const int32_t total = tstart[batch];
     const int32_t tb0 = tstart[b], tb1 = tstart[b + 1];
-    const int n4 = hq * D / 4;
-    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
-        const int h = (i * 4) / D;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float lt = 0.f;
-        if (tb1 > tb0) {
-            const int32_t chunk = (total + ctas - 1) / ctas;
-            const int c0 = tb0 / chunk, c1 = (tb1 - 1) / chunk;
-            float M = -INFINITY;
-            for (int c = c0; c <= c1; ++c) M = fmaxf(M, part_ml[(((int64_t)c + b) * hq + h) * 2]);
-            if (M != -INFINITY) {
-                for (int c = c0; c <= c1; ++c) {
-                    const int64_t slot = (int64_t)c + b;
-                    const float mc = part_ml[(slot * hq + h) * 2];
-                    const float w = (mc == -INFINITY) ? 0.f : ex2(mc - M);
-                    lt += part_ml[(slot * hq + h) * 2 + 1] * w;
-                    const float4 oc = *reinterpret_cast<const float4*>(part_o + slot * hq * D + i * 4);
-                    acc.x += oc.x * w; acc.y += oc.y * w; acc.z += oc.z * w; acc.w += oc.w * w;
-                }
+    float acc[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+    float lt = 0.f;
+    if (tb1 > tb0) {
+        const int32_t chunk = (total + ctas - 1) / ctas;
+        const int c0 = tb0 / chunk, c1 = (tb1 - 1) / chunk;
+        float M = -INFINITY;
+        for (int c = c0 + lane; c <= c1; c += 32)
+            M = fmaxf(M, part_ml[(((int64_t)c + b) * hq + h) * 2]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        if (M != -INFINITY) {
+#pragma unroll 4
+            for (int c = c0; c <= c1; ++c) {
+                const int64_t slot = (int64_t)c + b;
+                const float2 ml = *reinterpret_cast<const float2*>(part_ml + (slot * hq + h) * 2);
+                const float wgt = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
+                lt += ml.y * wgt;
+                const float* src = part_o + (slot * hq + h) * D + lane * DPL;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[e] += src[e] * wgt;
             }
         }
-        const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        const float r0 = acc.x * inv, r1 = acc.y * inv, r2 = acc.z * inv, r3 = acc.w * inv;
-        const int64_t oi = (int64_t)b * hq * D + (int64_t)i * 4;
-        if constexpr (BF16) {
-            uint2 pk = make_uint2(pack_bf16x2(r0, r1), pack_bf16x2(r2, r3));
-            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + oi) = pk;
-        } else {
-            *reinterpret_cast<float4*>(static_cast<float*>(out) + oi) = make_float4(r0, r1, r2, r3);
-        }
+    }
+    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+    const int64_t oi = ((int64_t)b * hq + h) * D + lane * DPL;
+    if constexpr (BF16) {
+        uint16_t* o = static_cast<uint16_t*>(out) + oi;
+#pragma unroll
+        for (int e = 0; e < DPL; e += 2)
+            *reinterpret_cast<uint32_t*>(o + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+    } else {
+        float* o = static_cast<float*>(out) + oi;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[e] = acc[e] * inv;
     }
 }
 
@@ -481,8 +557,8 @@ bool plan_decode(const DeviceInfo& dev, int32_t batch, int hq, int hkv, int d, i
         HC = kConsumerWarps;
     }
     const size_t row_bytes = (size_t)HC * d * elt;
-    // ~32 KiB of K+V per stage
-    int cap_rows = (int)(32768 / (2 * row_bytes));
+    // ~64 KiB of K+V per stage, at most 32 keys
+    int cap_rows = (int)(65536 / (2 * row_bytes));
     if (cap_rows < 1) cap_rows = 1;
     if (cap_rows > 32) cap_rows = 32;
     const int R = largest_pow2_divisor(block_size, cap_rows);
@@ -514,9 +590,23 @@ static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a, 
     kern<<<grid, kDecodeThreads, plan.smem_bytes, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<BF16><<<a.batch, 256, 0, stream>>>(a.part_o, a.part_ml, a.tstart_out,
-                                                             a.batch, plan.ctas, a.hq, D, out);
-    return cudaGetLastError();
+    // combine: programmatic dependent of the split kernel
+    cudaLaunchConfig_t cfg = {};
+    const int64_t warps = (int64_t)a.batch * a.hq;
+    cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, BF16>,
+                              static_cast<const float*>(a.part_o),
+                              static_cast<const float*>(a.part_ml),
+                              static_cast<const int32_t*>(a.tstart_out), a.batch, plan.ctas,
+                              a.hq, out);
 }
 
 cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_cache,
