@@ -12,21 +12,26 @@
 //   out = softmax(scale * Q K^T) V over the visible keys, 0 for a row that
 //   sees none.
 //
-// GB300 design, one CTA per (128-query tile, query head, request):
-//   warp 4   TMA producer: K and V tiles of 128 keys x 128 dims (bf16) into a
-//            2-stage ring, 128-byte swizzle; a tile is assembled from one box
-//            per page piece (min(B,128) rows) addressed through the block
-//            table; boxes past the request's keys use an out-of-range row and
-//            arrive zero-filled.
-//   warp 5   owns TMEM (512 columns: S double buffer 2 x 128, O 128) and is the
-//            single MMA issuer: S_j = Q K_j^T (M=N=128, K=16 per instruction,
-//            both operands K-major), then O += P_j V_j (P K-major, V MN-major),
-//            completion signalled with tcgen05.commit on mbarriers.
-//   warps 0-3 softmax: thread t owns query row t = TMEM lane t.  Per tile it
-//            reads its S row (tcgen05.ld), masks, keeps the running max m and
-//            sum l, writes p = 2^(s - m) as bf16 into the swizzled P tile, and
-//            rescales its O row in TMEM only when some row of the warp saw a
-//            larger max.  The epilogue divides O by l and stores bf16 rows.
+// GB300 design, one CTA per (128-query tile, pair of query heads of one KV
+// head, request) -- two Q tiles A and B that read the same K/V stream:
+//   warp 8   TMA producer: K and V tiles of 128 keys x 128 dims (bf16) into
+//            separate 2-stage rings, 128-byte swizzle; a tile is assembled from
+//            one box per page piece (min(B,128) rows) addressed through the
+//            block table; boxes past the request's keys use an out-of-range
+//            row and arrive zero-filled.
+//   warp 9   owns TMEM (512 columns: S_A, S_B, O_A, O_B, 128 each) and issues
+//            every tcgen05.mma: S_X = Q_X K^T (both operands K-major in shared
+//            memory), O_X += P_X V with P_X read from TMEM (the bf16 P tile
+//            overwrites the first 64 columns of S_X) and V MN-major.  The
+//            issue order PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1) keeps the
+//            tensor core on one tile while the other tile's softmax runs.
+//   warps 0-3 / 4-7  softmax of tile A / B: thread t owns query row t = TMEM
+//            lane t.  Per K/V tile it reads its S row, masks only on diagonal
+//            or ragged tiles, and computes p = 2^(s*scale*log2e - m_ref) with
+//            one FMA and one MUFU op per element.  m_ref is a lagging reference
+//            maximum: it (and O, l) is rescaled only when the row maximum grows
+//            by more than 2^8, so p <= 256 and the final o/l is unchanged.
+//   The epilogue divides O by l and stores bf16 rows.
 // Every mbarrier wait is time-limited; a timeout sets PKV_FLAG_TIMEOUT and the
 // CTA drains its copies and frees TMEM before returning.
 #include <cuda.h>
@@ -40,22 +45,23 @@ namespace pkv {
 
 namespace {
 
-constexpr int BM = 128;  // query rows per CTA
-constexpr int BN = 128;  // keys per tile
+constexpr int BM = 128;  // query rows per Q tile
+constexpr int BN = 128;  // keys per K/V tile
 constexpr int HD = 128;  // head_dim
-constexpr int STAGES = 2;
-constexpr int kThreads = 192;
+constexpr int SK = 2;    // K ring depth
+constexpr int SV = 2;    // V ring depth
+constexpr int kThreads = 384;  // 8 softmax warps, TMA warp, MMA warp, 2 spare
 constexpr int kTmemCols = 512;
-constexpr uint32_t kTileBytes = BN * HD * 2;     // 32 KiB: one K (or V) tile
-constexpr uint32_t kRegionBytes = BN * 128;      // 16 KiB: 64 dims (128 B) x 128 rows
+constexpr uint32_t kTileBytes = BN * HD * 2;  // 32 KiB: one Q, K or V tile
+constexpr uint32_t kRegionBytes = BN * 128;   // 16 KiB: 64 dims (128 B) x 128 rows
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleLog2 = 8.0f;  // rescale when the row max grows by > 2^8
 
 // shared memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_P = OFF_Q + kTileBytes;
-constexpr uint32_t OFF_K = OFF_P + kTileBytes;
-constexpr uint32_t OFF_V = OFF_K + STAGES * kTileBytes;
-constexpr uint32_t OFF_BAR = OFF_V + STAGES * kTileBytes;
+constexpr uint32_t OFF_Q = 0;  // Q_A, Q_B
+constexpr uint32_t OFF_K = OFF_Q + 2 * kTileBytes;
+constexpr uint32_t OFF_V = OFF_K + SK * kTileBytes;
+constexpr uint32_t OFF_BAR = OFF_V + SV * kTileBytes;
 constexpr uint32_t BAR_BYTES = 256;
 constexpr uint32_t GUARD_BYTES = 4096;  // unused tail after the barriers
 constexpr size_t kSmemBytes = OFF_BAR + BAR_BYTES + GUARD_BYTES + 1024;
@@ -91,6 +97,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(id), "r"(accumulate)
+        : "memory");
+}
+
+// A operand from TMEM (rows in lanes, 2 bf16 per 32-bit column), B from smem
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                                uint32_t id, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
         : "memory");
 }
 
@@ -165,13 +182,18 @@ struct PrefillArgs {
     float scale_log2;
     int32_t max_blocks;
     int32_t hq;
-    int32_t group;  // hq / hkv
+    int32_t group;       // hq / hkv
+    int32_t pair_heads;  // 1: a CTA takes query heads (2p, 2p+1); 0: head p alone
     int32_t block_size;
-    int32_t piece;  // rows per TMA box = min(B, 128)
+    int32_t piece;    // rows per TMA box = min(B, 128)
     int32_t oob_row;  // a row index beyond the pools (zero-filled by TMA)
     int32_t tiles_q;
     int32_t causal;
 };
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* err) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -180,18 +202,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-    uint64_t* kv_full = bars;             // [STAGES]
-    uint64_t* kv_empty = bars + 2;        // [STAGES]
-    uint64_t* s_full = bars + 4;          // [2]
-    uint64_t* s_free = bars + 6;          // [2]
-    uint64_t* p_full = bars + 8;
-    uint64_t* o_ready = bars + 9;
-    uint64_t* q_ready = bars + 10;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+    uint64_t* k_full = bars;        // [SK]
+    uint64_t* k_empty = bars + 2;   // [SK]
+    uint64_t* v_full = bars + 4;    // [SV]
+    uint64_t* v_empty = bars + 6;   // [SV]
+    uint64_t* s_full = bars + 8;    // [2] per Q tile
+    uint64_t* p_full = bars + 10;   // [2]
+    uint64_t* o_ready = bars + 12;  // [2]
+    uint64_t* q_ready = bars + 14;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.z, h = blockIdx.y;
+    const int r = blockIdx.z;
     const int qt = a.tiles_q - 1 - (int)blockIdx.x;  // later (heavier) tiles first
+    const int h_a = a.pair_heads ? 2 * (int)blockIdx.y : (int)blockIdx.y;
+    const bool has_b = a.pair_heads && h_a + 1 < a.hq;
     const int32_t cq0 = a.cu_q[r], cq1 = a.cu_q[r + 1];
     const int32_t ck0 = a.cu_k[r], ck1 = a.cu_k[r + 1];
     int32_t q_len = cq1 - cq0, k_len = ck1 - ck0;
@@ -212,30 +237,35 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int64_t out_row0 = (int64_t)cq0 + q0;
 
     if (n_tiles == 0) {  // no query row of this tile sees a key: output 0
-        for (int i = threadIdx.x; i < rows * (HD / 8); i += blockDim.x) {
-            const int rr = i / (HD / 8), c = i % (HD / 8);
-            *reinterpret_cast<uint4*>(a.out + ((out_row0 + rr) * a.hq + h) * HD + c * 8) =
+        const int nh = has_b ? 2 : 1;
+        for (int i = threadIdx.x; i < nh * rows * (HD / 8); i += blockDim.x) {
+            const int x = i / (rows * (HD / 8)), rem = i % (rows * (HD / 8));
+            const int rr = rem / (HD / 8), c = rem % (HD / 8);
+            *reinterpret_cast<uint4*>(a.out + ((out_row0 + rr) * a.hq + h_a + x) * HD + c * 8) =
                 make_uint4(0, 0, 0, 0);
         }
         return;
     }
-    const int kvh = h / a.group;
+    const int kvh = h_a / a.group;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+        for (int s = 0; s < SK; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&s_full[b], 1);
-            mbar_init(&s_free[b], 4);
+        for (int s = 0; s < SV; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
-        mbar_init(p_full, 4);
-        mbar_init(o_ready, 1);
-        mbar_init(q_ready, 4);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&s_full[x], 1);
+            mbar_init(&p_full[x], 4);
+            mbar_init(&o_ready[x], 1);
+        }
+        mbar_init(q_ready, has_b ? 8 : 4);
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
                      "r"(kTmemCols)
@@ -246,20 +276,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tm_s[2] = {tmem, tmem + 128};
-    const uint32_t tm_o = tmem + 256;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
             const int pieces = BN / a.piece;
             int issued = 0;
             for (int j = 0; j < n_tiles; ++j) {
-                const int s = j % STAGES;
-                if (!mbar_wait(&kv_empty[s], ((j / STAGES) & 1) ^ 1, a.err)) break;
-                mbar_arrive_expect_tx(&kv_full[s], 2 * kTileBytes);
-                unsigned char* kd = sm + OFF_K + s * kTileBytes;
-                unsigned char* vd = sm + OFF_V + s * kTileBytes;
+                const int sk = j % SK, sv = j % SV;
+                if (!mbar_wait(&k_empty[sk], ((j / SK) & 1) ^ 1, a.err)) break;
+                mbar_arrive_expect_tx(&k_full[sk], kTileBytes);
+                int32_t rowv[BN / 8];
                 for (int p = 0; p < pieces; ++p) {
                     const int32_t key = j * BN + p * a.piece;
                     int32_t row = a.oob_row;
@@ -270,62 +297,84 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         else
                             row = phys * a.block_size + key % a.block_size;
                     }
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const uint32_t off = hh * kRegionBytes + p * a.piece * 128;
-                        tma_load_3d(kd + off, &tmap_k, hh * 64, kvh, row, &kv_full[s]);
-                        tma_load_3d(vd + off, &tmap_v, hh * 64, kvh, row, &kv_full[s]);
-                    }
+                    rowv[p] = row;
+                    unsigned char* kd = sm + OFF_K + sk * kTileBytes + p * a.piece * 128;
+                    tma_load_3d(kd, &tmap_k, 0, kvh, row, &k_full[sk]);
+                    tma_load_3d(kd + kRegionBytes, &tmap_k, 64, kvh, row, &k_full[sk]);
+                }
+                if (!mbar_wait(&v_empty[sv], ((j / SV) & 1) ^ 1, a.err)) { ++issued; break; }
+                mbar_arrive_expect_tx(&v_full[sv], kTileBytes);
+                for (int p = 0; p < pieces; ++p) {
+                    unsigned char* vd = sm + OFF_V + sv * kTileBytes + p * a.piece * 128;
+                    tma_load_3d(vd, &tmap_v, 0, kvh, rowv[p], &v_full[sv]);
+                    tma_load_3d(vd + kRegionBytes, &tmap_v, 64, kvh, rowv[p], &v_full[sv]);
                 }
                 ++issued;
             }
             // drain: every issued tile has landed before the CTA can exit
-            for (int j = max(0, issued - STAGES); j < issued; ++j)
-                mbar_wait(&kv_full[j % STAGES], (j / STAGES) & 1, a.err);
+            for (int j = max(0, issued - SK); j < issued; ++j)
+                mbar_wait(&k_full[j % SK], (j / SK) & 1, a.err);
+            for (int j = max(0, issued - SV); j < issued; ++j)
+                mbar_wait(&v_full[j % SV], (j / SV) & 1, a.err);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
-            const uint32_t q_base = smem_u32(sm + OFF_Q), p_base = smem_u32(sm + OFF_P);
-            bool ok = mbar_wait(q_ready, 0, a.err);
-            auto issue_qk = [&](int j) -> bool {
-                const int s = j % STAGES;
-                if (!mbar_wait(&kv_full[s], (j / STAGES) & 1, a.err)) return false;
-                if (j >= 2 && !mbar_wait(&s_free[j & 1], ((j - 2) >> 1) & 1, a.err)) return false;
-                tc_fence_after();
-                const uint32_t k_base = smem_u32(sm + OFF_K + s * kTileBytes);
+            const uint32_t q_base = smem_u32(sm + OFF_Q);
+            const uint32_t tm_s[2] = {tmem, tmem + 128};
+            const uint32_t tm_o[2] = {tmem + 256, tmem + 384};
+            const int nx = has_b ? 2 : 1;
+            auto qk = [&](int x, int sk) {
+                const uint32_t k_base = smem_u32(sm + OFF_K + sk * kTileBytes);
 #pragma unroll
                 for (int k = 0; k < HD / 16; ++k) {
                     const uint32_t off = (k >> 2) * kRegionBytes + (k & 3) * 32;
-                    mma_bf16(tm_s[j & 1], sdesc(q_base + off, 16, 1024),
+                    mma_bf16(tm_s[x], sdesc(q_base + x * kTileBytes + off, 16, 1024),
                              sdesc(k_base + off, 16, 1024), IDESC_QK, k > 0);
                 }
-                mma_commit(&s_full[j & 1]);
-                return true;
+                mma_commit(&s_full[x]);
             };
-            if (ok) ok = issue_qk(0);
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                if (j + 1 < n_tiles && !issue_qk(j + 1)) break;
-                if (!mbar_wait(p_full, j & 1, a.err)) break;
-                tc_fence_after();
-                const int s = j % STAGES;
-                const uint32_t v_base = smem_u32(sm + OFF_V + s * kTileBytes);
+            auto pv = [&](int x, int sv, bool first) {
+                const uint32_t v_base = smem_u32(sm + OFF_V + sv * kTileBytes);
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    const uint32_t poff = (k >> 2) * kRegionBytes + (k & 3) * 32;
-                    mma_bf16(tm_o, sdesc(p_base + poff, 16, 1024),
-                             sdesc(v_base + k * 2048, kRegionBytes, 1024), IDESC_PV,
-                             (j > 0 || k > 0) ? 1u : 0u);
+                for (int k = 0; k < BN / 16; ++k)
+                    mma_bf16_tmem_a(tm_o[x], tm_s[x] + k * 8,
+                                    sdesc(v_base + k * 2048, kRegionBytes, 1024), IDESC_PV,
+                                    (!first || k > 0) ? 1u : 0u);
+                mma_commit(&o_ready[x]);
+            };
+            bool ok = mbar_wait(q_ready, 0, a.err) && mbar_wait(&k_full[0], 0, a.err);
+            if (ok) {
+                tc_fence_after();
+                for (int x = 0; x < nx; ++x) qk(x, 0);
+                mma_commit(&k_empty[0]);
+            }
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int sv = j % SV, sk1 = (j + 1) % SK;
+                const bool more = j + 1 < n_tiles;
+                if (!(ok = mbar_wait(&v_full[sv], (j / SV) & 1, a.err))) break;
+                if (more && !(ok = mbar_wait(&k_full[sk1], ((j + 1) / SK) & 1, a.err))) break;
+                for (int x = 0; x < nx; ++x) {
+                    if (!(ok = mbar_wait(&p_full[x], j & 1, a.err))) break;
+                    tc_fence_after();
+                    pv(x, sv, j == 0);
+                    if (more) qk(x, sk1);
                 }
-                mma_commit(o_ready);
-                mma_commit(&kv_empty[s]);
+                if (!ok) break;
+                mma_commit(&v_empty[sv]);
+                if (more) mma_commit(&k_empty[sk1]);
             }
         }
-    } else {
+    } else if (warp < 8 && (warp < 4 || has_b)) {
         // ------------------------------ softmax warps ------------------------------
-        const int t = threadIdx.x;  // query row within the tile == TMEM lane
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const int x = warp >> 2;        // Q tile: 0 = A, 1 = B
+        const int t = threadIdx.x & 127;  // query row in the tile == TMEM lane
+        const int h = h_a + x;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tm_s = tmem + x * 128 + lane_base;
+        const uint32_t tm_o = tmem + 256 + x * 128 + lane_base;
         {   // Q row t -> swizzled shared tile (zeros past the request)
-            unsigned char* qs = sm + OFF_Q;
+            unsigned char* qs = sm + OFF_Q + x * kTileBytes;
             const bool valid = t < rows;
             // rows past the request read row 0 of the tile (always in bounds), then zero it
             const int64_t qrow = out_row0 + (valid ? t : 0);
@@ -343,92 +392,80 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const int32_t row_i = q0 + t;  // query index within the request
         int32_t lim = k_len - 1;
         if (a.causal) lim = min(lim, row_i + diag);
-        float m = -INFINITY, l = 0.f;
+        const float sl = a.scale_log2;
+        float m_ref = -INFINITY;  // lagging reference max (raw score units)
+        float l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
-            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, a.err))) {
-                ok = false;
-                break;
-            }
+            if (!warp_wait(&s_full[x], j & 1, a.err)) { ok = false; break; }
             tc_fence_after();
             uint32_t sr[BN];
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) tmem_ld32(tm_s[j & 1] + lane_base + c * 32, sr + c * 32);
+            for (int c = 0; c < BN / 32; ++c) tmem_ld32(tm_s + c * 32, sr + c * 32);
             tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[j & 1]);
-
             const int32_t key0 = j * BN;
+            if (__any_sync(0xffffffffu, key0 + BN - 1 > lim)) {
+#pragma unroll
+                for (int c = 0; c < BN; ++c)
+                    if (key0 + c > lim) sr[c] = __float_as_uint(-INFINITY);
+            }
             float mx = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < BN; ++c) {
-                const float x = (key0 + c <= lim) ? __uint_as_float(sr[c]) * a.scale_log2 : -INFINITY;
-                sr[c] = __float_as_uint(x);
-                mx = fmaxf(mx, x);
+            for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+            const float m_new = fmaxf(m_ref, mx);
+            // rescale only when the maximum grew by more than 2^kRescaleLog2
+            const bool resc = (m_new - m_ref) * sl > kRescaleLog2;  // false when both -inf
+            float alpha = 1.f;
+            if (resc) {
+                alpha = (m_ref == -INFINITY) ? 0.f : ex2((m_ref - m_new) * sl);
+                m_ref = m_new;
             }
-            const float m_new = fmaxf(m, mx);
-            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = ex2(m - m_use);
+            const float ms = (m_ref == -INFINITY) ? 0.f : m_ref * sl;
             float sum = 0.f;
-            uint32_t* pk = sr;  // packed bf16 pairs overwrite the scores already consumed
+            uint32_t* pk = sr;  // packed bf16 pairs overwrite the consumed scores
 #pragma unroll
             for (int c = 0; c < BN; c += 2) {
-                const float p0 = ex2(__uint_as_float(sr[c]) - m_use);
-                const float p1 = ex2(__uint_as_float(sr[c + 1]) - m_use);
+                const float p0 = ex2(fmaf(__uint_as_float(sr[c]), sl, -ms));
+                const float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), sl, -ms));
                 sum += p0 + p1;
                 pk[c >> 1] = pack_bf16x2(p0, p1);
             }
             l = l * alpha + sum;
-            m = m_new;
-
-            if (j > 0) {
-                // PV_{j-1} done: P tile free and O stable
-                if (!__all_sync(0xffffffffu, mbar_wait(o_ready, (j - 1) & 1, a.err))) {
-                    ok = false;
-                    break;
-                }
+            tmem_st32(tm_s, pk);
+            tmem_st32(tm_s + 32, pk + 32);
+            if (j > 0 && __any_sync(0xffffffffu, resc)) {
+                // PV(j-1) done: O stable; scale it before PV(j) accumulates
+                if (!warp_wait(&o_ready[x], (j - 1) & 1, a.err)) { ok = false; break; }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-                    for (int c = 0; c < HD / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(tm_o + lane_base + c * 32, o);
-                        tmem_wait_ld();
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tm_o + c * 32, o);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(tm_o + lane_base + c * 32, o);
-                    }
-                    tmem_wait_st();
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(tm_o + c * 32, o);
                 }
             }
             // keys past the request in the last tile: zero their V rows so that
             // p = 0 never meets a non-finite value left in the pool
-            if (key0 + BN > k_len) {
-                const int s = j % STAGES;
-                if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[s], (j / STAGES) & 1, a.err))) {
-                    ok = false;
-                    break;
-                }
+            if (x == 0 && key0 + BN > k_len) {
+                const int sv = j % SV;
+                if (!warp_wait(&v_full[sv], (j / SV) & 1, a.err)) { ok = false; break; }
                 if (key0 + t >= k_len) {
-                    unsigned char* vs = sm + OFF_V + s * kTileBytes;
+                    unsigned char* vs = sm + OFF_V + sv * kTileBytes;
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
                         *reinterpret_cast<uint4*>(vs + swz(t, c)) = make_uint4(0, 0, 0, 0);
                 }
+                fence_async_smem();
             }
-            unsigned char* ps = sm + OFF_P;
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-                *reinterpret_cast<uint4*>(ps + swz(t, c)) =
-                    make_uint4(pk[c * 4], pk[c * 4 + 1], pk[c * 4 + 2], pk[c * 4 + 3]);
-            fence_async_smem();
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(&p_full[x]);
         }
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_ready, (n_tiles - 1) & 1, a.err));
+        if (ok) ok = warp_wait(&o_ready[x], (n_tiles - 1) & 1, a.err);
         if (ok) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -436,7 +473,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
             for (int c = 0; c < HD / 32; ++c) {
                 uint32_t o[32];
-                tmem_ld32(tm_o + lane_base + c * 32, o);
+                tmem_ld32(tm_o + c * 32, o);
                 tmem_wait_ld();
                 if (t < rows) {
 #pragma unroll
@@ -454,7 +491,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols)
@@ -538,6 +575,7 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
     a.max_blocks = max_blocks;
     a.hq = hq;
     a.group = hq / hkv;
+    a.pair_heads = (a.group % 2 == 0) ? 1 : 0;
     a.block_size = block_size;
     a.piece = piece;
     a.oob_row = (int32_t)rows;
@@ -547,7 +585,7 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.tiles_q, hq, batch);
+    dim3 grid(a.tiles_q, a.pair_heads ? (hq + 1) / 2 : hq, batch);
     prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mk, mv, a);
     return cudaGetLastError();
 }
