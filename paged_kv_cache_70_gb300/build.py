@@ -74,4 +74,6 @@ def build(force: bool = False, verbose: bool = False, extra: tuple[str, ...] = (
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    defines = tuple(a for a in sys.argv[1:] if a.startswith("-D"))
+    print(build(force="--force" in sys.argv or bool(defines), verbose="-v" in sys.argv,
+                extra=defines))

@@ -79,24 +79,6 @@ __host__ __device__ constexpr size_t decode_fixed_smem(int G, int D) {
     return 256 + kTstartBytes + merge_bytes(G, D);
 }
 
-// ---- packed fp32x2 arithmetic (sm_100 family) ---------------------------------
-__device__ __forceinline__ unsigned long long f2u(float2 a) {
-    return (unsigned long long)__float_as_uint(a.x) |
-           ((unsigned long long)__float_as_uint(a.y) << 32);
-}
-__device__ __forceinline__ float2 u2f(unsigned long long u) {
-    return make_float2(__uint_as_float((uint32_t)u), __uint_as_float((uint32_t)(u >> 32)));
-}
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    unsigned long long d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)), "l"(f2u(c)));
-    return u2f(d);
-}
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-    unsigned long long d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
-    return u2f(d);
-}
 // two bf16 packed in a word -> (element 2i, element 2i+1) as fp32 (exact)
 __device__ __forceinline__ float2 bf2(uint32_t w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));

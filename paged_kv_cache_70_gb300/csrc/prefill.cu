@@ -15,7 +15,7 @@
 // GB300 design, one CTA per (128-query tile, pair of query heads of one KV
 // head, request) -- two Q tiles A and B that read the same K/V stream:
 //   warp 8   TMA producer: K and V tiles of 128 keys x 128 dims (bf16) into
-//            separate 2-stage rings, 128-byte swizzle; a tile is assembled from
+//            separate rings (3 K stages, 2 V stages), 128-byte swizzle; a tile is assembled from
 //            one box per page piece (min(B,128) rows) addressed through the
 //            block table; boxes past the request's keys use an out-of-range
 //            row and arrive zero-filled.
@@ -48,14 +48,22 @@ namespace {
 constexpr int BM = 128;  // query rows per Q tile
 constexpr int BN = 128;  // keys per K/V tile
 constexpr int HD = 128;  // head_dim
-constexpr int SK = 2;    // K ring depth
+constexpr int SK = 3;    // K ring depth
 constexpr int SV = 2;    // V ring depth
 constexpr int kThreads = 384;  // 8 softmax warps, TMA warp, MMA warp, 2 spare
+// Register split (setmaxnreg): launched at 168 per thread; the producer
+// warpgroup (warps 8-11) drops to 88 and the two softmax warpgroups rise to
+// 208: 8*208 + 4*88 = 12*168 per thread-lane, and per SM quarter (3 warps)
+// 208+208+88 <= 512 registers per lane.
+constexpr int kRegsLow = 88;
+constexpr int kRegsHigh = 208;
+static_assert(8 * kRegsHigh + 4 * kRegsLow <= 12 * 168, "register split exceeds the launch");
 constexpr int kTmemCols = 512;
 constexpr uint32_t kTileBytes = BN * HD * 2;  // 32 KiB: one Q, K or V tile
 constexpr uint32_t kRegionBytes = BN * 128;   // 16 KiB: 64 dims (128 B) x 128 rows
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // rescale when the row max grows by > 2^8
+
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t OFF_Q = 0;  // Q_A, Q_B
@@ -63,8 +71,7 @@ constexpr uint32_t OFF_K = OFF_Q + 2 * kTileBytes;
 constexpr uint32_t OFF_V = OFF_K + SK * kTileBytes;
 constexpr uint32_t OFF_BAR = OFF_V + SV * kTileBytes;
 constexpr uint32_t BAR_BYTES = 256;
-constexpr uint32_t GUARD_BYTES = 4096;  // unused tail after the barriers
-constexpr size_t kSmemBytes = OFF_BAR + BAR_BYTES + GUARD_BYTES + 1024;
+constexpr size_t kSmemBytes = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
 
 // instruction descriptors: D fp32, A/B bf16, M = N = 128
 constexpr uint32_t idesc(uint32_t b_mn_major) {
@@ -73,12 +80,6 @@ constexpr uint32_t idesc(uint32_t b_mn_major) {
 }
 constexpr uint32_t IDESC_QK = idesc(0);
 constexpr uint32_t IDESC_PV = idesc(1);
-
-// shared-memory matrix descriptor, 128-byte swizzle
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
 
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -90,24 +91,33 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
-                                         uint32_t accumulate) {
+// Shared-memory descriptors split into 32-bit halves: the high word (stride
+// byte offset, version, 128-byte swizzle) is fixed per operand layout, the low
+// word holds (leading byte offset >> 4) << 16 | (address >> 4), so stepping an
+// operand is one 32-bit add (addresses stay below 256 KiB: no carry).
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
+    return ((lbo >> 4) << 16) | ((saddr & 0x3FFFFu) >> 4);
+}
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                       uint32_t id, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(id), "r"(accumulate)
+        "mov.b64 da, {%1, %5};\n\t"
+        "mov.b64 db, {%2, %5};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(id), "r"(accumulate), "n"(kDescHi)
         : "memory");
 }
-
-// A operand from TMEM (rows in lanes, 2 bf16 per 32-bit column), B from smem
-__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                                uint32_t id, uint32_t accumulate) {
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                       uint32_t id, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
+        "mov.b64 db, {%2, %5};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(id), "r"(accumulate), "n"(kDescHi)
         : "memory");
 }
 
@@ -202,15 +212,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-    uint64_t* k_full = bars;        // [SK]
-    uint64_t* k_empty = bars + 2;   // [SK]
-    uint64_t* v_full = bars + 4;    // [SV]
-    uint64_t* v_empty = bars + 6;   // [SV]
-    uint64_t* s_full = bars + 8;    // [2] per Q tile
-    uint64_t* p_full = bars + 10;   // [2]
-    uint64_t* o_ready = bars + 12;  // [2]
-    uint64_t* q_ready = bars + 14;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+    uint64_t* k_full = bars;             // [SK]
+    uint64_t* k_empty = k_full + SK;     // [SK]
+    uint64_t* v_full = k_empty + SK;     // [SV]
+    uint64_t* v_empty = v_full + SV;     // [SV]
+    uint64_t* s_full = v_empty + SV;     // [2] per Q tile
+    uint64_t* p_full = s_full + 2;       // [2]
+    uint64_t* o_ready = p_full + 2;      // [2]
+    uint64_t* q_ready = o_ready + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.z;
@@ -276,71 +286,76 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
-    if (warp == 8) {
+    if (warp >= 8) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+      if (warp == 8) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
             const int pieces = BN / a.piece;
-            int issued = 0;
+            int issued = 0, issued_v = 0;
+            auto page_row = [&](int32_t key) -> int32_t {
+                if (key >= k_len) return a.oob_row;  // zero-filled by TMA
+                const int32_t phys = a.table[(int64_t)r * a.max_blocks + key / a.block_size];
+                if (phys < 0 || phys >= a.num_blocks) {
+                    flag_error(a.err, PKV_FLAG_BAD_BLOCK);
+                    return a.oob_row;
+                }
+                return phys * a.block_size + key % a.block_size;
+            };
             for (int j = 0; j < n_tiles; ++j) {
                 const int sk = j % SK, sv = j % SV;
                 if (!mbar_wait(&k_empty[sk], ((j / SK) & 1) ^ 1, a.err)) break;
                 mbar_arrive_expect_tx(&k_full[sk], kTileBytes);
-                int32_t rowv[BN / 8];
                 for (int p = 0; p < pieces; ++p) {
-                    const int32_t key = j * BN + p * a.piece;
-                    int32_t row = a.oob_row;
-                    if (key < k_len) {
-                        const int32_t phys = a.table[(int64_t)r * a.max_blocks + key / a.block_size];
-                        if (phys < 0 || phys >= a.num_blocks)
-                            flag_error(a.err, PKV_FLAG_BAD_BLOCK);
-                        else
-                            row = phys * a.block_size + key % a.block_size;
-                    }
-                    rowv[p] = row;
+                    const int32_t row = page_row(j * BN + p * a.piece);
                     unsigned char* kd = sm + OFF_K + sk * kTileBytes + p * a.piece * 128;
                     tma_load_3d(kd, &tmap_k, 0, kvh, row, &k_full[sk]);
                     tma_load_3d(kd + kRegionBytes, &tmap_k, 64, kvh, row, &k_full[sk]);
                 }
-                if (!mbar_wait(&v_empty[sv], ((j / SV) & 1) ^ 1, a.err)) { ++issued; break; }
+                ++issued;
+                if (!mbar_wait(&v_empty[sv], ((j / SV) & 1) ^ 1, a.err)) break;
                 mbar_arrive_expect_tx(&v_full[sv], kTileBytes);
                 for (int p = 0; p < pieces; ++p) {
+                    const int32_t row = page_row(j * BN + p * a.piece);
                     unsigned char* vd = sm + OFF_V + sv * kTileBytes + p * a.piece * 128;
-                    tma_load_3d(vd, &tmap_v, 0, kvh, rowv[p], &v_full[sv]);
-                    tma_load_3d(vd + kRegionBytes, &tmap_v, 64, kvh, rowv[p], &v_full[sv]);
+                    tma_load_3d(vd, &tmap_v, 0, kvh, row, &v_full[sv]);
+                    tma_load_3d(vd + kRegionBytes, &tmap_v, 64, kvh, row, &v_full[sv]);
                 }
-                ++issued;
+                ++issued_v;
             }
             // drain: every issued tile has landed before the CTA can exit
             for (int j = max(0, issued - SK); j < issued; ++j)
                 mbar_wait(&k_full[j % SK], (j / SK) & 1, a.err);
-            for (int j = max(0, issued - SV); j < issued; ++j)
+            for (int j = max(0, issued_v - SV); j < issued_v; ++j)
                 mbar_wait(&v_full[j % SV], (j / SV) & 1, a.err);
         }
     } else if (warp == 9) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
-            const uint32_t q_base = smem_u32(sm + OFF_Q);
             const uint32_t tm_s[2] = {tmem, tmem + 128};
             const uint32_t tm_o[2] = {tmem + 256, tmem + 384};
             const int nx = has_b ? 2 : 1;
+            // descriptor low words of k-step 0; k-step k adds (k>>2)*16 KiB + (k&3)*32 B
+            // (K-major) or k*2 KiB (V, MN-major), in 16-byte units
+            const uint32_t q_lo0 = desc_lo(smem_u32(sm + OFF_Q), 16);
+            const uint32_t k_lo0 = desc_lo(smem_u32(sm + OFF_K), 16);
+            const uint32_t v_lo0 = desc_lo(smem_u32(sm + OFF_V), kRegionBytes);
             auto qk = [&](int x, int sk) {
-                const uint32_t k_base = smem_u32(sm + OFF_K + sk * kTileBytes);
+                const uint32_t qa = q_lo0 + x * (kTileBytes >> 4);
+                const uint32_t kb = k_lo0 + sk * (kTileBytes >> 4);
 #pragma unroll
                 for (int k = 0; k < HD / 16; ++k) {
-                    const uint32_t off = (k >> 2) * kRegionBytes + (k & 3) * 32;
-                    mma_bf16(tm_s[x], sdesc(q_base + x * kTileBytes + off, 16, 1024),
-                             sdesc(k_base + off, 16, 1024), IDESC_QK, k > 0);
+                    const uint32_t off = ((k >> 2) * kRegionBytes + (k & 3) * 32) >> 4;
+                    mma_ss(tm_s[x], qa + off, kb + off, IDESC_QK, k > 0);
                 }
                 mma_commit(&s_full[x]);
             };
             auto pv = [&](int x, int sv, bool first) {
-                const uint32_t v_base = smem_u32(sm + OFF_V + sv * kTileBytes);
+                const uint32_t vb = v_lo0 + sv * (kTileBytes >> 4);
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k)
-                    mma_bf16_tmem_a(tm_o[x], tm_s[x] + k * 8,
-                                    sdesc(v_base + k * 2048, kRegionBytes, 1024), IDESC_PV,
-                                    (!first || k > 0) ? 1u : 0u);
+                    mma_ts(tm_o[x], tm_s[x] + k * 8, vb + k * (2048 >> 4), IDESC_PV,
+                           (!first || k > 0) ? 1u : 0u);
                 mma_commit(&o_ready[x]);
             };
             bool ok = mbar_wait(q_ready, 0, a.err) && mbar_wait(&k_full[0], 0, a.err);
@@ -353,19 +368,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const int sv = j % SV, sk1 = (j + 1) % SK;
                 const bool more = j + 1 < n_tiles;
                 if (!(ok = mbar_wait(&v_full[sv], (j / SV) & 1, a.err))) break;
-                if (more && !(ok = mbar_wait(&k_full[sk1], ((j + 1) / SK) & 1, a.err))) break;
                 for (int x = 0; x < nx; ++x) {
                     if (!(ok = mbar_wait(&p_full[x], j & 1, a.err))) break;
                     tc_fence_after();
                     pv(x, sv, j == 0);
-                    if (more) qk(x, sk1);
+                    if (more) {
+                        // K(j+1) is needed only now, not before PV(j)
+                        if (x == 0 && !(ok = mbar_wait(&k_full[sk1], ((j + 1) / SK) & 1, a.err)))
+                            break;
+                        tc_fence_after();
+                        qk(x, sk1);
+                    }
                 }
                 if (!ok) break;
                 mma_commit(&v_empty[sv]);
                 if (more) mma_commit(&k_empty[sk1]);
             }
         }
-    } else if (warp < 8 && (warp < 4 || has_b)) {
+    }
+    } else {
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+      if (warp < 4 || has_b) {
         // ------------------------------ softmax warps ------------------------------
         const int x = warp >> 2;        // Q tile: 0 = A, 1 = B
         const int t = threadIdx.x & 127;  // query row in the tile == TMEM lane
@@ -409,9 +432,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 for (int c = 0; c < BN; ++c)
                     if (key0 + c > lim) sr[c] = __float_as_uint(-INFINITY);
             }
-            float mx = -INFINITY;
+            // row max as 8 independent chains (short dependency depth)
+            float mxv[8];
 #pragma unroll
-            for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+            for (int u = 0; u < 8; ++u) mxv[u] = fmaxf(__uint_as_float(sr[u]), __uint_as_float(sr[8 + u]));
+#pragma unroll
+            for (int c = 16; c < BN; c += 16)
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    mxv[u] = fmax3(mxv[u], __uint_as_float(sr[c + u]), __uint_as_float(sr[c + 8 + u]));
+            const float mx = fmax3(fmax3(mxv[0], mxv[1], mxv[2]), fmax3(mxv[3], mxv[4], mxv[5]),
+                                   fmaxf(mxv[6], mxv[7]));
             const float m_new = fmaxf(m_ref, mx);
             // rescale only when the maximum grew by more than 2^kRescaleLog2
             const bool resc = (m_new - m_ref) * sl > kRescaleLog2;  // false when both -inf
@@ -421,16 +452,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 m_ref = m_new;
             }
             const float ms = (m_ref == -INFINITY) ? 0.f : m_ref * sl;
-            float sum = 0.f;
+            const float2 sl2 = make_float2(sl, sl), nms2 = make_float2(-ms, -ms);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
             uint32_t* pk = sr;  // packed bf16 pairs overwrite the consumed scores
 #pragma unroll
-            for (int c = 0; c < BN; c += 2) {
-                const float p0 = ex2(fmaf(__uint_as_float(sr[c]), sl, -ms));
-                const float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), sl, -ms));
-                sum += p0 + p1;
-                pk[c >> 1] = pack_bf16x2(p0, p1);
+            for (int pr = 0; pr < BN / 2; ++pr) {
+                const float2 x2 = ffma2(
+                    make_float2(__uint_as_float(sr[2 * pr]), __uint_as_float(sr[2 * pr + 1])),
+                    sl2, nms2);
+                const float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+                acc[pr & 3] = fadd2(acc[pr & 3], p2);
+                pk[pr] = pack_bf16x2(p2.x, p2.y);
             }
-            l = l * alpha + sum;
+            const float2 acc01 = fadd2(acc[0], acc[1]), acc23 = fadd2(acc[2], acc[3]);
+            const float2 acct = fadd2(acc01, acc23);
+            l = l * alpha + (acct.x + acct.y);
             tmem_st32(tm_s, pk);
             tmem_st32(tm_s + 32, pk + 32);
             if (j > 0 && __any_sync(0xffffffffu, resc)) {
@@ -488,6 +525,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
             }
         }
+      }
     }
     tc_fence_before();
     __syncthreads();
