@@ -218,7 +218,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     uint64_t* v_empty = v_full + SV;     // [SV]
     uint64_t* s_full = v_empty + SV;     // [2] per Q tile
     uint64_t* p_full = s_full + 2;       // [2]
-    uint64_t* o_ready = p_full + 2;      // [2]
+    uint64_t* o_ready = p_full + 2;      // [2] last PV of the tile done
     uint64_t* q_ready = o_ready + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
 
@@ -350,13 +350,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
                 mma_commit(&s_full[x]);
             };
-            auto pv = [&](int x, int sv, bool first) {
+            // A commit tracks every earlier MMA of this thread, so S(j) being
+            // complete implies PV(j-1) is: O needs its own signal only after the
+            // last PV (for the epilogue).
+            auto pv = [&](int x, int sv, bool first, bool last) {
                 const uint32_t vb = v_lo0 + sv * (kTileBytes >> 4);
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k)
                     mma_ts(tm_o[x], tm_s[x] + k * 8, vb + k * (2048 >> 4), IDESC_PV,
                            (!first || k > 0) ? 1u : 0u);
-                mma_commit(&o_ready[x]);
+                if (last) mma_commit(&o_ready[x]);
             };
             bool ok = mbar_wait(q_ready, 0, a.err) && mbar_wait(&k_full[0], 0, a.err);
             if (ok) {
@@ -371,7 +374,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 for (int x = 0; x < nx; ++x) {
                     if (!(ok = mbar_wait(&p_full[x], j & 1, a.err))) break;
                     tc_fence_after();
-                    pv(x, sv, j == 0);
+                    pv(x, sv, j == 0, !more);
                     if (more) {
                         // K(j+1) is needed only now, not before PV(j)
                         if (x == 0 && !(ok = mbar_wait(&k_full[sk1], ((j + 1) / SK) & 1, a.err)))
@@ -471,9 +474,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             tmem_st32(tm_s, pk);
             tmem_st32(tm_s + 32, pk + 32);
             if (j > 0 && __any_sync(0xffffffffu, resc)) {
-                // PV(j-1) done: O stable; scale it before PV(j) accumulates
-                if (!warp_wait(&o_ready[x], (j - 1) & 1, a.err)) { ok = false; break; }
-                tc_fence_after();
+                // S(j) is complete, hence PV(j-1) too: O is stable; scale it
+                // before PV(j) accumulates
 #pragma unroll
                 for (int c = 0; c < HD / 32; ++c) {
                     uint32_t o[32];
@@ -502,7 +504,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[x]);
         }
-        if (ok) ok = warp_wait(&o_ready[x], (n_tiles - 1) & 1, a.err);
+        if (ok) ok = warp_wait(&o_ready[x], 0, a.err);  // last PV done
         if (ok) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
