@@ -14,11 +14,14 @@
 //
 // GB300 design, one CTA per (128-query tile, pair of query heads of one KV
 // head, request) -- two Q tiles A and B that read the same K/V stream:
-//   warp 8   TMA producer: K and V tiles of 128 keys x 128 dims (bf16) into
-//            separate rings (3 K stages, 2 V stages), 128-byte swizzle; a tile is assembled from
-//            one box per page piece (min(B,128) rows) addressed through the
-//            block table; boxes past the request's keys use an out-of-range
-//            row and arrive zero-filled.
+//   warp 8   TMA producer: first the two Q tiles (one box per 64 dims,
+//            ending at the tile's last query row so that a ragged tile never
+//            reads past its request), then K and V tiles of 128 keys x 128
+//            dims (bf16) into separate rings (3 K stages, 2 V stages),
+//            128-byte swizzle; a K/V tile is assembled from one box per page
+//            piece (min(B,128) rows) addressed through the block table; boxes
+//            past the request's keys use an out-of-range row and arrive
+//            zero-filled.
 //   warp 9   owns TMEM (512 columns: S_A, S_B, O_A, O_B, 128 each) and issues
 //            every tcgen05.mma: S_X = Q_X K^T (both operands K-major in shared
 //            memory), O_X += P_X V with P_X read from TMEM (the bf16 P tile
@@ -31,11 +34,13 @@
 //            one FMA and one MUFU op per element.  m_ref is a lagging reference
 //            maximum: it (and O, l) is rescaled only when the row maximum grows
 //            by more than 2^8, so p <= 256 and the final o/l is unchanged.
-//   The epilogue divides O by l and stores bf16 rows.
+//   The epilogue divides O by l, stages the bf16 rows in the (now dead) Q
+//   tile and stores them with coalesced 16-byte writes.
 // Every mbarrier wait is time-limited; a timeout sets PKV_FLAG_TIMEOUT and the
 // CTA drains its copies and frees TMEM before returning.
 #include <cuda.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -182,7 +187,6 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 }
 
 struct PrefillArgs {
-    const uint16_t* q;
     uint16_t* out;
     const int32_t* cu_q;
     const int32_t* cu_k;
@@ -206,7 +210,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsign
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                  const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -240,6 +245,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int32_t q0 = qt * BM;
     if (q0 >= q_len) return;
     const int rows = min(BM, q_len - q0);
+    // The Q box always ends at the tile's last query row, so a ragged tile
+    // (rows < 128) starts `shift` rows early: smem row / TMEM lane t holds
+    // query q0 + t - shift, and lanes below `shift` are not stored.
+    const int shift = BM - rows;
+    const int32_t box_row0 = cq0 + q0 + rows - BM;  // negative rows arrive zero-filled
     const int32_t diag = k_len - q_len;  // query i sees key j <= i + diag
     int32_t last_key = k_len - 1;
     if (a.causal) last_key = min(last_key, q0 + rows - 1 + diag);
@@ -272,7 +282,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             mbar_init(&p_full[x], 4);
             mbar_init(&o_ready[x], 1);
         }
-        mbar_init(q_ready, has_b ? 8 : 4);
+        mbar_init(q_ready, 1);
         fence_barrier_init();
     }
     if (warp == 9) {
@@ -302,6 +312,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
                 return phys * a.block_size + key % a.block_size;
             };
+            const int nq = has_b ? 2 : 1;
+            mbar_arrive_expect_tx(q_ready, nq * kTileBytes);
+            for (int x = 0; x < nq; ++x) {
+                unsigned char* qd = sm + OFF_Q + x * kTileBytes;
+                tma_load_3d(qd, &tmap_q, 0, h_a + x, box_row0, q_ready);
+                tma_load_3d(qd + kRegionBytes, &tmap_q, 64, h_a + x, box_row0, q_ready);
+            }
             for (int j = 0; j < n_tiles; ++j) {
                 const int sk = j % SK, sv = j % SV;
                 if (!mbar_wait(&k_empty[sk], ((j / SK) & 1) ^ 1, a.err)) break;
@@ -324,6 +341,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 ++issued_v;
             }
             // drain: every issued tile has landed before the CTA can exit
+            mbar_wait(q_ready, 0, a.err);
             for (int j = max(0, issued - SK); j < issued; ++j)
                 mbar_wait(&k_full[j % SK], (j / SK) & 1, a.err);
             for (int j = max(0, issued_v - SV); j < issued_v; ++j)
@@ -399,23 +417,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tm_s = tmem + x * 128 + lane_base;
         const uint32_t tm_o = tmem + 256 + x * 128 + lane_base;
-        {   // Q row t -> swizzled shared tile (zeros past the request)
-            unsigned char* qs = sm + OFF_Q + x * kTileBytes;
-            const bool valid = t < rows;
-            // rows past the request read row 0 of the tile (always in bounds), then zero it
-            const int64_t qrow = out_row0 + (valid ? t : 0);
-            const uint4* src = reinterpret_cast<const uint4*>(a.q + (qrow * a.hq + h) * HD);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                uint4 v = __ldg(src + c);
-                if (!valid) v = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(qs + swz(t, c)) = v;
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(q_ready);
-        }
-        const int32_t row_i = q0 + t;  // query index within the request
+        const int32_t row_i = q0 + t - shift;  // query index within the request
         int32_t lim = k_len - 1;
         if (a.causal) lim = min(lim, row_i + diag);
         const float sl = a.scale_log2;
@@ -505,26 +507,38 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             if (lane == 0) mbar_arrive(&p_full[x]);
         }
         if (ok) ok = warp_wait(&o_ready[x], 0, a.err);  // last PV done
+        // Epilogue: O / l as bf16 rows staged in this tile's Q buffer (its
+        // last reader, QK of the final K tile, completed before o_ready),
+        // then stored with coalesced 16-byte writes, 16 threads per row.
+        unsigned char* stage = sm + OFF_Q + x * kTileBytes;
         if (ok) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint16_t* dst = a.out + ((out_row0 + t) * a.hq + h) * HD;
 #pragma unroll
             for (int c = 0; c < HD / 32; ++c) {
                 uint32_t o[32];
                 tmem_ld32(tm_o + c * 32, o);
                 tmem_wait_ld();
-                if (t < rows) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-                        *reinterpret_cast<uint4*>(dst + c * 32 + e) = w;
-                    }
+                for (int e = 0; e < 32; e += 8) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                    *reinterpret_cast<uint4*>(stage + swz(t, c * 4 + e / 8)) = w;
                 }
+            }
+        }
+        asm volatile("bar.sync %0, 128;" ::"r"(1 + x) : "memory");  // the tile's 4 warps
+        if (ok) {
+#pragma unroll 4
+            for (int i = t; i < BM * (HD / 8); i += 128) {
+                const int rr = i >> 4, c = i & 15;
+                if (rr >= shift)
+                    *reinterpret_cast<uint4*>(a.out + ((out_row0 + rr - shift) * a.hq + h) * HD +
+                                              c * 8) =
+                        *reinterpret_cast<const uint4*>(stage + swz(rr, c));
             }
         }
       }
@@ -561,9 +575,10 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// pool [num_blocks*B rows, Hkv, 128] bf16 viewed as 3-D (dim, head, row); box
-// (64 dims, 1 head, piece rows), 128-byte swizzle
-bool make_pool_map(CUtensorMap* map, const void* base, int hkv, int64_t rows, int piece) {
+// [rows, heads, 128] bf16 viewed as 3-D (dim, head, row); box (64 dims, 1
+// head, piece rows), 128-byte swizzle.  Serves the K/V pools (rows = slots)
+// and q (rows = query tokens, piece = 128).
+bool make_rows_map(CUtensorMap* map, const void* base, int hkv, int64_t rows, int piece) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)hkv, (cuuint64_t)rows};
@@ -599,12 +614,15 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
     const int64_t rows = num_blocks * block_size;
     if (rows + 128 > 0x7fffffffLL) return cudaErrorNotSupported;
     const int piece = block_size < BN ? block_size : BN;
-    CUtensorMap mk, mv;
-    if (!make_pool_map(&mk, k_cache, hkv, rows, piece) ||
-        !make_pool_map(&mv, v_cache, hkv, rows, piece))
+    // q holds at most batch * max_seqlen_q rows; no box reaches past the
+    // last row of its own request, so this bound never clips a valid row
+    const int64_t q_rows = std::min<int64_t>((int64_t)batch * max_seqlen_q, 0x7fffffffLL);
+    CUtensorMap mq, mk, mv;
+    if (!make_rows_map(&mq, q, hq, q_rows, BM) ||
+        !make_rows_map(&mk, k_cache, hkv, rows, piece) ||
+        !make_rows_map(&mv, v_cache, hkv, rows, piece))
         return cudaErrorInvalidValue;
     PrefillArgs a;
-    a.q = static_cast<const uint16_t*>(q);
     a.out = static_cast<uint16_t*>(out);
     a.cu_q = cu_q;
     a.cu_k = cu_k;
@@ -626,7 +644,7 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(a.tiles_q, a.pair_heads ? (hq + 1) / 2 : hq, batch);
-    prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mk, mv, a);
+    prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, a);
     return cudaGetLastError();
 }
 
