@@ -34,8 +34,13 @@
 //            one FMA and one MUFU op per element.  m_ref is a lagging reference
 //            maximum: it (and O, l) is rescaled only when the row maximum grows
 //            by more than 2^8, so p <= 256 and the final o/l is unchanged.
-//   The epilogue divides O by l, stages the bf16 rows in the (now dead) Q
-//   tile and stores them with coalesced 16-byte writes.
+//            Once a reference exists, the exponentials run before any max is
+//            taken: a tile whose row sum stays <= 2^8 cannot hold a p > 2^8,
+//            and only otherwise is the row max read again from TMEM (S is
+//            still there) to decide whether to move the reference and redo.
+//   The epilogue divides O by l and stages the bf16 rows in the (now dead)
+//   Q tile; a full tile leaves by two TMA boxes, a ragged one with coalesced
+//   16-byte writes of its valid rows.
 // Every mbarrier wait is time-limited; a timeout sets PKV_FLAG_TIMEOUT and the
 // CTA drains its copies and frees TMEM before returning.
 #include <cuda.h>
@@ -179,6 +184,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// shared -> global TMA store of one box (completion tracked by bulk groups)
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x,
+                                             int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
 // byte offset of 16-byte chunk `c` (0..15) of row `r` in a 128-row x 256-byte
 // tile stored as two 128-byte-swizzled regions (the layout TMA writes with
 // CU_TENSOR_MAP_SWIZZLE_128B and the MMA reads as a K-major operand)
@@ -211,6 +226,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsign
 
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                  const __grid_constant__ CUtensorMap tmap_o,
                   const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
     extern __shared__ unsigned char smem_raw[];
@@ -432,47 +448,89 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
             for (int c = 0; c < BN / 32; ++c) tmem_ld32(tm_s + c * 32, sr + c * 32);
             tmem_wait_ld();
             const int32_t key0 = j * BN;
-            if (__any_sync(0xffffffffu, key0 + BN - 1 > lim)) {
+            const bool ragged = __any_sync(0xffffffffu, key0 + BN - 1 > lim);
+            auto mask = [&](uint32_t* v, int c0, int n) {
 #pragma unroll
-                for (int c = 0; c < BN; ++c)
-                    if (key0 + c > lim) sr[c] = __float_as_uint(-INFINITY);
-            }
-            // row max as 8 independent chains (short dependency depth)
-            float mxv[8];
+                for (int c = 0; c < n; ++c)
+                    if (key0 + c0 + c > lim) v[c] = __float_as_uint(-INFINITY);
+            };
+            if (ragged) mask(sr, 0, BN);
+            // p = 2^(s*scale*log2e - m_ref*scale*log2e) in place (bf16 pairs
+            // into sr[0..63]); returns the row sum of this tile
+            auto exp_pass = [&]() -> float {
+                const float ms = (m_ref == -INFINITY) ? 0.f : m_ref * sl;
+                const float2 sl2 = make_float2(sl, sl), nms2 = make_float2(-ms, -ms);
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int u = 0; u < 8; ++u) mxv[u] = fmaxf(__uint_as_float(sr[u]), __uint_as_float(sr[8 + u]));
-#pragma unroll
-            for (int c = 16; c < BN; c += 16)
+                for (int pr = 0; pr < BN / 2; ++pr) {
+                    const float2 x2 = ffma2(make_float2(__uint_as_float(sr[2 * pr]),
+                                                        __uint_as_float(sr[2 * pr + 1])),
+                                            sl2, nms2);
+                    const float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+                    acc[pr & 3] = fadd2(acc[pr & 3], p2);
+                    sr[pr] = pack_bf16x2(p2.x, p2.y);
+                }
+                const float2 acct = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+                return acct.x + acct.y;
+            };
+            // move the reference to max(m_ref, mx) only when that grows it by
+            // more than 2^kRescaleLog2 (false when both are -inf)
+            bool resc = false;
+            float alpha = 1.f;
+            auto update_ref = [&](float mx) {
+                const float m_new = fmaxf(m_ref, mx);
+                resc = (m_new - m_ref) * sl > kRescaleLog2;
+                if (resc) {
+                    alpha = (m_ref == -INFINITY) ? 0.f : ex2((m_ref - m_new) * sl);
+                    m_ref = m_new;
+                }
+            };
+            float psum;
+            if (__any_sync(0xffffffffu, m_ref == -INFINITY)) {
+                // no reference yet: the row max first (8 independent chains)
+                float mxv[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                    mxv[u] = fmax3(mxv[u], __uint_as_float(sr[c + u]), __uint_as_float(sr[c + 8 + u]));
-            const float mx = fmax3(fmax3(mxv[0], mxv[1], mxv[2]), fmax3(mxv[3], mxv[4], mxv[5]),
-                                   fmaxf(mxv[6], mxv[7]));
-            const float m_new = fmaxf(m_ref, mx);
-            // rescale only when the maximum grew by more than 2^kRescaleLog2
-            const bool resc = (m_new - m_ref) * sl > kRescaleLog2;  // false when both -inf
-            float alpha = 1.f;
-            if (resc) {
-                alpha = (m_ref == -INFINITY) ? 0.f : ex2((m_ref - m_new) * sl);
-                m_ref = m_new;
-            }
-            const float ms = (m_ref == -INFINITY) ? 0.f : m_ref * sl;
-            const float2 sl2 = make_float2(sl, sl), nms2 = make_float2(-ms, -ms);
-            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                             make_float2(0.f, 0.f)};
-            uint32_t* pk = sr;  // packed bf16 pairs overwrite the consumed scores
+                    mxv[u] = fmaxf(__uint_as_float(sr[u]), __uint_as_float(sr[8 + u]));
 #pragma unroll
-            for (int pr = 0; pr < BN / 2; ++pr) {
-                const float2 x2 = ffma2(
-                    make_float2(__uint_as_float(sr[2 * pr]), __uint_as_float(sr[2 * pr + 1])),
-                    sl2, nms2);
-                const float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
-                acc[pr & 3] = fadd2(acc[pr & 3], p2);
-                pk[pr] = pack_bf16x2(p2.x, p2.y);
+                for (int c = 16; c < BN; c += 16)
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        mxv[u] = fmax3(mxv[u], __uint_as_float(sr[c + u]),
+                                       __uint_as_float(sr[c + 8 + u]));
+                update_ref(fmax3(fmax3(mxv[0], mxv[1], mxv[2]), fmax3(mxv[3], mxv[4], mxv[5]),
+                                 fmaxf(mxv[6], mxv[7])));
+                psum = exp_pass();
+            } else {
+                // speculate that the reference still holds: every p <= 2^8
+                // unless the tile's sum exceeds 2^8 (or overflowed)
+                psum = exp_pass();
+                if (__any_sync(0xffffffffu, !(psum <= 256.f))) {
+                    // S is still in TMEM: its row max decides
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(tm_s + c * 32, v);
+                        tmem_wait_ld();
+                        if (ragged) mask(v, c * 32, 32);
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2)
+                            mx = fmax3(mx, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+                    }
+                    update_ref(mx);
+                    if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+                        for (int c = 0; c < BN / 32; ++c) tmem_ld32(tm_s + c * 32, sr + c * 32);
+                        tmem_wait_ld();
+                        if (ragged) mask(sr, 0, BN);
+                        psum = exp_pass();
+                    }
+                }
             }
-            const float2 acc01 = fadd2(acc[0], acc[1]), acc23 = fadd2(acc[2], acc[3]);
-            const float2 acct = fadd2(acc01, acc23);
-            l = l * alpha + (acct.x + acct.y);
+            l = l * alpha + psum;
+            uint32_t* pk = sr;
             tmem_st32(tm_s, pk);
             tmem_st32(tm_s + 32, pk + 32);
             if (j > 0 && __any_sync(0xffffffffu, resc)) {
@@ -530,8 +588,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 }
             }
         }
+        fence_async_smem();  // the staged rows are read by TMA below
         asm volatile("bar.sync %0, 128;" ::"r"(1 + x) : "memory");  // the tile's 4 warps
-        if (ok) {
+        if (ok && shift == 0) {
+            // a full tile: two TMA boxes (64 dims x 128 rows each)
+            if (t == 0) {
+                tma_store_3d(&tmap_o, stage, 0, h, (int32_t)out_row0);
+                tma_store_3d(&tmap_o, stage + kRegionBytes, 64, h, (int32_t)out_row0);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            }
+        } else if (ok) {
 #pragma unroll 4
             for (int i = t; i < BM * (HD / 8); i += 128) {
                 const int rr = i >> 4, c = i & 15;
@@ -617,8 +684,8 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
     // q holds at most batch * max_seqlen_q rows; no box reaches past the
     // last row of its own request, so this bound never clips a valid row
     const int64_t q_rows = std::min<int64_t>((int64_t)batch * max_seqlen_q, 0x7fffffffLL);
-    CUtensorMap mq, mk, mv;
-    if (!make_rows_map(&mq, q, hq, q_rows, BM) ||
+    CUtensorMap mq, mo, mk, mv;
+    if (!make_rows_map(&mq, q, hq, q_rows, BM) || !make_rows_map(&mo, out, hq, q_rows, BM) ||
         !make_rows_map(&mk, k_cache, hkv, rows, piece) ||
         !make_rows_map(&mv, v_cache, hkv, rows, piece))
         return cudaErrorInvalidValue;
@@ -644,7 +711,7 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(a.tiles_q, a.pair_heads ? (hq + 1) / 2 : hq, batch);
-    prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, a);
+    prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mo, mk, mv, a);
     return cudaGetLastError();
 }
 

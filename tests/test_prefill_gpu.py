@@ -177,3 +177,34 @@ def test_unsupported_combinations():
     with pytest.raises(pkv.PagedKVError) as e:
         run_gpu(c)
     assert e.value.status == -2
+
+
+@pytest.mark.parametrize("step", [0.15, 0.6])
+def test_growing_scores(step):
+    """Keys whose scores rise tile by tile: each 128-key tile of row 0 lies
+    ~`step` * 16 (log2 units) above the previous one, so the softmax's row
+    sum outgrows 2^8 without the reference moving (step 0.15) and the
+    reference itself moves and O is rescaled mid-row (both steps)."""
+    rng = np.random.default_rng(21)
+    d, B, qlen, klen = 128, 64, 130, 900
+    q = rng.standard_normal((qlen, 2, d))
+    u = q[qlen - 1, 0] / np.linalg.norm(q[qlen - 1, 0])
+    gain = step * (np.arange(klen) // 128) + 0.05 * rng.standard_normal(klen)
+    k = 0.3 * rng.standard_normal((klen, 1, d)) + (gain[:, None] * u[None, :] * 12.0)[:, None, :]
+    v = rng.standard_normal((klen, 1, d))
+    nb = -(-klen // B) + 2
+    order = rng.permutation(nb).astype(np.int32)
+    table = order[: -(-klen // B)][None, :].copy()
+    kc = np.zeros((nb, B, 1, d))
+    vc = np.zeros((nb, B, 1, d))
+    for j in range(klen):
+        kc[table[0, j // B], j % B] = k[j]
+        vc[table[0, j // B], j % B] = v[j]
+    c = dict(q=_bf(q), kc=_bf(kc), vc=_bf(vc), table=table,
+             cq=np.array([0, qlen], np.int32), ck=np.array([0, klen], np.int32), B=B,
+             scale=1 / math.sqrt(d))
+    for causal in (True, False):
+        got = widen(run_gpu(c, causal))
+        assert np.all(np.isfinite(got))
+        assert_close(got, run_oracle(c, causal), "bf16", f"step {step} causal {causal}")
+    assert pkv.paged_error_flags() == 0
