@@ -44,7 +44,7 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--only", choices=["all", "decode", "prefill"], default="all",
+    p.add_argument("--only", choices=["all", "decode", "prefill", "copy"], default="all",
                    help="measure one half only (profiling runs)")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
     return p.parse_args()
@@ -435,10 +435,16 @@ def main():
         dstep = run_decode(args, world, pkv, W, hbm_peak, peak_src, line)
     if args.only in ("all", "prefill"):
         run_prefill(args, world, pkv, W, bf16_peak, peak_src, line)
+    if args.only in ("all", "copy"):
+        run_copy(args, world, pkv, hbm_peak, peak_src, line)
     if args.only == "prefill":  # headline comes from the prefill half
         line["metric"] = "varlen prefill TFLOP/s"
         line["value"], line["unit"] = line["prefill"].get("value"), "TFLOP/s"
         line["ms_per_step"] = line["prefill"].get("ms_per_step")
+    if args.only == "copy":
+        line["metric"] = line["copy_blocks"]["metric"]
+        line["value"] = line["copy_blocks"]["value"]
+        line["ms_per_step"] = line["copy_blocks"]["ms_per_step"]
     cpu_baseline(args, world, rank, W, dstep, line)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -495,6 +501,58 @@ def run_decode(args, world, pkv, W, hbm_peak, peak_src, line):
     del ddev
     torch.cuda.empty_cache()
     return dstep
+
+
+COPY_PAIRS, COPY_GEOM = 8192, (16, 8, 128)  # block pairs; B, Hkv, d (bf16)
+
+
+def run_copy(args, world, pkv, hbm_peak, peak_src, line):
+    """paged_copy_blocks: the copies of copy-on-write.  8192 block pairs of a
+    B=16, Hkv=8, d=128 bf16 pool (32 KiB per block per pool): 512 MiB read and
+    512 MiB written per launch, far beyond L2."""
+    B, hkv, d = COPY_GEOM
+    nb = 2 * COPY_PAIRS + 16
+    g = torch.Generator().manual_seed(1099)
+    k = torch.randint(-32768, 32767, (nb, B, hkv, d), generator=g, dtype=torch.int16)
+    k_cache = k.view(torch.bfloat16).cuda()
+    v_cache = torch.roll(k, 1, 0).view(torch.bfloat16).cuda()
+    perm = torch.randperm(nb, generator=g)
+    src = perm[:COPY_PAIRS].to(torch.int32).cuda()
+    dst = perm[COPY_PAIRS: 2 * COPY_PAIRS].to(torch.int32).cuda()
+    block_bytes = B * hkv * d * 2
+    nbytes = COPY_PAIRS * block_bytes * 2 * 2  # K and V, read and written
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        pkv.paged_copy_blocks(k_cache, v_cache, src, dst)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for a, b in ev:
+        a.record(stream)
+        pkv.paged_copy_blocks(k_cache, v_cache, src, dst)
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = [a.elapsed_time(b) for a, b in ev]
+    mean = max_over_ranks(float(np.mean(ms)), world)
+    gbs = nbytes / (mean * 1e-3) / 1e9
+    line["copy_blocks"] = {
+        "metric": "copy-on-write block copies GB/s", "unit": "GB/s",
+        "value": round(world * gbs, 1), "ms_per_step": round(mean, 5),
+        "workload": f"{COPY_PAIRS} block pairs, B={B}, Hkv={hkv}, d={d}, bf16 "
+                    f"({block_bytes // 1024} KiB per block per pool); step = one paged_copy_blocks",
+        "roofline": {"bound": "hbm", "kernel": "copy_blocks_kernel", "achieved": round(gbs, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                     "peak_source": peak_src, "traffic": traffic_of("copy_blocks_kernel"),
+                     "algorithmic_bytes_per_launch": nbytes, "mean_ms": round(mean, 5),
+                     "median_ms": round(float(np.median(ms)), 5)},
+        "l2": "inputs larger than L2 (512 MiB read per launch)"}
+    line["gpu_launches"] += args.steps
+    line["error_flags"] |= pkv.paged_error_flags()
+    del k_cache, v_cache
+    torch.cuda.empty_cache()
 
 
 def run_prefill(args, world, pkv, W, bf16_peak, peak_src, line):

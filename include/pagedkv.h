@@ -59,6 +59,7 @@ typedef enum pkv_dtype { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_ERR_UNSUPPORTED (-2) /* valid but not implemented (dtype/head_dim/GQA combo) */
 #define PKV_ERR_WORKSPACE (-3)   /* workspace missing or smaller than the *_workspace_size */
 #define PKV_ERR_CUDA (-4)        /* a CUDA runtime call or kernel launch failed */
+#define PKV_ERR_NO_SPACE (-5)    /* block manager: not enough free blocks (nothing changed) */
 
 /* device error-word bits (paged_error_flags) */
 #define PKV_FLAG_BAD_BLOCK (1u << 0)   /* block-table entry outside [0, num_blocks) */
@@ -203,6 +204,79 @@ int paged_decode_noalloc(const void* q, const void* k_cache, const void* v_cache
  * the word.
  */
 int paged_error_flags(uint32_t* flags, int32_t clear);
+
+/*
+ * Block manager (host side) and block copies -- "11. Paged attention 与 online
+ * softmax" §11.3 (block sharing, copy-on-write, reference counts and the free
+ * stack) and "结合nanovllm的FlashAttention和PagedAttention主要原理概述" 题目6
+ * (prefix cache: chained block hashes, a hit shares the block, release in
+ * reverse block order).
+ *
+ * A pkv_block_manager owns the bookkeeping of one pool of num_blocks blocks of
+ * block_size tokens and the sequences that hold them; it makes no CUDA call and
+ * is not thread-safe (callers serialise).  Every pointer of the paged_bm_*
+ * calls is a HOST pointer.
+ *   - refs[b] = the number of sequence block tables that contain block b; a
+ *     block with refs 0 is on the free stack (top = block 0 at creation; a
+ *     released block is pushed on top, allocation pops the top).
+ *   - Only full blocks are shared by lookup.  The cache key of block i of a
+ *     token sequence is (the physical block of block i-1, or -1; the block's
+ *     block_size token ids), compared in full: two sequences share their
+ *     leading full blocks exactly as far as their tokens agree.
+ *   - PKV_ERR_NO_SPACE leaves the manager unchanged.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* a manager of num_blocks (< 2^31) blocks of block_size (>= 1) tokens */
+int paged_bm_create(int64_t num_blocks, int32_t block_size, pkv_block_manager** out);
+int paged_bm_destroy(pkv_block_manager* bm);
+
+/* New sequence holding tokens[0 .. n_tokens): its leading full blocks that are
+ * cached are shared (refs +1), the rest are allocated (refs 1) and the full
+ * ones cached.  *seq_out: the sequence id; *cached_tokens_out (may be NULL):
+ * tokens in shared blocks, i.e. tokens whose K/V are already in the pool. */
+int paged_bm_allocate(pkv_block_manager* bm, const int64_t* tokens, int64_t n_tokens,
+                      int64_t* seq_out, int64_t* cached_tokens_out);
+
+/* New sequence with the same tokens and blocks as `seq` (every block refs +1). */
+int paged_bm_fork(pkv_block_manager* bm, int64_t seq, int64_t* child_out);
+
+/* One more token for `seq`.  A full last block gets a new block after it; a
+ * partial last block that is shared (refs > 1) is replaced by a new block the
+ * sequence owns and *cow_src_out / *cow_dst_out name the block whose contents
+ * must be copied first (paged_copy_blocks) -- otherwise both are -1.  A block
+ * that the token fills enters the cache. */
+int paged_bm_append(pkv_block_manager* bm, int64_t seq, int64_t token, int32_t* cow_src_out,
+                    int32_t* cow_dst_out);
+
+/* Release a sequence: its blocks in reverse order, refs -1 each; a block at 0
+ * leaves the cache and is pushed on the free stack. */
+int paged_bm_free(pkv_block_manager* bm, int64_t seq);
+
+/* The sequence's block table (host int32 array of `capacity` entries);
+ * *n_blocks_out receives its length (also when capacity is too small, which
+ * returns PKV_ERR_INVALID). */
+int paged_bm_block_table(const pkv_block_manager* bm, int64_t seq, int32_t* table_out,
+                         int32_t capacity, int32_t* n_blocks_out);
+int paged_bm_seq_len(const pkv_block_manager* bm, int64_t seq, int64_t* len_out);
+int paged_bm_ref_count(const pkv_block_manager* bm, int32_t block, int32_t* ref_out);
+
+/* The free stack, bottom first, into stack_out[capacity] (NULL: count only);
+ * *n_out receives the number of free blocks. */
+int paged_bm_free_blocks(const pkv_block_manager* bm, int32_t* stack_out, int64_t capacity,
+                         int64_t* n_out);
+
+/*
+ * paged_copy_blocks -- the copies a copy-on-write needs (§11.3: the old
+ * contents go into the new block before the write).  For i < n_pairs, block
+ * dst[i] of both pools becomes a bitwise copy of block src[i] (block_size *
+ * kvDim elements of geom->dtype).  src, dst: DEVICE int32 arrays; a dst block
+ * must not also be a src block or appear twice (the result is unspecified
+ * then).  An id outside [0, num_blocks) skips the pair and sets
+ * PKV_FLAG_BAD_BLOCK.
+ */
+int paged_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst,
+                      int32_t n_pairs, const pkv_geom* geom, cudaStream_t stream);
 
 /* paged_status_string -- static text for a PKV_* status code. */
 const char* paged_status_string(int status);

@@ -7,6 +7,9 @@ raises if the library has not been built.
 """
 from ._binding import (  # noqa: F401
     EXPORTED,
+    PKV_ERR_NO_SPACE,
+    BlockManager,
+    paged_copy_blocks,
     LIB_PATH,
     PKV_BF16,
     PKV_F32,

@@ -36,7 +36,19 @@ EXPORTED = (
     "paged_error_flags",
     "paged_status_string",
     "paged_decode_noalloc",
+    "paged_bm_create",
+    "paged_bm_destroy",
+    "paged_bm_allocate",
+    "paged_bm_fork",
+    "paged_bm_append",
+    "paged_bm_free",
+    "paged_bm_block_table",
+    "paged_bm_seq_len",
+    "paged_bm_ref_count",
+    "paged_bm_free_blocks",
+    "paged_copy_blocks",
 )
+PKV_ERR_NO_SPACE = -5
 
 
 class PagedKVError(RuntimeError):
@@ -95,6 +107,22 @@ def load_library(path: str | None = None):
         lib.paged_decode_noalloc.restype = ctypes.c_int
         lib.paged_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         lib.paged_error_flags.restype = ctypes.c_int
+        pp, i64p, i32p = ctypes.POINTER(vp), ctypes.POINTER(i64), ctypes.POINTER(i32)
+        lib.paged_bm_create.argtypes = [i64, i32, pp]
+        lib.paged_bm_destroy.argtypes = [vp]
+        lib.paged_bm_allocate.argtypes = [vp, vp, i64, i64p, i64p]
+        lib.paged_bm_fork.argtypes = [vp, i64, i64p]
+        lib.paged_bm_append.argtypes = [vp, i64, i64, i32p, i32p]
+        lib.paged_bm_free.argtypes = [vp, i64]
+        lib.paged_bm_block_table.argtypes = [vp, i64, vp, i32, i32p]
+        lib.paged_bm_seq_len.argtypes = [vp, i64, i64p]
+        lib.paged_bm_ref_count.argtypes = [vp, i32, i32p]
+        lib.paged_bm_free_blocks.argtypes = [vp, vp, i64, i64p]
+        for f in ("create", "destroy", "allocate", "fork", "append", "free", "block_table",
+                  "seq_len", "ref_count", "free_blocks"):
+            getattr(lib, "paged_bm_" + f).restype = ctypes.c_int
+        lib.paged_copy_blocks.argtypes = [vp, vp, vp, vp, i32, gp, vp]
+        lib.paged_copy_blocks.restype = ctypes.c_int
         lib.paged_status_string.argtypes = [ctypes.c_int]
         lib.paged_status_string.restype = ctypes.c_char_p
         if path is None:
@@ -285,3 +313,104 @@ def paged_error_flags(clear: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _check("paged_error_flags", load_library().paged_error_flags(ctypes.byref(v), 1 if clear else 0))
     return int(v.value)
+
+
+class BlockManager:
+    """Host-side block manager of one pool (reference counts, free stack,
+    prefix sharing of full blocks, copy-on-write), a handle on the library's
+    native manager (include/pagedkv.h, paged_bm_*)."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self._lib = load_library()
+        h = ctypes.c_void_p()
+        _check("paged_bm_create", self._lib.paged_bm_create(num_blocks, block_size,
+                                                            ctypes.byref(h)))
+        self._h = h
+        self.num_blocks, self.block_size = num_blocks, block_size
+
+    def close(self) -> None:
+        if self._h:
+            self._lib.paged_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):  # pragma: no cover - interpreter shutdown order
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def allocate(self, tokens) -> tuple[int, int]:
+        """New sequence; returns (sequence id, tokens already cached)."""
+        arr = (ctypes.c_int64 * max(1, len(tokens)))(*[int(t) for t in tokens])
+        sid, cached = ctypes.c_int64(), ctypes.c_int64()
+        _check("paged_bm_allocate", self._lib.paged_bm_allocate(
+            self._h, ctypes.cast(arr, ctypes.c_void_p), len(tokens), ctypes.byref(sid),
+            ctypes.byref(cached)))
+        return sid.value, cached.value
+
+    def fork(self, seq: int) -> int:
+        c = ctypes.c_int64()
+        _check("paged_bm_fork", self._lib.paged_bm_fork(self._h, seq, ctypes.byref(c)))
+        return c.value
+
+    def append(self, seq: int, token: int) -> tuple[int, int]:
+        """Returns the (src, dst) block copy the write needs first, or (-1, -1)."""
+        s, d = ctypes.c_int32(), ctypes.c_int32()
+        _check("paged_bm_append", self._lib.paged_bm_append(self._h, seq, int(token),
+                                                            ctypes.byref(s), ctypes.byref(d)))
+        return s.value, d.value
+
+    def free(self, seq: int) -> None:
+        _check("paged_bm_free", self._lib.paged_bm_free(self._h, seq))
+
+    def table(self, seq: int) -> list[int]:
+        n = ctypes.c_int32()
+        self._lib.paged_bm_block_table(self._h, seq, None, 0, ctypes.byref(n))
+        buf = (ctypes.c_int32 * max(1, n.value))()
+        _check("paged_bm_block_table", self._lib.paged_bm_block_table(
+            self._h, seq, ctypes.cast(buf, ctypes.c_void_p), n.value, ctypes.byref(n)))
+        return list(buf[: n.value])
+
+    def seq_len(self, seq: int) -> int:
+        n = ctypes.c_int64()
+        _check("paged_bm_seq_len", self._lib.paged_bm_seq_len(self._h, seq, ctypes.byref(n)))
+        return n.value
+
+    def ref_count(self, block: int) -> int:
+        r = ctypes.c_int32()
+        _check("paged_bm_ref_count", self._lib.paged_bm_ref_count(self._h, block,
+                                                                  ctypes.byref(r)))
+        return r.value
+
+    def free_stack(self) -> list[int]:
+        """Free blocks, bottom of the stack first."""
+        n = ctypes.c_int64()
+        _check("paged_bm_free_blocks", self._lib.paged_bm_free_blocks(self._h, None, 0,
+                                                                      ctypes.byref(n)))
+        buf = (ctypes.c_int32 * max(1, n.value))()
+        _check("paged_bm_free_blocks", self._lib.paged_bm_free_blocks(
+            self._h, ctypes.cast(buf, ctypes.c_void_p), n.value, ctypes.byref(n)))
+        return list(buf[: n.value])
+
+    def num_free(self) -> int:
+        n = ctypes.c_int64()
+        _check("paged_bm_free_blocks", self._lib.paged_bm_free_blocks(self._h, None, 0,
+                                                                      ctypes.byref(n)))
+        return n.value
+
+
+def paged_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src: torch.Tensor,
+                      dst: torch.Tensor) -> None:
+    """Block dst[i] of both pools becomes a copy of block src[i] (int32 CUDA
+    tensors): the copies a copy-on-write needs."""
+    _cuda_contig("k_cache", k_cache)
+    _cuda_contig("v_cache", v_cache, k_cache.dtype)
+    _cuda_contig("src", src, torch.int32)
+    _cuda_contig("dst", dst, torch.int32)
+    if src.numel() != dst.numel() or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch")
+    g = geom_of(k_cache, k_cache.shape[2])
+    with torch.cuda.device(k_cache.device):
+        st = load_library().paged_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(src), _ptr(dst),
+                                              src.numel(), ctypes.byref(g), _stream(k_cache))
+    _check("paged_copy_blocks", st)

@@ -181,6 +181,21 @@ int paged_varlen_prefill(const void* q, const void* k_cache, const void* v_cache
     return cuda_status(e);
 }
 
+int paged_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst,
+                      int32_t n_pairs, const pkv_geom* geom, cudaStream_t stream) {
+    int st = check_geom(geom);
+    if (st != PKV_OK) return st;
+    if (n_pairs < 0 || n_pairs > 65535) return n_pairs < 0 ? PKV_ERR_INVALID : PKV_ERR_UNSUPPORTED;
+    if (n_pairs == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !src || !dst) return PKV_ERR_INVALID;
+    DeviceInfo dev;
+    if (pkv::current_device_info(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    const int64_t block_bytes = (int64_t)geom->block_size * geom->num_kv_heads * geom->head_dim *
+                                elt_size(geom->dtype);
+    return cuda_status(pkv::launch_copy_blocks(k_cache, v_cache, src, dst, n_pairs, block_bytes,
+                                               geom->num_blocks, dev.err, stream));
+}
+
 int paged_error_flags(uint32_t* flags, int32_t clear) {
     if (!flags) return PKV_ERR_INVALID;
     DeviceInfo dev;
@@ -204,6 +219,7 @@ const char* paged_status_string(int status) {
         case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
         case PKV_ERR_WORKSPACE: return "workspace missing or too small";
         case PKV_ERR_CUDA: return "CUDA error";
+        case PKV_ERR_NO_SPACE: return "not enough free blocks";
         default: return "unknown status";
     }
 }

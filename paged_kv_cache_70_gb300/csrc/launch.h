@@ -31,6 +31,10 @@ cudaError_t launch_kv_write(const void* k, const void* v, int src_dtype, const i
                             int64_t kv_dim, int64_t num_slots, unsigned int* err,
                             cudaStream_t stream);
 
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src,
+                               const int32_t* dst, int32_t n_pairs, int64_t block_bytes,
+                               int64_t num_blocks, unsigned int* err, cudaStream_t stream);
+
 // ---- decode -----------------------------------------------------------------
 struct DecodePlan {
     int heads_per_cta;   // KV heads one CTA handles (HC)

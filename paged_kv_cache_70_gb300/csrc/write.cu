@@ -10,6 +10,8 @@
 // vectors of the K row and of the V row (2 KiB rows for Hkv=8, d=128, bf16), so
 // a warp issues fully coalesced 512-byte transactions.  The kernel is HBM-bound
 // (2 * kvDim * elt bytes read and written per token).
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -179,6 +181,86 @@ cudaError_t launch_kv_write(const void* k, const void* v, int src_dtype, const i
         kv_write_scalar_kernel<<<(unsigned)grid, threads, 0, stream>>>(
             k, v, src_dtype, slots, num_tokens, k_cache, v_cache, cache_dtype, kv_dim, num_slots,
             err);
+    }
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// block copies (copy-on-write, "11. Paged attention 与 online softmax" §11.3)
+// ---------------------------------------------------------------------------
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;  // 16-byte vectors in flight per thread and pool
+
+// grid (chunks of kCopyThreads * kCopyUnroll vectors, pairs): each CTA copies
+// one chunk of block src[pair] to block dst[pair] in both pools
+__global__ void __launch_bounds__(kCopyThreads)
+copy_blocks_kernel(uint4* __restrict__ kc, uint4* __restrict__ vc,
+                   const int32_t* __restrict__ src, const int32_t* __restrict__ dst,
+                   int64_t vec_per_block, int64_t num_blocks, unsigned int* err) {
+    const int32_t s = __ldg(src + blockIdx.y), d = __ldg(dst + blockIdx.y);
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag_error(err, PKV_FLAG_BAD_BLOCK);
+        return;
+    }
+    const int64_t base = (int64_t)blockIdx.x * kCopyThreads * kCopyUnroll + threadIdx.x;
+    const uint4* ks = kc + s * vec_per_block;
+    const uint4* vs = vc + s * vec_per_block;
+    uint4* kd = kc + d * vec_per_block;
+    uint4* vd = vc + d * vec_per_block;
+    uint4 a[kCopyUnroll], b[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t i = base + u * kCopyThreads;
+        if (i < vec_per_block) {
+            a[u] = __ldcs(ks + i);
+            b[u] = __ldcs(vs + i);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t i = base + u * kCopyThreads;
+        if (i < vec_per_block) {
+            __stcs(kd + i, a[u]);
+            __stcs(vd + i, b[u]);
+        }
+    }
+}
+
+// element-wise fallback for pools whose blocks are not 16-byte multiples
+__global__ void copy_blocks_bytes_kernel(unsigned char* __restrict__ kc,
+                                         unsigned char* __restrict__ vc,
+                                         const int32_t* __restrict__ src,
+                                         const int32_t* __restrict__ dst, int64_t block_bytes,
+                                         int64_t num_blocks, unsigned int* err) {
+    const int32_t s = src[blockIdx.y], d = dst[blockIdx.y];
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag_error(err, PKV_FLAG_BAD_BLOCK);
+        return;
+    }
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < block_bytes;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        kc[d * block_bytes + i] = kc[s * block_bytes + i];
+        vc[d * block_bytes + i] = vc[s * block_bytes + i];
+    }
+}
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src,
+                               const int32_t* dst, int32_t n_pairs, int64_t block_bytes,
+                               int64_t num_blocks, unsigned int* err, cudaStream_t stream) {
+    if (n_pairs == 0) return cudaSuccess;
+    if (block_bytes % 16 == 0 && aligned16(k_cache) && aligned16(v_cache)) {
+        const int64_t vec = block_bytes / 16;
+        const int64_t per_cta = (int64_t)kCopyThreads * kCopyUnroll;
+        const dim3 grid((unsigned)((vec + per_cta - 1) / per_cta), (unsigned)n_pairs);
+        copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(
+            static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), src, dst, vec, num_blocks,
+            err);
+    } else {
+        const dim3 grid((unsigned)std::min<int64_t>((block_bytes + 255) / 256, 64),
+                        (unsigned)n_pairs);
+        copy_blocks_bytes_kernel<<<grid, 256, 0, stream>>>(
+            static_cast<unsigned char*>(k_cache), static_cast<unsigned char*>(v_cache), src, dst,
+            block_bytes, num_blocks, err);
     }
     return cudaGetLastError();
 }
