@@ -503,6 +503,9 @@ def run_decode(args, world, pkv, W, hbm_peak, peak_src, line):
     return dstep
 
 
+W_NAME_PACKED = ("causal varlen prefill over packed K/V: the chunked-prefill workload's 16 "
+                 "requests (q~U[1,2048], cached~U[0,2048]) with each request's keys "
+                 "contiguous; L2 flushed between steps")
 COPY_PAIRS, COPY_GEOM = 8192, (16, 8, 128)  # block pairs; B, Hkv, d (bf16)
 
 
@@ -599,8 +602,58 @@ def run_prefill(args, world, pkv, W, bf16_peak, peak_src, line):
                 "h2d_bytes_per_step": ph2d, "d2h_bytes_per_step": pd2h}
         line["gpu_launches"] += 3 * args.steps
         line["error_flags"] |= pkv.paged_error_flags()
+        run_prefill_packed(args, world, pkv, pstep, pdev, flops, flush, bf16_peak, peak_src,
+                           line)
     del pdev
     torch.cuda.empty_cache()
+
+
+def run_prefill_packed(args, world, pkv, pstep, pdev, flops, flush, bf16_peak, peak_src, line):
+    """The same attention with packed K/V (block_table = NULL): each request's
+    keys gathered once (untimed) into contiguous [total_k, Hkv, d] arrays."""
+    s = pstep
+    B = s.block_size
+    rows = []
+    for r in range(s.n_prefill):
+        kl = int(s.cu_k[r + 1] - s.cu_k[r])
+        p = np.arange(kl)
+        rows.append(s.prefill_table[r][p // B].astype(np.int64) * B + p % B)
+    idx = torch.from_numpy(np.concatenate(rows)).cuda()
+    kp = pdev.k_cache.view(-1, s.hkv, s.d)[idx].contiguous()
+    vp = pdev.v_cache.view(-1, s.hkv, s.d)[idx].contiguous()
+    call = lambda: pkv.paged_varlen_prefill(pdev.q, kp, vp, pdev.cu_q, pdev.cu_k,
+                                            s.max_seqlen_q, s.max_seqlen_k, None,
+                                            causal=s.causal, scale=s.scale, out=pdev.out)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for i, (a, b) in enumerate(ev):
+        flush.fill_(i & 0xff)
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = [a.elapsed_time(b) for a, b in ev]
+    mean = max_over_ranks(float(np.mean(ms)), world)
+    tf = flops / (mean * 1e-3) / 1e12
+    line["prefill_contiguous"] = {
+        "metric": "varlen prefill TFLOP/s (packed K/V, block_table = NULL)",
+        "workload": W_NAME_PACKED, "value": round(world * tf, 2), "unit": "TFLOP/s",
+        "ms_per_step": round(mean, 5), "flops_per_step": flops,
+        "roofline": {"bound": "tensor", "kernel": "paged_varlen_prefill (packed)",
+                     "achieved": round(tf, 1), "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": round(tf / bf16_peak, 4), "peak_source": peak_src + " (bf16 burst)",
+                     "traffic": None, "mean_ms": round(mean, 5),
+                     "median_ms": round(float(np.median(ms)), 5)}}
+    line["gpu_launches"] += args.steps
+    line["error_flags"] |= pkv.paged_error_flags()
+    del kp, vp
 
 
 def cpu_baseline(args, world, rank, W, dstep, line):

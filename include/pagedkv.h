@@ -157,8 +157,14 @@ size_t paged_varlen_prefill_workspace_size(int32_t batch, int32_t max_seqlen_q,
  * q_len positions); a row that sees no key outputs 0.
  * max_seqlen_q / max_seqlen_k are host-side upper bounds of the per-request
  * lengths (they size the launch).  q, out [total_q, Hq, d].
- * Supported: bf16, head_dim 128, Hq/Hkv in {1, 2, 4, 8, ...}, any block_size
- * that is a multiple of 16 or divides 128.
+ * Contiguous mode ("从零开始写Qwen3（六）PagedAttention", "一个小细节": without
+ * a prefix cache the varlen call reads packed K/V): block_table == NULL makes
+ * k_cache / v_cache packed arrays [rows, Hkv, d] with rows = geom->num_blocks
+ * * geom->block_size (any factorisation, e.g. block_size 1), and request r's
+ * keys are rows cu_seqlens_k[r] .. cu_seqlens_k[r+1]-1; max_blocks_per_seq is
+ * ignored.  Keys past row `rows` are flagged PKV_FLAG_BAD_LENGTH.
+ * Supported: bf16, head_dim 128, Hq/Hkv in {1, 2, 4, 8, ...}; paged mode: a
+ * block_size that is a multiple of 128 or divides 128 and is >= 8.
  */
 int paged_varlen_prefill(const void* q, const void* k_cache, const void* v_cache,
                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,

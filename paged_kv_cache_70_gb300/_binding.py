@@ -276,20 +276,28 @@ def paged_varlen_prefill_workspace_size(batch: int, max_seqlen_q: int, q_heads: 
 
 def paged_varlen_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                          cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
-                         max_seqlen_q: int, max_seqlen_k: int, block_table: torch.Tensor,
+                         max_seqlen_q: int, max_seqlen_k: int, block_table: torch.Tensor | None,
                          causal: bool = True, scale: float | None = None,
                          out: torch.Tensor | None = None,
                          workspace: torch.Tensor | None = None) -> torch.Tensor:
-    """Causal varlen prefill of q [total_q, Hq, d] over the paged cache."""
+    """Causal varlen prefill of q [total_q, Hq, d] over the paged cache, or
+    (block_table None) over packed K/V [total_k, Hkv, d] whose request r holds
+    rows cu_seqlens_k[r] .. cu_seqlens_k[r+1]-1."""
     _cuda_contig("q", q, k_cache.dtype)
     _cuda_contig("k_cache", k_cache)
     _cuda_contig("v_cache", v_cache, k_cache.dtype)
     _cuda_contig("cu_seqlens_q", cu_seqlens_q, torch.int32)
     _cuda_contig("cu_seqlens_k", cu_seqlens_k, torch.int32)
-    _cuda_contig("block_table", block_table, torch.int32)
     batch = cu_seqlens_q.numel() - 1
     total_q, hq, d = q.shape
-    g = geom_of(k_cache, hq)
+    if block_table is None:
+        if k_cache.dim() != 3 or v_cache.shape != k_cache.shape:
+            raise ValueError("packed K/V must be [total_k, Hkv, d]")
+        rows, hkv, dk = k_cache.shape
+        g = Geom(hq, hkv, dk, 1, rows, _dtype_code(k_cache))
+    else:
+        _cuda_contig("block_table", block_table, torch.int32)
+        g = geom_of(k_cache, hq)
     lib = load_library()
     need = int(lib.paged_varlen_prefill_workspace_size(batch, max_seqlen_q, ctypes.byref(g)))
     if workspace is None and need:
@@ -301,7 +309,8 @@ def paged_varlen_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
     with torch.cuda.device(q.device):
         st = lib.paged_varlen_prefill(
             _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch,
-            int(max_seqlen_q), int(max_seqlen_k), _ptr(block_table), block_table.shape[1],
+            int(max_seqlen_q), int(max_seqlen_k), _ptr(block_table),
+            0 if block_table is None else block_table.shape[1],
             1 if causal else 0, scale, _ptr(out), _ptr(workspace),
             0 if workspace is None else workspace.numel(), ctypes.byref(g), _stream(q))
     _check("paged_varlen_prefill", st)

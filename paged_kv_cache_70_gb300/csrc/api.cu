@@ -163,7 +163,7 @@ int paged_varlen_prefill(const void* q, const void* k_cache, const void* v_cache
     if (batch < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || max_blocks_per_seq < 0)
         return PKV_ERR_INVALID;
     if (batch == 0 || max_seqlen_q == 0) return PKV_OK;
-    if (!q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !block_table || !out)
+    if (!q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !out)
         return PKV_ERR_INVALID;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
         return PKV_ERR_INVALID;

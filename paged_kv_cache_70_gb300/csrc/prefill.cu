@@ -251,8 +251,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const int32_t cq0 = a.cu_q[r], cq1 = a.cu_q[r + 1];
     const int32_t ck0 = a.cu_k[r], ck1 = a.cu_k[r + 1];
     int32_t q_len = cq1 - cq0, k_len = ck1 - ck0;
-    const int32_t cap = a.max_blocks * a.block_size;
-    if (q_len < 0 || k_len < 0 || k_len > cap || q_len > a.tiles_q * BM) {
+    // keys a request may have: its block-table row, or (packed K/V) the rows
+    // from its first key to the end of the arrays
+    const int32_t cap = a.table ? a.max_blocks * a.block_size : max(0, a.oob_row - ck0);
+    if (q_len < 0 || k_len < 0 || k_len > cap || q_len > a.tiles_q * BM ||
+        (!a.table && ck0 < 0)) {
         if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
             flag_error(a.err, PKV_FLAG_BAD_LENGTH);
         if (q_len < 0) q_len = 0;
@@ -321,6 +324,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
             int issued = 0, issued_v = 0;
             auto page_row = [&](int32_t key) -> int32_t {
                 if (key >= k_len) return a.oob_row;  // zero-filled by TMA
+                if (!a.table) return ck0 + key;       // packed K/V
                 const int32_t phys = a.table[(int64_t)r * a.max_blocks + key / a.block_size];
                 if (phys < 0 || phys >= a.num_blocks) {
                     flag_error(a.err, PKV_FLAG_BAD_BLOCK);
@@ -674,13 +678,15 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
     (void)workspace;
     if (d != HD) return cudaErrorNotSupported;
     // a TMA box of min(B,128) rows must tile 128 keys on 1024-byte boundaries
-    const bool b_ok = (block_size >= 128) ? (block_size % 128 == 0)
-                                          : (block_size >= 8 && 128 % block_size == 0);
+    // (packed K/V: one 128-row box per tile, any block_size)
+    const bool packed = block_table == nullptr;
+    const bool b_ok = packed || ((block_size >= 128) ? (block_size % 128 == 0)
+                                                     : (block_size >= 8 && 128 % block_size == 0));
     if (!b_ok || batch > 65535 || hq > 65535) return cudaErrorNotSupported;
     if (dev.max_smem_optin < kSmemBytes) return cudaErrorNotSupported;
     const int64_t rows = num_blocks * block_size;
     if (rows + 128 > 0x7fffffffLL) return cudaErrorNotSupported;
-    const int piece = block_size < BN ? block_size : BN;
+    const int piece = (packed || block_size >= BN) ? BN : block_size;
     // q holds at most batch * max_seqlen_q rows; no box reaches past the
     // last row of its own request, so this bound never clips a valid row
     const int64_t q_rows = std::min<int64_t>((int64_t)batch * max_seqlen_q, 0x7fffffffLL);

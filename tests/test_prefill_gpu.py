@@ -208,3 +208,73 @@ def test_growing_scores(step):
         assert np.all(np.isfinite(got))
         assert_close(got, run_oracle(c, causal), "bf16", f"step {step} causal {causal}")
     assert pkv.paged_error_flags() == 0
+
+
+def packed_case(qlens, klens, hq=16, hkv=8, d=128, seed=0, tail=0):
+    """Packed K/V [sum(klens) + tail, Hkv, d]; request r's keys are rows
+    cu_k[r] .. cu_k[r+1]-1 (tail rows after the last request hold NaN)."""
+    rng = np.random.default_rng(seed)
+    cq = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(klens)]).astype(np.int32)
+    k = _bf(rng.standard_normal((int(ck[-1]) + tail, hkv, d)))
+    v = _bf(rng.standard_normal((int(ck[-1]) + tail, hkv, d)))
+    k[int(ck[-1]):] = 0x7fc0
+    v[int(ck[-1]):] = 0x7fc0
+    q = _bf(rng.standard_normal((int(cq[-1]), hq, d)))
+    return dict(q=q, k=k, v=v, cq=cq, ck=ck, scale=1 / math.sqrt(d))
+
+
+def run_packed(c, causal=True):
+    return pkv.paged_varlen_prefill(
+        to_dev(c["q"]), to_dev(c["k"]), to_dev(c["v"]), to_dev(c["cq"]), to_dev(c["ck"]),
+        int(np.diff(c["cq"]).max()), int(np.diff(c["ck"]).max()), None, causal=causal,
+        scale=c["scale"])
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("qlens,klens,tail", [
+    ([10, 3, 1], [0, 1, 7], 0),                       # the varlen example's lengths
+    ([1, 127, 128, 129, 300], [1, 200, 128, 400, 1000], 0),
+    ([64, 700], [64, 1500], 37),                      # NaN rows after the last request
+    ([200, 64], [260, 64], 0),
+])
+def test_contiguous_varlen(qlens, klens, tail, causal):
+    """block_table = NULL: plain varlen attention over packed K/V."""
+    c = packed_case(qlens, klens, seed=sum(qlens) + tail, tail=tail)
+    got = widen(run_packed(c, causal))
+    want = oracle.prefill(c["q"], c["k"], c["v"], c["cq"], c["ck"], c["scale"], causal=causal)
+    assert np.all(np.isfinite(got))
+    assert_close(got, want, "bf16", f"packed {qlens}/{klens}")
+    assert pkv.paged_error_flags() == 0
+
+
+def test_contiguous_equals_paged_bitwise():
+    """The same keys read packed or through a block table give identical bits."""
+    qlens, klens, B = [100, 256, 33], [300, 900, 33], 64
+    c = packed_case(qlens, klens, seed=5)
+    rng = np.random.default_rng(6)
+    need = [-(-k // B) for k in klens]
+    nb = sum(need) + 2
+    order = rng.permutation(nb).astype(np.int32)
+    table = np.full((len(klens), max(need)), -1, np.int32)
+    kc = np.zeros((nb, B) + c["k"].shape[1:], np.uint16)
+    vc = np.zeros_like(kc)
+    nxt = 0
+    for r, kl in enumerate(klens):
+        table[r, : need[r]] = order[nxt: nxt + need[r]]
+        nxt += need[r]
+        for j in range(kl):
+            kc[table[r, j // B], j % B] = c["k"][c["ck"][r] + j]
+            vc[table[r, j // B], j % B] = c["v"][c["ck"][r] + j]
+    paged = pkv.paged_varlen_prefill(
+        to_dev(c["q"]), to_dev(kc), to_dev(vc), to_dev(c["cq"]), to_dev(c["ck"]), max(qlens),
+        max(klens), to_dev(table), causal=True, scale=c["scale"])
+    assert np.array_equal(to_host(paged), to_host(run_packed(c)))
+
+
+def test_contiguous_keys_past_the_arrays_are_flagged():
+    c = packed_case([8], [40], seed=2)
+    c["ck"] = np.array([0, 60], np.int32)  # claims more keys than the arrays hold
+    run_packed(c)
+    torch.cuda.synchronize()
+    assert pkv.paged_error_flags() & pkv.PKV_FLAG_BAD_LENGTH
