@@ -18,6 +18,7 @@ reference arm of this build) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -44,7 +45,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--only", choices=["all", "decode", "prefill", "copy"], default="all",
+    p.add_argument("--only", choices=["all", "decode", "prefill", "copy", "shared"],
+                   default="all",
                    help="measure one half only (profiling runs)")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
     return p.parse_args()
@@ -437,10 +439,16 @@ def main():
         run_prefill(args, world, pkv, W, bf16_peak, peak_src, line)
     if args.only in ("all", "copy"):
         run_copy(args, world, pkv, hbm_peak, peak_src, line)
+    if args.only in ("all", "shared"):
+        run_shared_prefix(args, world, pkv, W, hbm_peak, peak_src, line)
     if args.only == "prefill":  # headline comes from the prefill half
         line["metric"] = "varlen prefill TFLOP/s"
         line["value"], line["unit"] = line["prefill"].get("value"), "TFLOP/s"
         line["ms_per_step"] = line["prefill"].get("ms_per_step")
+    if args.only == "shared":
+        line["metric"] = line["decode_shared_prefix"]["metric"]
+        line["value"] = line["decode_shared_prefix"]["value"]
+        line["ms_per_step"] = line["decode_shared_prefix"]["ms_per_step"]
     if args.only == "copy":
         line["metric"] = line["copy_blocks"]["metric"]
         line["value"] = line["copy_blocks"]["value"]
@@ -555,6 +563,77 @@ def run_copy(args, world, pkv, hbm_peak, peak_src, line):
     line["gpu_launches"] += args.steps
     line["error_flags"] |= pkv.paged_error_flags()
     del k_cache, v_cache
+    torch.cuda.empty_cache()
+
+
+def run_shared_prefix(args, world, pkv, W, hbm_peak, peak_src, line):
+    """Decode half of the continuous-batching workload: 256 sequences in 8
+    groups of 32 that share a 2048-token prefix (128 blocks of 16), suffixes
+    U[0,512] plus the new token.  Shared-prefix decode (each prefix block read
+    once per group) against plain paged decode of the same step.  The roofline
+    counts UNIQUE bytes: the prefixes once, every suffix, q and out."""
+    s = W.config(5)
+    nd = s.n_decode
+    dev = lambda a: to_dev(a)
+    k_cache, v_cache = dev(s.k_cache), dev(s.v_cache)
+    q, table, lens = dev(s.q_decode), dev(s.decode_table.copy()), dev(s.cache_seqlens)
+    groups = 8
+    gcu = dev(np.arange(0, nd + 1, nd // groups, dtype=np.int32))
+    plen = dev(np.full(groups, 2048, np.int32))
+    out = torch.empty_like(q)
+    row = s.hkv * s.d * 2 * 2  # K + V bytes per key
+    unique = (groups * 2048 + int((s.cache_seqlens - 2048).sum())) * row + 2 * q.numel() * 2
+    logical = int(s.cache_seqlens.sum()) * row + 2 * q.numel() * 2
+    ws = torch.empty(pkv._binding.load_library().paged_decode_shared_prefix_workspace_size(
+        nd, ctypes.byref(pkv.geom_of(k_cache, s.hq))), dtype=torch.uint8, device="cuda")
+    wsp = torch.empty(max(1, pkv.paged_decode_workspace_size(nd, s.hq, k_cache)),
+                      dtype=torch.uint8, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    shared = lambda: pkv.paged_decode_shared_prefix(q, k_cache, v_cache, table, lens, gcu, plen,
+                                                    nd // groups, s.scale, out=out, workspace=ws)
+    plain = lambda: pkv.paged_decode(q, k_cache, v_cache, table, lens, s.scale, out=out,
+                                     workspace=wsp)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i, (a, b) in enumerate(ev):
+            flush.fill_(i & 0xff)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        ms = [a.elapsed_time(b) for a, b in ev]
+        return max_over_ranks(float(np.mean(ms)), world), float(np.median(ms))
+
+    sh_ms, sh_med = timed(shared)
+    pl_ms, _ = timed(plain)
+    gbs = unique / (sh_ms * 1e-3) / 1e9
+    line["decode_shared_prefix"] = {
+        "metric": "shared-prefix decode GB/s of unique K/V", "unit": "GB/s",
+        "value": round(world * gbs, 1), "ms_per_step": round(sh_ms, 5),
+        "workload": "decode half of the continuous-batching step: 256 sequences, 8 groups of "
+                    "32 sharing a 2048-token prefix (B=16), suffixes U[0,512]+1, GQA 16/8, "
+                    "d=128, bf16; L2 flushed between steps",
+        "unique_bytes": unique, "logical_bytes": logical,
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_shared_prefix (prefix on the "
+                     "tensor cores + suffix split + combine)", "achieved": round(gbs, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                     "peak_source": peak_src, "traffic": None, "mean_ms": round(sh_ms, 5),
+                     "median_ms": round(sh_med, 5)},
+        "plain_decode_same_step": {"ms": round(pl_ms, 5),
+                                   "logical_GBps": round(logical / (pl_ms * 1e-3) / 1e9, 1),
+                                   "speedup_of_shared": round(pl_ms / sh_ms, 3)}}
+    line["gpu_launches"] += 3 * args.steps
+    line["error_flags"] |= pkv.paged_error_flags()
+    del k_cache, v_cache, ws, wsp, flush
     torch.cuda.empty_cache()
 
 

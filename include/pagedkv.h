@@ -174,6 +174,39 @@ int paged_varlen_prefill(const void* q, const void* k_cache, const void* v_cache
                          cudaStream_t stream);
 
 /*
+ * paged_decode_shared_prefix -- paged_decode for batches whose sequences come
+ * in groups that share the physical blocks of a common prefix ("11. Paged
+ * attention 与 online softmax" §11.3 block sharing; the prefix cache of
+ * "结合nanovllm的FlashAttention和PagedAttention主要原理概述" 题目6), reading each
+ * shared block once per group instead of once per sequence.
+ *   group_cu [n_groups + 1] (device): group g is sequences group_cu[g] ..
+ *   group_cu[g+1]-1 of the batch (group_cu[0] = 0, group_cu[n_groups] =
+ *   batch: the batch is ordered by group; a sequence sharing nothing is a
+ *   group of one with prefix 0).  group_prefix_len [n_groups] (device): the
+ *   leading keys every sequence of group g holds in the same physical blocks,
+ *   a multiple of block_size and at most each member's cache_seqlens; the
+ *   prefix blocks are read through the table row of the group's first
+ *   sequence.  max_group_size: a host-side bound of the group sizes.
+ * The result is paged_decode's (same arguments and layouts otherwise): the
+ * prefix part is the attention of the group's queries over the prefix keys
+ * (one pass over them, on the tensor cores), the rest the decode of each
+ * sequence's own keys, merged with §11.2's boxed rule.
+ * Supported: bf16, head_dim 128, Hq/Hkv in {1, 2, 4}, block_size a multiple of
+ * 128 or a divisor of 128 (>= 8).  workspace: at least
+ * paged_decode_shared_prefix_workspace_size(batch, geom) bytes, 256-byte
+ * aligned.  A prefix length that is negative, longer than a member's keys or
+ * not a multiple of block_size sets PKV_FLAG_BAD_LENGTH.
+ */
+size_t paged_decode_shared_prefix_workspace_size(int32_t batch, const pkv_geom* geom);
+int paged_decode_shared_prefix(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, int32_t max_blocks_per_seq,
+                               const int32_t* cache_seqlens, int32_t batch,
+                               const int32_t* group_cu, const int32_t* group_prefix_len,
+                               int32_t n_groups, int32_t max_group_size, float scale, void* out,
+                               void* workspace, size_t workspace_bytes, const pkv_geom* geom,
+                               cudaStream_t stream);
+
+/*
  * paged_decode_noalloc -- paged_decode for callers that cannot allocate device
  * memory.  The pages have no counterpart: this is a deployment variant of
  * paged_decode that takes no workspace.

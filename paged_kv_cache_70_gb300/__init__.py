@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     paged_build_slot_mapping,
     paged_decode,
     paged_decode_noalloc,
+    paged_decode_shared_prefix,
     paged_decode_workspace_size,
     paged_error_flags,
     paged_kv_write,

@@ -47,6 +47,8 @@ EXPORTED = (
     "paged_bm_ref_count",
     "paged_bm_free_blocks",
     "paged_copy_blocks",
+    "paged_decode_shared_prefix_workspace_size",
+    "paged_decode_shared_prefix",
 )
 PKV_ERR_NO_SPACE = -5
 
@@ -121,6 +123,11 @@ def load_library(path: str | None = None):
         for f in ("create", "destroy", "allocate", "fork", "append", "free", "block_table",
                   "seq_len", "ref_count", "free_blocks"):
             getattr(lib, "paged_bm_" + f).restype = ctypes.c_int
+        lib.paged_decode_shared_prefix_workspace_size.argtypes = [i32, gp]
+        lib.paged_decode_shared_prefix_workspace_size.restype = sz
+        lib.paged_decode_shared_prefix.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, vp, i32, i32,
+                                                   ctypes.c_float, vp, vp, sz, gp, vp]
+        lib.paged_decode_shared_prefix.restype = ctypes.c_int
         lib.paged_copy_blocks.argtypes = [vp, vp, vp, vp, i32, gp, vp]
         lib.paged_copy_blocks.restype = ctypes.c_int
         lib.paged_status_string.argtypes = [ctypes.c_int]
@@ -264,6 +271,46 @@ def paged_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
             _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
             _ptr(cache_seqlens), batch, scale, _ptr(out), ctypes.byref(g), _stream(q))
     _check("paged_decode_noalloc", st)
+    return out
+
+
+def paged_decode_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               block_table: torch.Tensor, cache_seqlens: torch.Tensor,
+                               group_cu: torch.Tensor, group_prefix_len: torch.Tensor,
+                               max_group_size: int, scale: float | None = None,
+                               out: torch.Tensor | None = None,
+                               workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """paged_decode for a batch ordered by groups (sequences group_cu[g] ..
+    group_cu[g+1]-1) whose first group_prefix_len[g] keys sit in shared blocks:
+    each shared block is read once per group."""
+    _cuda_contig("q", q, k_cache.dtype)
+    _cuda_contig("k_cache", k_cache)
+    _cuda_contig("v_cache", v_cache, k_cache.dtype)
+    _cuda_contig("block_table", block_table, torch.int32)
+    _cuda_contig("cache_seqlens", cache_seqlens, torch.int32)
+    _cuda_contig("group_cu", group_cu, torch.int32)
+    _cuda_contig("group_prefix_len", group_prefix_len, torch.int32)
+    batch, hq, d = q.shape
+    n_groups = group_cu.numel() - 1
+    if group_prefix_len.numel() < n_groups or block_table.shape[0] < batch:
+        raise ValueError("shape mismatch")
+    g = geom_of(k_cache, hq)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        need = int(lib.paged_decode_shared_prefix_workspace_size(batch, ctypes.byref(g)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, q.dtype)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    with torch.cuda.device(q.device):
+        st = lib.paged_decode_shared_prefix(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+            _ptr(cache_seqlens), batch, _ptr(group_cu), _ptr(group_prefix_len), n_groups,
+            int(max_group_size), scale, _ptr(out), _ptr(workspace), workspace.numel(),
+            ctypes.byref(g), _stream(q))
+    _check("paged_decode_shared_prefix", st)
     return out
 
 

@@ -181,6 +181,79 @@ int paged_varlen_prefill(const void* q, const void* k_cache, const void* v_cache
     return cuda_status(e);
 }
 
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// the prefix keys of a group are split into at most this many chunks (work
+// items for the SMs); each chunk leaves its own partial per (sequence, head)
+constexpr int kMaxPrefixChunks = 8;
+
+static size_t shared_prefix_extra_bytes(int32_t batch, const pkv_geom* g) {
+    return align256((size_t)kMaxPrefixChunks * batch * g->num_heads * g->head_dim * 2) +
+           align256((size_t)kMaxPrefixChunks * batch * g->num_heads * 4);
+}
+
+size_t paged_decode_shared_prefix_workspace_size(int32_t batch, const pkv_geom* geom) {
+    const size_t dec = paged_decode_workspace_size(batch, geom);
+    if (!dec) return 0;
+    return dec + shared_prefix_extra_bytes(batch, geom);
+}
+
+int paged_decode_shared_prefix(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, int32_t max_blocks_per_seq,
+                               const int32_t* cache_seqlens, int32_t batch,
+                               const int32_t* group_cu, const int32_t* group_prefix_len,
+                               int32_t n_groups, int32_t max_group_size, float scale, void* out,
+                               void* workspace, size_t workspace_bytes, const pkv_geom* geom,
+                               cudaStream_t stream) {
+    int st = check_geom(geom);
+    if (st != PKV_OK) return st;
+    if (batch < 0 || max_blocks_per_seq < 0 || n_groups < 0 || max_group_size < 0)
+        return PKV_ERR_INVALID;
+    if (batch == 0) return PKV_OK;
+    if (n_groups == 0 || max_group_size == 0) return PKV_ERR_INVALID;
+    if (!q || !k_cache || !v_cache || !block_table || !cache_seqlens || !out || !group_cu ||
+        !group_prefix_len)
+        return PKV_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+        return PKV_ERR_INVALID;
+    if (geom->dtype != PKV_BF16 || geom->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    if (pkv::current_device_info(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    pkv::DecodePlan plan;
+    if (!pkv::plan_decode(dev, batch, geom->num_heads, geom->num_kv_heads, geom->head_dim,
+                          geom->block_size, elt_size(geom->dtype), &plan))
+        return PKV_ERR_UNSUPPORTED;
+    const size_t need = plan.ws_bytes + shared_prefix_extra_bytes(batch, geom);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return PKV_ERR_WORKSPACE;
+    unsigned char* x_out = static_cast<unsigned char*>(workspace) + plan.ws_bytes;
+    float* x_lse = reinterpret_cast<float*>(
+        x_out + align256((size_t)kMaxPrefixChunks * batch * geom->num_heads * geom->head_dim * 2));
+    // enough (group, chunk, head pair, query tile) items to cover the SMs once
+    const int units = n_groups * (geom->num_heads / geom->num_kv_heads % 2 == 0
+                                      ? geom->num_heads / 2 : geom->num_heads) *
+                      ((max_group_size + 127) / 128);
+    int kchunks = units > 0 ? dev.num_sms / units : 1;
+    kchunks = kchunks < 1 ? 1 : (kchunks > kMaxPrefixChunks ? kMaxPrefixChunks : kchunks);
+    // 1. the prefix of every group, once: non-causal attention of the group's
+    //    queries over its first group_prefix_len[g] keys, read through the
+    //    block-table row of the group's first sequence (tensor cores)
+    pkv::PrefillExtra ex{group_prefix_len, group_cu, x_lse, kchunks, batch};
+    cudaError_t e = pkv::launch_prefill(dev, q, k_cache, v_cache, group_cu, group_cu, n_groups,
+                                        max_group_size, 0, block_table, max_blocks_per_seq, 0,
+                                        scale, x_out, nullptr, geom->num_heads,
+                                        geom->num_kv_heads, geom->head_dim, geom->block_size,
+                                        geom->num_blocks, dev.err, stream, &ex);
+    if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    // 2. each sequence's own keys after the prefix, merged with the prefix state
+    pkv::SharedPrefix sp{group_cu, group_prefix_len, n_groups, x_out, x_lse, kchunks};
+    return cuda_status(pkv::launch_decode(plan, q, k_cache, v_cache, block_table,
+                                          max_blocks_per_seq, cache_seqlens, batch, scale, out,
+                                          workspace, geom->num_heads, geom->num_kv_heads,
+                                          geom->head_dim, geom->block_size, geom->num_blocks,
+                                          geom->dtype, dev.err, stream, &sp));
+}
+
 int paged_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst,
                       int32_t n_pairs, const pkv_geom* geom, cudaStream_t stream) {
     int st = check_geom(geom);

@@ -55,6 +55,10 @@ struct DecodeArgs {
     float* part_o;        // [ctas + batch][hq][D]
     float* part_ml;       // [ctas + batch][hq][2]
     int32_t* tstart_out;  // [batch + 1]
+    // shared-prefix mode (else null): sequences group_cu[g] .. group_cu[g+1]-1
+    // share their first group_plen[g] keys, which this kernel then skips
+    const int32_t* group_cu;
+    const int32_t* group_plen;
     unsigned int* err;
     int64_t num_blocks;
     float qscale;  // scale * log2(e)
@@ -66,6 +70,7 @@ struct DecodeArgs {
     int32_t block_size;
     int32_t rows;  // R
     int32_t stages;
+    int32_t n_groups;
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -115,6 +120,25 @@ __device__ __forceinline__ int32_t clamp_len(int32_t L, int32_t cap) {
     return L < 0 ? 0 : (L > cap ? cap : L);
 }
 
+// First key of sequence b this kernel covers: 0, or in shared-prefix mode the
+// group's prefix length (a multiple of the block size, at most L; anything
+// else is flagged and rounded down to a whole tile).
+__device__ __forceinline__ int32_t seq_start(const DecodeArgs& a, int b, int32_t L) {
+    if (!a.group_cu) return 0;
+    int lo = 0, hi = a.n_groups;  // last g with group_cu[g] <= b
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(a.group_cu + mid) <= b) lo = mid; else hi = mid;
+    }
+    int32_t s = __ldg(a.group_plen + lo);
+    if (s < 0 || s > L || s % a.block_size) {
+        flag_error(a.err, PKV_FLAG_BAD_LENGTH);
+        s = s < 0 ? 0 : (s > L ? L : s);
+        s -= s % a.rows;
+    }
+    return s;
+}
+
 // Exclusive scan of per-sequence tile counts into tstart[0..batch] (all threads).
 __device__ void scan_tiles(const DecodeArgs& a, int32_t* tstart) {
     __shared__ int32_t warp_tot[kDecodeThreads / 32];
@@ -125,7 +149,7 @@ __device__ void scan_tiles(const DecodeArgs& a, int32_t* tstart) {
     int32_t sum = 0;
     for (int b = lo; b < hi; ++b) {
         const int32_t L = clamp_len(a.seqlens[b], cap);
-        sum += (L + a.rows - 1) / a.rows;
+        sum += (L - seq_start(a, b, L) + a.rows - 1) / a.rows;
     }
     const int lane = tid & 31, warp = tid >> 5;
     int32_t inc = sum;
@@ -142,7 +166,7 @@ __device__ void scan_tiles(const DecodeArgs& a, int32_t* tstart) {
     for (int b = lo; b < hi; ++b) {
         tstart[b] = run;
         const int32_t L = clamp_len(a.seqlens[b], cap);
-        run += (L + a.rows - 1) / a.rows;
+        run += (L - seq_start(a, b, L) + a.rows - 1) / a.rows;
     }
     if (tid == nthr - 1) tstart[a.batch] = base + inc;
 }
@@ -228,14 +252,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
         const uint64_t pol = l2_evict_first_policy();
         int b = seq_of_tile(tstart, a.batch, t0);
         int32_t L = clamp_len(a.seqlens[b], cap);
+        int32_t st = seq_start(a, b, L);
         for (int32_t t = t0, k = 0; t < t1; ++t, ++k) {
             while (t >= tstart[b + 1]) {
                 ++b;
                 L = clamp_len(a.seqlens[b], cap);
+                st = seq_start(a, b, L);
             }
             const int s = k % S;
             if (!mbar_wait(&empty[s], ((k / S) & 1) ^ 1, a.err)) return;
-            const int32_t pos0 = (t - tstart[b]) * R;
+            const int32_t pos0 = st + (t - tstart[b]) * R;
             const int32_t rows = min(R, L - pos0);
             const int32_t phys = a.table[(int64_t)b * a.max_blocks + pos0 / a.block_size];
             if (phys < 0 || phys >= a.num_blocks) {
@@ -281,13 +307,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
     float m[G], l[G];
     int b = seq_of_tile(tstart, a.batch, t0);
     int loaded = -1;
-    int32_t L = 0;
+    int32_t L = 0, st = 0;
 
     for (int32_t t = t0, k = 0; t < t1; ++t, ++k) {
         while (t >= tstart[b + 1]) ++b;
         if (b != loaded) {
             loaded = b;
             L = clamp_len(a.seqlens[b], cap);
+            st = seq_start(a, b, L);
             const float2 sc2 = make_float2(a.qscale, a.qscale);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
@@ -305,7 +332,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
         }
         const int s = k % S;
         if (!mbar_wait(&full[s], (k / S) & 1, a.err)) return;
-        const int32_t rows = min(R, L - (t - tstart[b]) * R);
+        const int32_t rows = min(R, L - st - (t - tstart[b]) * R);
         if (stage_ok[s]) {
             const unsigned char* ks = stage_base + (size_t)s * 2 * half_bytes;
             const unsigned char* vs = ks + half_bytes;
@@ -460,12 +487,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
 }
 
 // Merge the partial states of every (sequence, head) and normalise.  One warp
-// per (sequence, head); lane i owns dims [i*D/32, (i+1)*D/32).
+// per (sequence, head); lane i owns dims [i*D/32, (i+1)*D/32).  In shared-
+// prefix mode one more partial joins the merge: the prefix attention's
+// normalised output x_out (bf16) with x_lse = m + log2(l) in the same log2
+// units, i.e. the state (m = x_lse, l = 1, o = x_out).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(128)
 decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                       const int32_t* __restrict__ tstart, int32_t batch, int ctas, int hq,
-                      void* __restrict__ out) {
+                      void* __restrict__ out, const uint16_t* __restrict__ x_out,
+                      const float* __restrict__ x_lse, int x_chunks) {
     constexpr int DPL = D / 32;
     // wait until the split kernel's partials are complete and visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -479,24 +510,37 @@ decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict_
 #pragma unroll
     for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
     float lt = 0.f;
-    if (tb1 > tb0) {
-        const int32_t chunk = (total + ctas - 1) / ctas;
-        const int c0 = tb0 / chunk, c1 = (tb1 - 1) / chunk;
-        float M = -INFINITY;
-        for (int c = c0 + lane; c <= c1; c += 32)
-            M = fmaxf(M, part_ml[(((int64_t)c + b) * hq + h) * 2]);
+    const int32_t chunk = total > 0 ? (total + ctas - 1) / ctas : 1;
+    const int c0 = tb0 / chunk, c1 = tb1 > tb0 ? (tb1 - 1) / chunk : c0 - 1;
+    const int64_t xstride = (int64_t)batch * hq;  // one prefix chunk's (sequence, head) count
+    float M = -INFINITY;
+    for (int c = lane; c < x_chunks; c += 32) M = fmaxf(M, x_lse[c * xstride + (int64_t)b * hq + h]);
+    for (int c = c0 + lane; c <= c1; c += 32)
+        M = fmaxf(M, part_ml[(((int64_t)c + b) * hq + h) * 2]);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        if (M != -INFINITY) {
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (M != -INFINITY) {
 #pragma unroll 4
-            for (int c = c0; c <= c1; ++c) {
-                const int64_t slot = (int64_t)c + b;
-                const float2 ml = *reinterpret_cast<const float2*>(part_ml + (slot * hq + h) * 2);
-                const float wgt = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
-                lt += ml.y * wgt;
-                const float* src = part_o + (slot * hq + h) * D + lane * DPL;
+        for (int c = c0; c <= c1; ++c) {
+            const int64_t slot = (int64_t)c + b;
+            const float2 ml = *reinterpret_cast<const float2*>(part_ml + (slot * hq + h) * 2);
+            const float wgt = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
+            lt += ml.y * wgt;
+            const float* src = part_o + (slot * hq + h) * D + lane * DPL;
 #pragma unroll
-                for (int e = 0; e < DPL; ++e) acc[e] += src[e] * wgt;
+            for (int e = 0; e < DPL; ++e) acc[e] += src[e] * wgt;
+        }
+        for (int c = 0; c < x_chunks; ++c) {
+            const float mx = x_lse[c * xstride + (int64_t)b * hq + h];
+            if (mx == -INFINITY) continue;
+            const float wgt = ex2(mx - M);
+            lt += wgt;
+            const uint16_t* src = x_out + (c * xstride + (int64_t)b * hq + h) * D + lane * DPL;
+#pragma unroll
+            for (int e = 0; e < DPL; e += 2) {
+                const uint32_t pr = *reinterpret_cast<const uint32_t*>(src + e);
+                acc[e] += bf16lo(pr) * wgt;
+                acc[e + 1] += bf16hi(pr) * wgt;
             }
         }
     }
@@ -563,6 +607,7 @@ bool plan_decode(const DeviceInfo& dev, int32_t batch, int hq, int hkv, int d, i
 
 template <int D, bool BF16, int G>
 static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a, void* out,
+                                   const uint16_t* x_out, const float* x_lse, int x_chunks,
                                    cudaStream_t stream) {
     auto kern = decode_split_kernel<D, BF16, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -588,16 +633,23 @@ static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a, 
                               static_cast<const float*>(a.part_o),
                               static_cast<const float*>(a.part_ml),
                               static_cast<const int32_t*>(a.tstart_out), a.batch, plan.ctas,
-                              a.hq, out);
+                              a.hq, out, x_out, x_lse, x_chunks);
 }
 
 cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_cache,
                           const void* v_cache, const int32_t* block_table, int32_t max_blocks,
                           const int32_t* cache_seqlens, int32_t batch, float scale, void* out,
                           void* workspace, int hq, int hkv, int d, int block_size,
-                          int64_t num_blocks, int dtype, unsigned int* err, cudaStream_t stream) {
+                          int64_t num_blocks, int dtype, unsigned int* err, cudaStream_t stream,
+                          const SharedPrefix* sp) {
     if (batch == 0) return cudaSuccess;
     DecodeArgs a;
+    a.group_cu = sp ? sp->group_cu : nullptr;
+    a.group_plen = sp ? sp->group_plen : nullptr;
+    a.n_groups = sp ? sp->n_groups : 0;
+    const uint16_t* x_out = sp ? static_cast<const uint16_t*>(sp->x_out) : nullptr;
+    const float* x_lse = sp ? sp->x_lse : nullptr;
+    const int x_chunks = sp ? sp->x_chunks : 0;
     a.q = q;
     a.k_cache = static_cast<const unsigned char*>(k_cache);
     a.v_cache = static_cast<const unsigned char*>(v_cache);
@@ -624,7 +676,8 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
     const int G = hq / hkv;
     const bool bf = dtype == PKV_BF16;
 #define PKV_DECODE_CASE(DD, BB, GG) \
-    if (d == DD && bf == BB && G == GG) return launch_decode_t<DD, BB, GG>(plan, a, out, stream);
+    if (d == DD && bf == BB && G == GG) \
+        return launch_decode_t<DD, BB, GG>(plan, a, out, x_out, x_lse, x_chunks, stream);
     PKV_DECODE_CASE(128, true, 1) PKV_DECODE_CASE(128, true, 2) PKV_DECODE_CASE(128, true, 4)
     PKV_DECODE_CASE(128, false, 1) PKV_DECODE_CASE(128, false, 2) PKV_DECODE_CASE(128, false, 4)
     PKV_DECODE_CASE(64, true, 1) PKV_DECODE_CASE(64, true, 2) PKV_DECODE_CASE(64, true, 4)

@@ -48,6 +48,18 @@ struct DecodePlan {
 
 constexpr int kDecodeMaxBatch = 4096;
 
+// Shared-prefix decode: groups of consecutive sequences share a prefix whose
+// attention (normalised output and log2-sum-exp per sequence and head) was
+// computed separately; the decode covers the keys after it and merges.
+struct SharedPrefix {
+    const int32_t* group_cu;    // [n_groups + 1]
+    const int32_t* group_plen;  // [n_groups]
+    int32_t n_groups;
+    const void* x_out;          // [x_chunks, batch, hq, d] bf16
+    const float* x_lse;         // [x_chunks, batch, hq]
+    int32_t x_chunks;           // prefix partials per (sequence, head)
+};
+
 // Returns false when the geometry is not supported.
 bool plan_decode(const DeviceInfo& dev, int32_t batch, int hq, int hkv, int d, int block_size,
                  int elt, DecodePlan* plan);
@@ -56,10 +68,20 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
                           const void* v_cache, const int32_t* block_table, int32_t max_blocks,
                           const int32_t* cache_seqlens, int32_t batch, float scale, void* out,
                           void* workspace, int hq, int hkv, int d, int block_size,
-                          int64_t num_blocks, int dtype, unsigned int* err, cudaStream_t stream);
+                          int64_t num_blocks, int dtype, unsigned int* err, cudaStream_t stream,
+                          const SharedPrefix* shared = nullptr);
 
 // ---- prefill ----------------------------------------------------------------
 size_t prefill_workspace_bytes(int32_t batch, int32_t max_seqlen_q, int hq);
+
+// optional per-request inputs and outputs of the prefill kernel (see prefill.cu)
+struct PrefillExtra {
+    const int32_t* req_klen;
+    const int32_t* req_table_row;
+    float* lse;
+    int32_t kchunks;     // key chunks per request (non-causal), 1 = none
+    int32_t chunk_rows;  // output rows of one chunk (kchunks > 1)
+};
 
 cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_cache,
                            const void* v_cache, const int32_t* cu_q, const int32_t* cu_k,
@@ -67,6 +89,6 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
                            const int32_t* block_table, int32_t max_blocks, int causal,
                            float scale, void* out, void* workspace, int hq, int hkv, int d,
                            int block_size, int64_t num_blocks, unsigned int* err,
-                           cudaStream_t stream);
+                           cudaStream_t stream, const PrefillExtra* extra = nullptr);
 
 }  // namespace pkv

@@ -203,6 +203,19 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 
 struct PrefillArgs {
     uint16_t* out;
+    // optional (else null): keys of request r = req_klen[r] instead of the
+    // cu_k difference, block-table row of request r = req_table_row[r]
+    // instead of r, and the row's log2-sum-exp m + log2(l) in
+    // lse[(row) * hq + head]
+    const int32_t* req_klen;
+    const int32_t* req_table_row;
+    float* lse;
+    // key chunks (non-causal only): grid.z enumerates (request, chunk); chunk
+    // c of a request covers keys [c*per, (c+1)*per), per = its keys / kchunks
+    // rounded up to whole tiles, and writes output rows shifted by
+    // c * chunk_rows (out and lse hold kchunks stacked outputs)
+    int32_t kchunks;
+    int32_t chunk_rows;
     const int32_t* cu_q;
     const int32_t* cu_k;
     const int32_t* table;
@@ -224,6 +237,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsign
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
 }
 
+// kExt: the per-request key counts / table rows, key chunks and log2-sum-exp
+// output of PrefillArgs are in use (a separate instantiation, so the plain
+// prefill compiles without them)
+template <bool kExt>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_o,
@@ -244,13 +261,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.z;
+    const int r = kExt ? (int)blockIdx.z / a.kchunks : (int)blockIdx.z;
+    const int kchunk = kExt ? (int)blockIdx.z % a.kchunks : 0;
     const int qt = a.tiles_q - 1 - (int)blockIdx.x;  // later (heavier) tiles first
     const int h_a = a.pair_heads ? 2 * (int)blockIdx.y : (int)blockIdx.y;
     const bool has_b = a.pair_heads && h_a + 1 < a.hq;
     const int32_t cq0 = a.cu_q[r], cq1 = a.cu_q[r + 1];
     const int32_t ck0 = a.cu_k[r], ck1 = a.cu_k[r + 1];
-    int32_t q_len = cq1 - cq0, k_len = ck1 - ck0;
+    int32_t q_len = cq1 - cq0, k_len = (kExt && a.req_klen) ? a.req_klen[r] : ck1 - ck0;
+    const int64_t trow = (kExt && a.req_table_row) ? a.req_table_row[r] : r;
     // keys a request may have: its block-table row, or (packed K/V) the rows
     // from its first key to the end of the arrays
     const int32_t cap = a.table ? a.max_blocks * a.block_size : max(0, a.oob_row - ck0);
@@ -260,6 +279,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
             flag_error(a.err, PKV_FLAG_BAD_LENGTH);
         if (q_len < 0) q_len = 0;
         k_len = k_len < 0 ? 0 : (k_len > cap ? cap : k_len);
+    }
+    int32_t kbase = 0;  // first key of this chunk
+    if (kExt && a.kchunks > 1) {
+        const int32_t per = ((k_len + a.kchunks - 1) / a.kchunks + BN - 1) / BN * BN;
+        kbase = kchunk * per;
+        k_len = max(0, min(per, k_len - kbase));
     }
     const int32_t q0 = qt * BM;
     if (q0 >= q_len) return;
@@ -273,10 +298,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     int32_t last_key = k_len - 1;
     if (a.causal) last_key = min(last_key, q0 + rows - 1 + diag);
     const int n_tiles = last_key < 0 ? 0 : last_key / BN + 1;
-    const int64_t out_row0 = (int64_t)cq0 + q0;
+    const int64_t out_row0 = (int64_t)cq0 + q0 + (kExt ? (int64_t)kchunk * a.chunk_rows : 0);
 
     if (n_tiles == 0) {  // no query row of this tile sees a key: output 0
         const int nh = has_b ? 2 : 1;
+        if (kExt && a.lse)
+            for (int i = threadIdx.x; i < nh * rows; i += blockDim.x)
+                a.lse[(out_row0 + i % rows) * a.hq + h_a + i / rows] = -INFINITY;
         for (int i = threadIdx.x; i < nh * rows * (HD / 8); i += blockDim.x) {
             const int x = i / (rows * (HD / 8)), rem = i % (rows * (HD / 8));
             const int rr = rem / (HD / 8), c = rem % (HD / 8);
@@ -324,8 +352,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
             int issued = 0, issued_v = 0;
             auto page_row = [&](int32_t key) -> int32_t {
                 if (key >= k_len) return a.oob_row;  // zero-filled by TMA
+                if constexpr (kExt) key += kbase;
                 if (!a.table) return ck0 + key;       // packed K/V
-                const int32_t phys = a.table[(int64_t)r * a.max_blocks + key / a.block_size];
+                const int32_t phys = a.table[trow * a.max_blocks + key / a.block_size];
                 if (phys < 0 || phys >= a.num_blocks) {
                     flag_error(a.err, PKV_FLAG_BAD_BLOCK);
                     return a.oob_row;
@@ -341,6 +370,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
             }
             for (int j = 0; j < n_tiles; ++j) {
                 const int sk = j % SK, sv = j % SV;
+                if (kExt && a.table && pieces > 1 && j + 1 < n_tiles) {
+                    // the next tile's table entries towards L1 while this one waits
+                    // (entries idx0 .. idx1 of the request's row; idx0 < max_blocks
+                    // because a tile starts below k_len <= max_blocks * B)
+                    const int32_t idx0 = (kbase + (j + 1) * BN) / a.block_size;
+                    const int32_t idx1 = min(idx0 + pieces - 1, a.max_blocks - 1);
+                    const int32_t* row = a.table + trow * a.max_blocks;
+                    asm volatile("prefetch.global.L1 [%0];" ::"l"(row + idx0));
+                    asm volatile("prefetch.global.L1 [%0];" ::"l"(row + idx1));
+                }
                 if (!mbar_wait(&k_empty[sk], ((j / SK) & 1) ^ 1, a.err)) break;
                 mbar_arrive_expect_tx(&k_full[sk], kTileBytes);
                 for (int p = 0; p < pieces; ++p) {
@@ -573,6 +612,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         // last reader, QK of the final K tile, completed before o_ready),
         // then stored with coalesced 16-byte writes, 16 threads per row.
         unsigned char* stage = sm + OFF_Q + x * kTileBytes;
+        if (kExt && ok && a.lse && t >= shift)
+            a.lse[(out_row0 + t - shift) * a.hq + h] =
+                l > 0.f ? m_ref * sl + __log2f(l) : -INFINITY;
         if (ok) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -673,7 +715,7 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
                            const int32_t* block_table, int32_t max_blocks, int causal,
                            float scale, void* out, void* workspace, int hq, int hkv, int d,
                            int block_size, int64_t num_blocks, unsigned int* err,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, const PrefillExtra* ex) {
     (void)max_seqlen_k;
     (void)workspace;
     if (d != HD) return cudaErrorNotSupported;
@@ -691,12 +733,22 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
     // last row of its own request, so this bound never clips a valid row
     const int64_t q_rows = std::min<int64_t>((int64_t)batch * max_seqlen_q, 0x7fffffffLL);
     CUtensorMap mq, mo, mk, mv;
-    if (!make_rows_map(&mq, q, hq, q_rows, BM) || !make_rows_map(&mo, out, hq, q_rows, BM) ||
+    const int kchunks = (ex && ex->kchunks > 1 && !causal) ? ex->kchunks : 1;
+    if ((int64_t)batch * kchunks > 65535) return cudaErrorNotSupported;
+    // output rows: kchunks stacked outputs of chunk_rows rows each
+    const int64_t o_rows =
+        kchunks > 1 ? std::min<int64_t>((int64_t)kchunks * ex->chunk_rows, 0x7fffffffLL) : q_rows;
+    if (!make_rows_map(&mq, q, hq, q_rows, BM) || !make_rows_map(&mo, out, hq, o_rows, BM) ||
         !make_rows_map(&mk, k_cache, hkv, rows, piece) ||
         !make_rows_map(&mv, v_cache, hkv, rows, piece))
         return cudaErrorInvalidValue;
     PrefillArgs a;
     a.out = static_cast<uint16_t*>(out);
+    a.req_klen = ex ? ex->req_klen : nullptr;
+    a.req_table_row = ex ? ex->req_table_row : nullptr;
+    a.lse = ex ? ex->lse : nullptr;
+    a.kchunks = (ex && ex->kchunks > 1 && !causal) ? ex->kchunks : 1;
+    a.chunk_rows = ex ? ex->chunk_rows : 0;
     a.cu_q = cu_q;
     a.cu_k = cu_k;
     a.table = block_table;
@@ -712,12 +764,12 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
     a.oob_row = (int32_t)rows;
     a.tiles_q = (max_seqlen_q + BM - 1) / BM;
     a.causal = causal ? 1 : 0;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    auto kern = ex ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.tiles_q, a.pair_heads ? (hq + 1) / 2 : hq, batch);
-    prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mo, mk, mv, a);
+    dim3 grid(a.tiles_q, a.pair_heads ? (hq + 1) / 2 : hq, batch * a.kchunks);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(mq, mo, mk, mv, a);
     return cudaGetLastError();
 }
 
