@@ -500,6 +500,7 @@ def run_decode(args, world, pkv, W, hbm_peak, peak_src, line):
         "clocks": clk,
     })
     line["gpu_launches"] += 4 * args.steps
+    run_decode_append(args, world, pkv, dstep, ddev, step_bytes, hbm_peak, peak_src, line)
     if not args.no_e2e:
         e2e_ms, h2d, d2h = time_e2e(dstep, ddev, args.steps, args.warmup, world)
         line["e2e"] = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2),
@@ -515,6 +516,44 @@ W_NAME_PACKED = ("causal varlen prefill over packed K/V: the chunked-prefill wor
                  "requests (q~U[1,2048], cached~U[0,2048]) with each request's keys "
                  "contiguous; L2 flushed between steps")
 COPY_PAIRS, COPY_GEOM = 8192, (16, 8, 128)  # block pairs; B, Hkv, d (bf16)
+
+
+def run_decode_append(args, world, pkv, dstep, ddev, step_bytes, hbm_peak, peak_src, line):
+    """The same decode step in one call: paged_decode_append writes the new
+    token's K/V and attends over the cached keys plus the new one (split +
+    combine, two launches instead of four)."""
+    before = to_dev((dstep.cache_seqlens - 1).astype(np.int32))
+    out = torch.empty_like(ddev.q)
+    call = lambda: pkv.paged_decode_append(ddev.q, ddev.new_k, ddev.new_v, ddev.k_cache,
+                                           ddev.v_cache, ddev.dtable, before, dstep.scale,
+                                           out=out, workspace=ddev.ws)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for a, b in ev:
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = [a.elapsed_time(b) for a, b in ev]
+    mean = max_over_ranks(float(np.mean(ms)), world)
+    gbs = step_bytes / (mean * 1e-3) / 1e9
+    line["decode_append"] = {
+        "metric": "decode KV GB/s, step as one call with the in-place append", "unit": "GB/s",
+        "value": round(world * gbs, 2), "ms_per_step": round(mean, 5),
+        "workload": "the headline long-context decode step (same bytes per step)",
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_append (split + combine with the "
+                     "appended key and its cache write)", "achieved": round(gbs, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                     "peak_source": peak_src, "traffic": None, "mean_ms": round(mean, 5),
+                     "median_ms": round(float(np.median(ms)), 5)}}
+    line["gpu_launches"] += 2 * args.steps
 
 
 def run_copy(args, world, pkv, hbm_peak, peak_src, line):

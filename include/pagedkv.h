@@ -138,6 +138,28 @@ int paged_decode(const void* q, const void* k_cache, const void* v_cache,
                  cudaStream_t stream);
 
 /*
+ * paged_decode_append -- paged_decode with the in-place append of the new
+ * token ("Sayfalı dikkat" decode path: the flash_attn_with_kvcache call takes
+ * the new k and v, writes them into the cache and attends over them together
+ * with the cached keys).  cache_seqlens[b] counts the keys cached BEFORE this
+ * step.  For every sequence b:
+ *   - k_new[b], v_new[b] ([batch, Hkv, d], the cache dtype) are written at
+ *     position cache_seqlens[b] (slot = block_table[b][L / B] * B + L % B);
+ *   - out[b,h] = attention of q[b,h] over the cache_seqlens[b] cached keys
+ *     and the new key (cache_seqlens[b] + 1 keys in all).
+ * The caller advances cache_seqlens afterwards.  The new key is scored from
+ * k_new directly (not read back from the cache) and written after the cached
+ * keys have been read.  Supported, workspace and errors as paged_decode (same
+ * workspace size); a position past max_blocks_per_seq * B or a bad table
+ * entry skips that write and sets PKV_FLAG_BAD_LENGTH / _BAD_BLOCK.
+ */
+int paged_decode_append(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                        void* v_cache, const int32_t* block_table, int32_t max_blocks_per_seq,
+                        const int32_t* cache_seqlens, int32_t batch, float scale, void* out,
+                        void* workspace, size_t workspace_bytes, const pkv_geom* geom,
+                        cudaStream_t stream);
+
+/*
  * paged_varlen_prefill_workspace_size -- bytes of device scratch
  * paged_varlen_prefill needs (0 when it needs none).  Returns 0 for invalid
  * arguments as well.

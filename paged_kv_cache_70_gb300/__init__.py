@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     load_library,
     paged_build_slot_mapping,
     paged_decode,
+    paged_decode_append,
     paged_decode_noalloc,
     paged_decode_shared_prefix,
     paged_decode_workspace_size,

@@ -49,6 +49,7 @@ EXPORTED = (
     "paged_copy_blocks",
     "paged_decode_shared_prefix_workspace_size",
     "paged_decode_shared_prefix",
+    "paged_decode_append",
 )
 PKV_ERR_NO_SPACE = -5
 
@@ -128,6 +129,9 @@ def load_library(path: str | None = None):
         lib.paged_decode_shared_prefix.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, vp, i32, i32,
                                                    ctypes.c_float, vp, vp, sz, gp, vp]
         lib.paged_decode_shared_prefix.restype = ctypes.c_int
+        lib.paged_decode_append.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, ctypes.c_float,
+                                            vp, vp, sz, gp, vp]
+        lib.paged_decode_append.restype = ctypes.c_int
         lib.paged_copy_blocks.argtypes = [vp, vp, vp, vp, i32, gp, vp]
         lib.paged_copy_blocks.restype = ctypes.c_int
         lib.paged_status_string.argtypes = [ctypes.c_int]
@@ -271,6 +275,43 @@ def paged_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
             _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
             _ptr(cache_seqlens), batch, scale, _ptr(out), ctypes.byref(g), _stream(q))
     _check("paged_decode_noalloc", st)
+    return out
+
+
+def paged_decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                        k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
+                        cache_seqlens: torch.Tensor, scale: float | None = None,
+                        out: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Decode with the in-place append: k_new/v_new [batch, Hkv, d] are written
+    at position cache_seqlens[b] (keys cached before the step) and attended to
+    together with the cached keys."""
+    _cuda_contig("q", q, k_cache.dtype)
+    _cuda_contig("k_new", k_new, k_cache.dtype)
+    _cuda_contig("v_new", v_new, k_cache.dtype)
+    _cuda_contig("k_cache", k_cache)
+    _cuda_contig("v_cache", v_cache, k_cache.dtype)
+    _cuda_contig("block_table", block_table, torch.int32)
+    _cuda_contig("cache_seqlens", cache_seqlens, torch.int32)
+    batch, hq, d = q.shape
+    if k_new.shape != (batch,) + tuple(k_cache.shape[2:]) or v_new.shape != k_new.shape:
+        raise ValueError("k_new / v_new must be [batch, Hkv, d]")
+    g = geom_of(k_cache, hq)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        need = int(lib.paged_decode_workspace_size(batch, ctypes.byref(g)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, q.dtype)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    with torch.cuda.device(q.device):
+        st = lib.paged_decode_append(
+            _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+            block_table.shape[1], _ptr(cache_seqlens), batch, scale, _ptr(out), _ptr(workspace),
+            workspace.numel(), ctypes.byref(g), _stream(q))
+    _check("paged_decode_append", st)
     return out
 
 

@@ -146,6 +146,36 @@ int paged_decode(const void* q, const void* k_cache, const void* v_cache,
                                           geom->dtype, dev.err, stream));
 }
 
+int paged_decode_append(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                        void* v_cache, const int32_t* block_table, int32_t max_blocks_per_seq,
+                        const int32_t* cache_seqlens, int32_t batch, float scale, void* out,
+                        void* workspace, size_t workspace_bytes, const pkv_geom* geom,
+                        cudaStream_t stream) {
+    int st = check_geom(geom);
+    if (st != PKV_OK) return st;
+    if (batch < 0 || max_blocks_per_seq < 0) return PKV_ERR_INVALID;
+    if (batch == 0) return PKV_OK;
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !block_table || !cache_seqlens || !out)
+        return PKV_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(k_new, 16) || !aligned(v_new, 16))
+        return PKV_ERR_INVALID;
+    DeviceInfo dev;
+    if (pkv::current_device_info(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    pkv::DecodePlan plan;
+    if (!pkv::plan_decode(dev, batch, geom->num_heads, geom->num_kv_heads, geom->head_dim,
+                          geom->block_size, elt_size(geom->dtype), &plan))
+        return PKV_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256))
+        return PKV_ERR_WORKSPACE;
+    pkv::DecodeAppend ap{k_new, v_new, k_cache, v_cache};
+    return cuda_status(pkv::launch_decode(plan, q, k_cache, v_cache, block_table,
+                                          max_blocks_per_seq, cache_seqlens, batch, scale, out,
+                                          workspace, geom->num_heads, geom->num_kv_heads,
+                                          geom->head_dim, geom->block_size, geom->num_blocks,
+                                          geom->dtype, dev.err, stream, nullptr, &ap));
+}
+
 size_t paged_varlen_prefill_workspace_size(int32_t batch, int32_t max_seqlen_q,
                                            const pkv_geom* geom) {
     if (check_geom(geom) != PKV_OK || batch < 0 || max_seqlen_q < 0) return 0;

@@ -486,56 +486,113 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
     }
 }
 
+// Inputs of the combine kernel.
+struct CombineArgs {
+    const float* part_o;
+    const float* part_ml;
+    const int32_t* tstart;
+    int32_t batch;
+    int ctas;
+    int hq;
+    void* out;
+    // shared-prefix mode (else null): x_chunks prefix partials per (sequence,
+    // head), normalised output (bf16) and log2-sum-exp
+    const uint16_t* x_out;
+    const float* x_lse;
+    int x_chunks;
+    // in-place append (else null): sequence b's new token (k_new, v_new
+    // [batch, hkv, D]) joins the attention as one more key and is written to
+    // the cache at position seqlens[b] through the block table
+    const void* q;
+    const void* k_new;
+    const void* v_new;
+    unsigned char* k_cache;
+    unsigned char* v_cache;
+    const int32_t* table;
+    const int32_t* seqlens;
+    int64_t num_blocks;
+    int32_t max_blocks;
+    int32_t block_size;
+    int32_t hkv;
+    float qscale;
+    unsigned int* err;
+};
+
+// DPL consecutive elements of a bf16 or fp32 row as fp32
+template <bool BF16, int DPL>
+__device__ __forceinline__ void load_row(const void* base, int64_t elem, float* x) {
+#pragma unroll
+    for (int e = 0; e < DPL; ++e)
+        x[e] = BF16 ? __uint_as_float((uint32_t) static_cast<const uint16_t*>(base)[elem + e] << 16)
+                    : static_cast<const float*>(base)[elem + e];
+}
+
 // Merge the partial states of every (sequence, head) and normalise.  One warp
-// per (sequence, head); lane i owns dims [i*D/32, (i+1)*D/32).  In shared-
-// prefix mode one more partial joins the merge: the prefix attention's
-// normalised output x_out (bf16) with x_lse = m + log2(l) in the same log2
-// units, i.e. the state (m = x_lse, l = 1, o = x_out).
+// per (sequence, head); lane i owns dims [i*D/32, (i+1)*D/32).  Shared-prefix
+// mode adds the prefix chunks, each as the state (m = lse, l = 1, o = out);
+// append mode adds the new key (m = its score, l = 1, o = its V row) and
+// writes the new K/V row into the cache (the split kernel, which read only
+// the keys before it, has completed).
 template <int D, bool BF16>
-__global__ void __launch_bounds__(128)
-decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-                      const int32_t* __restrict__ tstart, int32_t batch, int ctas, int hq,
-                      void* __restrict__ out, const uint16_t* __restrict__ x_out,
-                      const float* __restrict__ x_lse, int x_chunks) {
+__global__ void __launch_bounds__(128) decode_combine_kernel(const CombineArgs c) {
     constexpr int DPL = D / 32;
     // wait until the split kernel's partials are complete and visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int hq = c.hq, batch = c.batch;
     if (w >= (int64_t)batch * hq) return;
     const int b = (int)(w / hq), h = (int)(w % hq);
-    const int32_t total = tstart[batch];
-    const int32_t tb0 = tstart[b], tb1 = tstart[b + 1];
+    const int32_t total = c.tstart[batch];
+    const int32_t tb0 = c.tstart[b], tb1 = c.tstart[b + 1];
     float acc[DPL];
 #pragma unroll
     for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
     float lt = 0.f;
-    const int32_t chunk = total > 0 ? (total + ctas - 1) / ctas : 1;
+    const int32_t chunk = total > 0 ? (total + c.ctas - 1) / c.ctas : 1;
     const int c0 = tb0 / chunk, c1 = tb1 > tb0 ? (tb1 - 1) / chunk : c0 - 1;
     const int64_t xstride = (int64_t)batch * hq;  // one prefix chunk's (sequence, head) count
     float M = -INFINITY;
-    for (int c = lane; c < x_chunks; c += 32) M = fmaxf(M, x_lse[c * xstride + (int64_t)b * hq + h]);
-    for (int c = c0 + lane; c <= c1; c += 32)
-        M = fmaxf(M, part_ml[(((int64_t)c + b) * hq + h) * 2]);
+    for (int x = lane; x < c.x_chunks; x += 32)
+        M = fmaxf(M, c.x_lse[x * xstride + (int64_t)b * hq + h]);
+    for (int cc = c0 + lane; cc <= c1; cc += 32)
+        M = fmaxf(M, c.part_ml[(((int64_t)cc + b) * hq + h) * 2]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    // the appended key: score q . k_new in log2 units
+    const int kvh = h / (hq / (c.hkv > 0 ? c.hkv : 1));
+    float s_new = -INFINITY, v_new[DPL];
+    if (c.k_new) {
+        const int64_t row = ((int64_t)b * c.hkv + kvh) * D + lane * DPL;
+        float qv[DPL], kv[DPL];
+        load_row<BF16, DPL>(c.q, ((int64_t)b * hq + h) * D + lane * DPL, qv);
+        load_row<BF16, DPL>(c.k_new, row, kv);
+        load_row<BF16, DPL>(c.v_new, row, v_new);
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) dot = fmaf(qv[e], kv[e], dot);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        s_new = dot * c.qscale;
+        M = fmaxf(M, s_new);
+    }
     if (M != -INFINITY) {
 #pragma unroll 4
-        for (int c = c0; c <= c1; ++c) {
-            const int64_t slot = (int64_t)c + b;
-            const float2 ml = *reinterpret_cast<const float2*>(part_ml + (slot * hq + h) * 2);
+        for (int cc = c0; cc <= c1; ++cc) {
+            const int64_t slot = (int64_t)cc + b;
+            const float2 ml = *reinterpret_cast<const float2*>(c.part_ml + (slot * hq + h) * 2);
             const float wgt = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
             lt += ml.y * wgt;
-            const float* src = part_o + (slot * hq + h) * D + lane * DPL;
+            const float* src = c.part_o + (slot * hq + h) * D + lane * DPL;
 #pragma unroll
             for (int e = 0; e < DPL; ++e) acc[e] += src[e] * wgt;
         }
-        for (int c = 0; c < x_chunks; ++c) {
-            const float mx = x_lse[c * xstride + (int64_t)b * hq + h];
+        for (int x = 0; x < c.x_chunks; ++x) {
+            const float mx = c.x_lse[x * xstride + (int64_t)b * hq + h];
             if (mx == -INFINITY) continue;
             const float wgt = ex2(mx - M);
             lt += wgt;
-            const uint16_t* src = x_out + (c * xstride + (int64_t)b * hq + h) * D + lane * DPL;
+            const uint16_t* src = c.x_out + (x * xstride + (int64_t)b * hq + h) * D + lane * DPL;
 #pragma unroll
             for (int e = 0; e < DPL; e += 2) {
                 const uint32_t pr = *reinterpret_cast<const uint32_t*>(src + e);
@@ -543,18 +600,50 @@ decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict_
                 acc[e + 1] += bf16hi(pr) * wgt;
             }
         }
+        if (c.k_new) {
+            const float wgt = ex2(s_new - M);
+            lt += wgt;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[e] = fmaf(v_new[e], wgt, acc[e]);
+        }
     }
     const float inv = lt > 0.f ? 1.f / lt : 0.f;
     const int64_t oi = ((int64_t)b * hq + h) * D + lane * DPL;
     if constexpr (BF16) {
-        uint16_t* o = static_cast<uint16_t*>(out) + oi;
+        uint16_t* o = static_cast<uint16_t*>(c.out) + oi;
 #pragma unroll
         for (int e = 0; e < DPL; e += 2)
             *reinterpret_cast<uint32_t*>(o + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
     } else {
-        float* o = static_cast<float*>(out) + oi;
+        float* o = static_cast<float*>(c.out) + oi;
 #pragma unroll
         for (int e = 0; e < DPL; ++e) o[e] = acc[e] * inv;
+    }
+    // one warp per KV head writes the new K/V row into the cache
+    if (c.k_new && h % (hq / c.hkv) == 0) {
+        const int32_t L = c.seqlens[b];
+        const int32_t B = c.block_size;
+        if (L < 0 || L >= c.max_blocks * B) {
+            if (lane == 0) flag_error(c.err, PKV_FLAG_BAD_LENGTH);
+            return;
+        }
+        const int32_t phys = c.table[(int64_t)b * c.max_blocks + L / B];
+        if (phys < 0 || phys >= c.num_blocks) {
+            if (lane == 0) flag_error(c.err, PKV_FLAG_BAD_BLOCK);
+            return;
+        }
+        constexpr int ELT = BF16 ? 2 : 4;
+        const int64_t src = ((int64_t)b * c.hkv + kvh) * D + lane * DPL;
+        const int64_t dst = (((int64_t)phys * B + L % B) * c.hkv + kvh) * D + lane * DPL;
+#pragma unroll
+        for (int e = 0; e < DPL * ELT; e += 4) {
+            *reinterpret_cast<uint32_t*>(c.k_cache + dst * ELT + e) =
+                *reinterpret_cast<const uint32_t*>(static_cast<const unsigned char*>(c.k_new) +
+                                                   src * ELT + e);
+            *reinterpret_cast<uint32_t*>(c.v_cache + dst * ELT + e) =
+                *reinterpret_cast<const uint32_t*>(static_cast<const unsigned char*>(c.v_new) +
+                                                   src * ELT + e);
+        }
     }
 }
 
@@ -606,9 +695,8 @@ bool plan_decode(const DeviceInfo& dev, int32_t batch, int hq, int hkv, int d, i
 }
 
 template <int D, bool BF16, int G>
-static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a, void* out,
-                                   const uint16_t* x_out, const float* x_lse, int x_chunks,
-                                   cudaStream_t stream) {
+static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a,
+                                   const CombineArgs& c, cudaStream_t stream) {
     auto kern = decode_split_kernel<D, BF16, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)plan.smem_bytes);
@@ -629,11 +717,7 @@ static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, BF16>,
-                              static_cast<const float*>(a.part_o),
-                              static_cast<const float*>(a.part_ml),
-                              static_cast<const int32_t*>(a.tstart_out), a.batch, plan.ctas,
-                              a.hq, out, x_out, x_lse, x_chunks);
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, BF16>, c);
 }
 
 cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_cache,
@@ -641,15 +725,13 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
                           const int32_t* cache_seqlens, int32_t batch, float scale, void* out,
                           void* workspace, int hq, int hkv, int d, int block_size,
                           int64_t num_blocks, int dtype, unsigned int* err, cudaStream_t stream,
-                          const SharedPrefix* sp) {
+                          const SharedPrefix* sp, const DecodeAppend* ap) {
     if (batch == 0) return cudaSuccess;
     DecodeArgs a;
     a.group_cu = sp ? sp->group_cu : nullptr;
     a.group_plen = sp ? sp->group_plen : nullptr;
     a.n_groups = sp ? sp->n_groups : 0;
-    const uint16_t* x_out = sp ? static_cast<const uint16_t*>(sp->x_out) : nullptr;
-    const float* x_lse = sp ? sp->x_lse : nullptr;
-    const int x_chunks = sp ? sp->x_chunks : 0;
+
     a.q = q;
     a.k_cache = static_cast<const unsigned char*>(k_cache);
     a.v_cache = static_cast<const unsigned char*>(v_cache);
@@ -675,9 +757,36 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
     a.stages = plan.stages;
     const int G = hq / hkv;
     const bool bf = dtype == PKV_BF16;
+    CombineArgs c = {};
+    c.part_o = a.part_o;
+    c.part_ml = a.part_ml;
+    c.tstart = a.tstart_out;
+    c.batch = batch;
+    c.ctas = plan.ctas;
+    c.hq = hq;
+    c.out = out;
+    if (sp) {
+        c.x_out = static_cast<const uint16_t*>(sp->x_out);
+        c.x_lse = sp->x_lse;
+        c.x_chunks = sp->x_chunks;
+    }
+    if (ap) {
+        c.q = q;
+        c.k_new = ap->k_new;
+        c.v_new = ap->v_new;
+        c.k_cache = static_cast<unsigned char*>(ap->k_cache);
+        c.v_cache = static_cast<unsigned char*>(ap->v_cache);
+        c.table = block_table;
+        c.seqlens = cache_seqlens;
+        c.num_blocks = num_blocks;
+        c.max_blocks = max_blocks;
+        c.block_size = block_size;
+    }
+    c.hkv = hkv;
+    c.qscale = a.qscale;
+    c.err = err;
 #define PKV_DECODE_CASE(DD, BB, GG) \
-    if (d == DD && bf == BB && G == GG) \
-        return launch_decode_t<DD, BB, GG>(plan, a, out, x_out, x_lse, x_chunks, stream);
+    if (d == DD && bf == BB && G == GG) return launch_decode_t<DD, BB, GG>(plan, a, c, stream);
     PKV_DECODE_CASE(128, true, 1) PKV_DECODE_CASE(128, true, 2) PKV_DECODE_CASE(128, true, 4)
     PKV_DECODE_CASE(128, false, 1) PKV_DECODE_CASE(128, false, 2) PKV_DECODE_CASE(128, false, 4)
     PKV_DECODE_CASE(64, true, 1) PKV_DECODE_CASE(64, true, 2) PKV_DECODE_CASE(64, true, 4)

@@ -60,6 +60,15 @@ struct SharedPrefix {
     int32_t x_chunks;           // prefix partials per (sequence, head)
 };
 
+// In-place append: the new token of every sequence ([batch, hkv, d], the
+// cache dtype) is attended to as key cache_seqlens[b] and written there.
+struct DecodeAppend {
+    const void* k_new;
+    const void* v_new;
+    void* k_cache;
+    void* v_cache;
+};
+
 // Returns false when the geometry is not supported.
 bool plan_decode(const DeviceInfo& dev, int32_t batch, int hq, int hkv, int d, int block_size,
                  int elt, DecodePlan* plan);
@@ -69,7 +78,8 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
                           const int32_t* cache_seqlens, int32_t batch, float scale, void* out,
                           void* workspace, int hq, int hkv, int d, int block_size,
                           int64_t num_blocks, int dtype, unsigned int* err, cudaStream_t stream,
-                          const SharedPrefix* shared = nullptr);
+                          const SharedPrefix* shared = nullptr,
+                          const DecodeAppend* append = nullptr);
 
 // ---- prefill ----------------------------------------------------------------
 size_t prefill_workspace_bytes(int32_t batch, int32_t max_seqlen_q, int hq);
