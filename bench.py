@@ -45,7 +45,7 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--only", choices=["all", "decode", "prefill", "copy", "shared"],
+    p.add_argument("--only", choices=["all", "decode", "prefill", "copy", "shared", "mixed"],
                    default="all",
                    help="measure one half only (profiling runs)")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
@@ -441,10 +441,16 @@ def main():
         run_copy(args, world, pkv, hbm_peak, peak_src, line)
     if args.only in ("all", "shared"):
         run_shared_prefix(args, world, pkv, W, hbm_peak, peak_src, line)
+    if args.only in ("all", "mixed"):
+        run_mixed_step(args, world, pkv, W, hbm_peak, peak_src, line)
     if args.only == "prefill":  # headline comes from the prefill half
         line["metric"] = "varlen prefill TFLOP/s"
         line["value"], line["unit"] = line["prefill"].get("value"), "TFLOP/s"
         line["ms_per_step"] = line["prefill"].get("ms_per_step")
+    if args.only == "mixed":
+        line["metric"] = line["mixed_step"]["metric"]
+        line["value"] = line["mixed_step"]["value"]
+        line["ms_per_step"] = line["mixed_step"]["ms_per_step"]
     if args.only == "shared":
         line["metric"] = line["decode_shared_prefix"]["metric"]
         line["value"] = line["decode_shared_prefix"]["value"]
@@ -673,6 +679,80 @@ def run_shared_prefix(args, world, pkv, W, hbm_peak, peak_src, line):
     line["gpu_launches"] += 3 * args.steps
     line["error_flags"] |= pkv.paged_error_flags()
     del k_cache, v_cache, ws, wsp, flush
+    torch.cuda.empty_cache()
+
+
+def run_mixed_step(args, world, pkv, W, hbm_peak, peak_src, line):
+    """The whole continuous-batching step in one paged_mixed_step call: 2304
+    new rows (+5 % padding) written, causal prefill of 4 x 512 tokens, and
+    the in-place append + shared-prefix decode of 256 sequences.  Bytes
+    counted once each: K/V of every key read (shared prefixes once), the new
+    rows read and written, q and out."""
+    s = W.config(5)
+    nd = s.n_decode
+    is_dec = (s.token_seq >= 0) & (s.token_seq < nd)
+    dec_rows = np.where(is_dec)[0]
+    dec_rows = dec_rows[np.argsort(s.token_seq[dec_rows])]
+    pf_rows = np.where(~is_dec)[0]
+    B = s.block_size
+    seq = s.token_seq
+    slots = np.full(len(seq), -1, np.int32)
+    ok = seq >= 0
+    slots[ok] = s.table[seq[ok], s.token_pos[ok] // B] * B + s.token_pos[ok] % B
+    kc, vc = to_dev(s.k_cache), to_dev(s.v_cache)
+    decode = dict(q=to_dev(s.q_decode), k_new=to_dev(s.new_k[dec_rows]),
+                  v_new=to_dev(s.new_v[dec_rows]), table=to_dev(s.decode_table.copy()),
+                  seqlens=to_dev(s.cache_seqlens - 1),
+                  group_cu=to_dev(np.arange(0, nd + 1, nd // 8, dtype=np.int32)),
+                  group_prefix_len=to_dev(np.full(8, 2048, np.int32)), max_group_size=nd // 8,
+                  out=torch.empty(s.q_decode.shape, dtype=torch.bfloat16, device="cuda"))
+    prefill = dict(k_new=to_dev(s.new_k[pf_rows]), v_new=to_dev(s.new_v[pf_rows]),
+                   slots=to_dev(slots[pf_rows]), q=to_dev(s.q_prefill), cu_q=to_dev(s.cu_q),
+                   cu_k=to_dev(s.cu_k), max_q=s.max_seqlen_q, max_k=s.max_seqlen_k,
+                   table=to_dev(s.prefill_table.copy()),
+                   out=torch.empty(s.q_prefill.shape, dtype=torch.bfloat16, device="cuda"))
+    ws = torch.empty(pkv._binding.load_library().paged_mixed_step_workspace_size(
+        nd, ctypes.byref(pkv.geom_of(kc, s.hq))), dtype=torch.uint8, device="cuda")
+    row = s.hkv * s.d * 2 * 2
+    n_new = int((s.token_seq >= 0).sum())
+    nbytes = ((8 * 2048 + int((s.cache_seqlens - 1 - 2048).sum())) * row  # decode keys once
+              + int(s.cu_k[-1]) * row                                    # prefill keys
+              + 2 * n_new * row                                           # new rows r + w
+              + 2 * (s.q_decode.size + s.q_prefill.size) * 2)             # q and out
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    call = lambda: pkv.paged_mixed_step(kc, vc, s.scale, prefill=prefill, decode=decode,
+                                        workspace=ws)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for i, (a, b) in enumerate(ev):
+        flush.fill_(i & 0xff)
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = [a.elapsed_time(b) for a, b in ev]
+    mean = max_over_ranks(float(np.mean(ms)), world)
+    gbs = nbytes / (mean * 1e-3) / 1e9
+    line["mixed_step"] = {
+        "metric": "continuous-batching step GB/s of unique bytes", "unit": "GB/s",
+        "value": round(world * gbs, 1), "ms_per_step": round(mean, 5),
+        "workload": W.CONFIG_NAMES[5] + "; one paged_mixed_step call; L2 flushed between steps",
+        "unique_bytes": nbytes,
+        "roofline": {"bound": "hbm", "kernel": "paged_mixed_step (write, prefill, shared-prefix "
+                     "pass, split, combine with append)", "achieved": round(gbs, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                     "peak_source": peak_src, "traffic": None, "mean_ms": round(mean, 5),
+                     "median_ms": round(float(np.median(ms)), 5)}}
+    line["gpu_launches"] += 5 * args.steps
+    line["error_flags"] |= pkv.paged_error_flags()
+    del kc, vc, ws, flush
     torch.cuda.empty_cache()
 
 

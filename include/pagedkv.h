@@ -229,6 +229,61 @@ int paged_decode_shared_prefix(const void* q, const void* k_cache, const void* v
                                cudaStream_t stream);
 
 /*
+ * paged_mixed_step -- one continuous-batching step in one call: prefill
+ * requests and decode sequences over the same pools ("从零开始写Qwen3（六）
+ * PagedAttention", "fast-attn 库的使用": the varlen call for prefill, the
+ * kvcache call for decode; "11. Paged attention 与 online softmax" §11.3 for
+ * groups sharing a prefix).  In order on `stream`:
+ *   1. the prefill requests' new K/V rows are written at prefill_slots
+ *      (paged_kv_write; negative slots skipped);
+ *   2. causal varlen prefill of the prefill requests (paged_varlen_prefill);
+ *   3. decode of the decode sequences with the in-place append
+ *      (paged_decode_append), through the shared-prefix path when n_groups > 0
+ *      (paged_decode_shared_prefix semantics).
+ * Parts with a zero count are skipped.  The decode kernels are launched as
+ * programmatic dependents of the prefill kernel, which they do not read: they
+ * start on SMs the prefill leaves free instead of after it.  Arguments mean
+ * what they mean in the single calls; all pointers in the struct are DEVICE
+ * pointers.  Supported as the single calls; with a prefill part or groups:
+ * bf16 and head_dim 128.  workspace: at least
+ * paged_mixed_step_workspace_size(decode_batch, geom) bytes, 256-byte aligned.
+ */
+typedef struct pkv_mixed_step {
+    /* prefill requests */
+    const void* prefill_k_new;   /* [prefill_new_tokens, Hkv, d] */
+    const void* prefill_v_new;
+    const int32_t* prefill_slots; /* [prefill_new_tokens] */
+    int64_t prefill_new_tokens;
+    const void* prefill_q;        /* [total_q, Hq, d] */
+    const int32_t* cu_seqlens_q;  /* [prefill_batch + 1] */
+    const int32_t* cu_seqlens_k;
+    int32_t prefill_batch;
+    int32_t max_seqlen_q;
+    int32_t max_seqlen_k;
+    const int32_t* prefill_table; /* [prefill_batch, prefill_max_blocks] */
+    int32_t prefill_max_blocks;
+    void* prefill_out;            /* [total_q, Hq, d] */
+    /* decode sequences (in-place append) */
+    const void* decode_q;         /* [decode_batch, Hq, d] */
+    const void* decode_k_new;     /* [decode_batch, Hkv, d] */
+    const void* decode_v_new;
+    const int32_t* decode_table;  /* [decode_batch, decode_max_blocks] */
+    int32_t decode_max_blocks;
+    const int32_t* decode_seqlens; /* keys cached before the step */
+    int32_t decode_batch;
+    const int32_t* group_cu;      /* [n_groups + 1], or NULL with n_groups 0 */
+    const int32_t* group_prefix_len;
+    int32_t n_groups;
+    int32_t max_group_size;
+    void* decode_out;             /* [decode_batch, Hq, d] */
+    float scale;
+} pkv_mixed_step;
+
+size_t paged_mixed_step_workspace_size(int32_t decode_batch, const pkv_geom* geom);
+int paged_mixed_step(const pkv_mixed_step* step, void* k_cache, void* v_cache, void* workspace,
+                     size_t workspace_bytes, const pkv_geom* geom, cudaStream_t stream);
+
+/*
  * paged_decode_noalloc -- paged_decode for callers that cannot allocate device
  * memory.  The pages have no counterpart: this is a deployment variant of
  * paged_decode that takes no workspace.

@@ -26,6 +26,7 @@ from ._binding import (  # noqa: F401
     paged_decode,
     paged_decode_append,
     paged_decode_noalloc,
+    paged_mixed_step,
     paged_decode_shared_prefix,
     paged_decode_workspace_size,
     paged_error_flags,

@@ -50,6 +50,8 @@ EXPORTED = (
     "paged_decode_shared_prefix_workspace_size",
     "paged_decode_shared_prefix",
     "paged_decode_append",
+    "paged_mixed_step_workspace_size",
+    "paged_mixed_step",
 )
 PKV_ERR_NO_SPACE = -5
 
@@ -68,6 +70,26 @@ class Geom(ctypes.Structure):
         ("block_size", ctypes.c_int32),
         ("num_blocks", ctypes.c_int64),
         ("dtype", ctypes.c_int32),
+    ]
+
+
+class MixedStep(ctypes.Structure):
+    """pkv_mixed_step of include/pagedkv.h"""
+    _fields_ = [
+        ("prefill_k_new", ctypes.c_void_p), ("prefill_v_new", ctypes.c_void_p),
+        ("prefill_slots", ctypes.c_void_p), ("prefill_new_tokens", ctypes.c_int64),
+        ("prefill_q", ctypes.c_void_p), ("cu_seqlens_q", ctypes.c_void_p),
+        ("cu_seqlens_k", ctypes.c_void_p), ("prefill_batch", ctypes.c_int32),
+        ("max_seqlen_q", ctypes.c_int32), ("max_seqlen_k", ctypes.c_int32),
+        ("prefill_table", ctypes.c_void_p), ("prefill_max_blocks", ctypes.c_int32),
+        ("prefill_out", ctypes.c_void_p),
+        ("decode_q", ctypes.c_void_p), ("decode_k_new", ctypes.c_void_p),
+        ("decode_v_new", ctypes.c_void_p), ("decode_table", ctypes.c_void_p),
+        ("decode_max_blocks", ctypes.c_int32), ("decode_seqlens", ctypes.c_void_p),
+        ("decode_batch", ctypes.c_int32), ("group_cu", ctypes.c_void_p),
+        ("group_prefix_len", ctypes.c_void_p), ("n_groups", ctypes.c_int32),
+        ("max_group_size", ctypes.c_int32), ("decode_out", ctypes.c_void_p),
+        ("scale", ctypes.c_float),
     ]
 
 
@@ -132,6 +154,10 @@ def load_library(path: str | None = None):
         lib.paged_decode_append.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, ctypes.c_float,
                                             vp, vp, sz, gp, vp]
         lib.paged_decode_append.restype = ctypes.c_int
+        lib.paged_mixed_step_workspace_size.argtypes = [i32, gp]
+        lib.paged_mixed_step_workspace_size.restype = sz
+        lib.paged_mixed_step.argtypes = [ctypes.POINTER(MixedStep), vp, vp, vp, sz, gp, vp]
+        lib.paged_mixed_step.restype = ctypes.c_int
         lib.paged_copy_blocks.argtypes = [vp, vp, vp, vp, i32, gp, vp]
         lib.paged_copy_blocks.restype = ctypes.c_int
         lib.paged_status_string.argtypes = [ctypes.c_int]
@@ -511,3 +537,73 @@ def paged_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src: torch.T
         st = load_library().paged_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(src), _ptr(dst),
                                               src.numel(), ctypes.byref(g), _stream(k_cache))
     _check("paged_copy_blocks", st)
+
+
+def paged_mixed_step(k_cache: torch.Tensor, v_cache: torch.Tensor, scale: float,
+                     prefill: dict | None = None, decode: dict | None = None,
+                     workspace: torch.Tensor | None = None):
+    """One continuous-batching step (include/pagedkv.h, paged_mixed_step).
+
+    prefill: k_new, v_new [N, Hkv, d] and slots [N] (the requests' new rows,
+    negative slots skipped), q [total_q, Hq, d], cu_q, cu_k, max_q, max_k,
+    table; decode: q [batch, Hq, d], k_new, v_new [batch, Hkv, d], table,
+    seqlens (keys cached before the step), optionally group_cu,
+    group_prefix_len, max_group_size.  Returns (prefill_out, decode_out)."""
+    _cuda_contig("k_cache", k_cache)
+    _cuda_contig("v_cache", v_cache, k_cache.dtype)
+    st = MixedStep()
+    st.scale = float(scale)
+    keep = []
+    pout = dout = None
+    hq = None
+    if prefill:
+        for n in ("k_new", "v_new", "q"):
+            _cuda_contig("prefill " + n, prefill[n], k_cache.dtype)
+        for n in ("slots", "cu_q", "cu_k", "table"):
+            _cuda_contig("prefill " + n, prefill[n], torch.int32)
+        pout = prefill.get("out")
+        if pout is None:
+            pout = torch.empty_like(prefill["q"])
+        hq = prefill["q"].shape[1]
+        st.prefill_k_new, st.prefill_v_new = prefill["k_new"].data_ptr(), prefill["v_new"].data_ptr()
+        st.prefill_slots = prefill["slots"].data_ptr()
+        st.prefill_new_tokens = prefill["slots"].numel()
+        st.prefill_q, st.prefill_out = prefill["q"].data_ptr(), pout.data_ptr()
+        st.cu_seqlens_q, st.cu_seqlens_k = prefill["cu_q"].data_ptr(), prefill["cu_k"].data_ptr()
+        st.prefill_batch = prefill["cu_q"].numel() - 1
+        st.max_seqlen_q, st.max_seqlen_k = int(prefill["max_q"]), int(prefill["max_k"])
+        st.prefill_table = prefill["table"].data_ptr()
+        st.prefill_max_blocks = prefill["table"].shape[1]
+    if decode:
+        for n in ("q", "k_new", "v_new"):
+            _cuda_contig("decode " + n, decode[n], k_cache.dtype)
+        for n in ("table", "seqlens"):
+            _cuda_contig("decode " + n, decode[n], torch.int32)
+        dout = decode.get("out")
+        if dout is None:
+            dout = torch.empty_like(decode["q"])
+        hq = decode["q"].shape[1]
+        st.decode_q, st.decode_out = decode["q"].data_ptr(), dout.data_ptr()
+        st.decode_k_new, st.decode_v_new = decode["k_new"].data_ptr(), decode["v_new"].data_ptr()
+        st.decode_table = decode["table"].data_ptr()
+        st.decode_max_blocks = decode["table"].shape[1]
+        st.decode_seqlens = decode["seqlens"].data_ptr()
+        st.decode_batch = decode["q"].shape[0]
+        if decode.get("group_cu") is not None:
+            _cuda_contig("group_cu", decode["group_cu"], torch.int32)
+            _cuda_contig("group_prefix_len", decode["group_prefix_len"], torch.int32)
+            st.group_cu = decode["group_cu"].data_ptr()
+            st.group_prefix_len = decode["group_prefix_len"].data_ptr()
+            st.n_groups = decode["group_cu"].numel() - 1
+            st.max_group_size = int(decode["max_group_size"])
+    g = geom_of(k_cache, hq if hq is not None else k_cache.shape[2])
+    lib = load_library()
+    with torch.cuda.device(k_cache.device):
+        need = int(lib.paged_mixed_step_workspace_size(st.decode_batch, ctypes.byref(g)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=k_cache.device)
+    with torch.cuda.device(k_cache.device):
+        rc = lib.paged_mixed_step(ctypes.byref(st), _ptr(k_cache), _ptr(v_cache), _ptr(workspace),
+                                  workspace.numel(), ctypes.byref(g), _stream(k_cache))
+    _check("paged_mixed_step", rc)
+    return pout, dout

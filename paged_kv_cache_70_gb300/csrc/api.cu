@@ -284,6 +284,108 @@ int paged_decode_shared_prefix(const void* q, const void* k_cache, const void* v
                                           geom->dtype, dev.err, stream, &sp));
 }
 
+size_t paged_mixed_step_workspace_size(int32_t decode_batch, const pkv_geom* geom) {
+    if (check_geom(geom) != PKV_OK || decode_batch < 0) return 0;
+    if (decode_batch == 0) return 256;
+    return paged_decode_shared_prefix_workspace_size(decode_batch, geom);
+}
+
+int paged_mixed_step(const pkv_mixed_step* s, void* k_cache, void* v_cache, void* workspace,
+                     size_t workspace_bytes, const pkv_geom* geom, cudaStream_t stream) {
+    int st = check_geom(geom);
+    if (st != PKV_OK) return st;
+    if (!s || !k_cache || !v_cache) return PKV_ERR_INVALID;
+    if (s->prefill_new_tokens < 0 || s->prefill_batch < 0 || s->decode_batch < 0 ||
+        s->n_groups < 0)
+        return PKV_ERR_INVALID;
+    const bool pf = s->prefill_batch > 0 && s->max_seqlen_q > 0;
+    const bool dec = s->decode_batch > 0;
+    const bool grp = dec && s->n_groups > 0;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return PKV_ERR_INVALID;
+    if ((pf || grp) && (geom->dtype != PKV_BF16 || geom->head_dim != 128))
+        return PKV_ERR_UNSUPPORTED;
+    if (s->prefill_new_tokens > 0 &&
+        (!s->prefill_k_new || !s->prefill_v_new || !s->prefill_slots))
+        return PKV_ERR_INVALID;
+    if (pf && (!s->prefill_q || !s->cu_seqlens_q || !s->cu_seqlens_k || !s->prefill_table ||
+               !s->prefill_out || !aligned(s->prefill_q, 16) || !aligned(s->prefill_out, 16)))
+        return PKV_ERR_INVALID;
+    if (dec && (!s->decode_q || !s->decode_k_new || !s->decode_v_new || !s->decode_table ||
+                !s->decode_seqlens || !s->decode_out || !aligned(s->decode_q, 16) ||
+                !aligned(s->decode_out, 16) || !aligned(s->decode_k_new, 16) ||
+                !aligned(s->decode_v_new, 16)))
+        return PKV_ERR_INVALID;
+    if (grp && (!s->group_cu || !s->group_prefix_len || s->max_group_size <= 0))
+        return PKV_ERR_INVALID;
+    DeviceInfo dev;
+    if (pkv::current_device_info(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    pkv::DecodePlan plan;
+    if (dec) {
+        if (!pkv::plan_decode(dev, s->decode_batch, geom->num_heads, geom->num_kv_heads,
+                              geom->head_dim, geom->block_size, elt_size(geom->dtype), &plan))
+            return PKV_ERR_UNSUPPORTED;
+        const size_t need = plan.ws_bytes + (grp ? shared_prefix_extra_bytes(s->decode_batch, geom)
+                                                 : 0);
+        if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+            return PKV_ERR_WORKSPACE;
+    }
+    const int64_t kv_dim = (int64_t)geom->num_kv_heads * geom->head_dim;
+    bool chained = false;  // a kernel this call launched precedes the next one
+    // 1. the prefill requests' new rows
+    if (s->prefill_new_tokens > 0) {
+        cudaError_t e = pkv::launch_kv_write(s->prefill_k_new, s->prefill_v_new, geom->dtype,
+                                             s->prefill_slots, s->prefill_new_tokens, k_cache,
+                                             v_cache, geom->dtype, kv_dim,
+                                             geom->num_blocks * geom->block_size, dev.err, stream);
+        if (e != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    // 2. causal varlen prefill
+    if (pf) {
+        cudaError_t e = pkv::launch_prefill(
+            dev, s->prefill_q, k_cache, v_cache, s->cu_seqlens_q, s->cu_seqlens_k,
+            s->prefill_batch, s->max_seqlen_q, s->max_seqlen_k, s->prefill_table,
+            s->prefill_max_blocks, 1, s->scale, s->prefill_out, nullptr, geom->num_heads,
+            geom->num_kv_heads, geom->head_dim, geom->block_size, geom->num_blocks, dev.err,
+            stream);
+        if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+        if (e != cudaSuccess) return PKV_ERR_CUDA;
+        chained = true;
+    }
+    if (!dec) return PKV_OK;
+    // 3. decode with the append (shared prefixes first when grouped)
+    pkv::SharedPrefix sp{};
+    if (grp) {
+        unsigned char* x_out = static_cast<unsigned char*>(workspace) + plan.ws_bytes;
+        float* x_lse = reinterpret_cast<float*>(
+            x_out + align256((size_t)kMaxPrefixChunks * s->decode_batch * geom->num_heads *
+                             geom->head_dim * 2));
+        const int units = s->n_groups * (geom->num_heads / geom->num_kv_heads % 2 == 0
+                                             ? geom->num_heads / 2 : geom->num_heads) *
+                          ((s->max_group_size + 127) / 128);
+        int kchunks = units > 0 ? dev.num_sms / units : 1;
+        kchunks = kchunks < 1 ? 1 : (kchunks > kMaxPrefixChunks ? kMaxPrefixChunks : kchunks);
+        pkv::PrefillExtra ex{s->group_prefix_len, s->group_cu, x_lse, kchunks, s->decode_batch,
+                             chained};
+        cudaError_t e = pkv::launch_prefill(
+            dev, s->decode_q, k_cache, v_cache, s->group_cu, s->group_cu, s->n_groups,
+            s->max_group_size, 0, s->decode_table, s->decode_max_blocks, 0, s->scale, x_out,
+            nullptr, geom->num_heads, geom->num_kv_heads, geom->head_dim, geom->block_size,
+            geom->num_blocks, dev.err, stream, &ex);
+        if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+        if (e != cudaSuccess) return PKV_ERR_CUDA;
+        sp = pkv::SharedPrefix{s->group_cu, s->group_prefix_len, s->n_groups, x_out, x_lse,
+                               kchunks};
+        chained = true;
+    }
+    pkv::DecodeAppend ap{s->decode_k_new, s->decode_v_new, k_cache, v_cache};
+    pkv::DecodeChain ch{chained};
+    return cuda_status(pkv::launch_decode(
+        plan, s->decode_q, k_cache, v_cache, s->decode_table, s->decode_max_blocks,
+        s->decode_seqlens, s->decode_batch, s->scale, s->decode_out, workspace, geom->num_heads,
+        geom->num_kv_heads, geom->head_dim, geom->block_size, geom->num_blocks, geom->dtype,
+        dev.err, stream, grp ? &sp : nullptr, &ap, &ch));
+}
+
 int paged_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst,
                       int32_t n_pairs, const pkv_geom* geom, cudaStream_t stream) {
     int st = check_geom(geom);

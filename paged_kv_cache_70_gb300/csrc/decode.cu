@@ -71,6 +71,7 @@ struct DecodeArgs {
     int32_t rows;  // R
     int32_t stages;
     int32_t n_groups;
+    int32_t wait_prior;  // this grid completes only after the previous kernel has
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -248,6 +249,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
 
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
+        // an otherwise idle lane holds the grid open until the kernel launched
+        // before it has completed (the combine waits for this grid)
+        if (a.wait_prior && lane == 31 && blockIdx.x == 0 && blockIdx.y == 0)
+            asm volatile("griddepcontrol.wait;" ::: "memory");
         if (lane != 0) return;
         const uint64_t pol = l2_evict_first_policy();
         int b = seq_of_tile(tstart, a.batch, t0);
@@ -696,14 +701,28 @@ bool plan_decode(const DeviceInfo& dev, int32_t batch, int hq, int hkv, int d, i
 
 template <int D, bool BF16, int G>
 static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a,
-                                   const CombineArgs& c, cudaStream_t stream) {
+                                   const CombineArgs& c, bool pdl_split, cudaStream_t stream) {
     auto kern = decode_split_kernel<D, BF16, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)plan.smem_bytes);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.ctas, plan.head_groups);
-    kern<<<grid, kDecodeThreads, plan.smem_bytes, stream>>>(a);
-    e = cudaGetLastError();
+    if (pdl_split) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kDecodeThreads);
+        cfg.dynamicSmemBytes = plan.smem_bytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, a);
+    } else {
+        kern<<<grid, kDecodeThreads, plan.smem_bytes, stream>>>(a);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     // combine: programmatic dependent of the split kernel
     cudaLaunchConfig_t cfg = {};
@@ -725,9 +744,11 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
                           const int32_t* cache_seqlens, int32_t batch, float scale, void* out,
                           void* workspace, int hq, int hkv, int d, int block_size,
                           int64_t num_blocks, int dtype, unsigned int* err, cudaStream_t stream,
-                          const SharedPrefix* sp, const DecodeAppend* ap) {
+                          const SharedPrefix* sp, const DecodeAppend* ap,
+                          const DecodeChain* chain) {
     if (batch == 0) return cudaSuccess;
     DecodeArgs a;
+    a.wait_prior = (chain && chain->pdl_split) ? 1 : 0;
     a.group_cu = sp ? sp->group_cu : nullptr;
     a.group_plen = sp ? sp->group_plen : nullptr;
     a.n_groups = sp ? sp->n_groups : 0;
@@ -786,7 +807,8 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
     c.qscale = a.qscale;
     c.err = err;
 #define PKV_DECODE_CASE(DD, BB, GG) \
-    if (d == DD && bf == BB && G == GG) return launch_decode_t<DD, BB, GG>(plan, a, c, stream);
+    if (d == DD && bf == BB && G == GG) \
+        return launch_decode_t<DD, BB, GG>(plan, a, c, a.wait_prior != 0, stream);
     PKV_DECODE_CASE(128, true, 1) PKV_DECODE_CASE(128, true, 2) PKV_DECODE_CASE(128, true, 4)
     PKV_DECODE_CASE(128, false, 1) PKV_DECODE_CASE(128, false, 2) PKV_DECODE_CASE(128, false, 4)
     PKV_DECODE_CASE(64, true, 1) PKV_DECODE_CASE(64, true, 2) PKV_DECODE_CASE(64, true, 4)

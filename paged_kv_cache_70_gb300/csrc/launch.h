@@ -69,6 +69,13 @@ struct DecodeAppend {
     void* v_cache;
 };
 
+// Launch options of the decode pair: the split kernel as a programmatic
+// dependent of the previous kernel (which it does not read), completing only
+// after that kernel has (so the combine, which waits for the split, sees it).
+struct DecodeChain {
+    bool pdl_split;
+};
+
 // Returns false when the geometry is not supported.
 bool plan_decode(const DeviceInfo& dev, int32_t batch, int hq, int hkv, int d, int block_size,
                  int elt, DecodePlan* plan);
@@ -79,7 +86,8 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
                           void* workspace, int hq, int hkv, int d, int block_size,
                           int64_t num_blocks, int dtype, unsigned int* err, cudaStream_t stream,
                           const SharedPrefix* shared = nullptr,
-                          const DecodeAppend* append = nullptr);
+                          const DecodeAppend* append = nullptr,
+                          const DecodeChain* chain = nullptr);
 
 // ---- prefill ----------------------------------------------------------------
 size_t prefill_workspace_bytes(int32_t batch, int32_t max_seqlen_q, int hq);
@@ -91,6 +99,7 @@ struct PrefillExtra {
     float* lse;
     int32_t kchunks;     // key chunks per request (non-causal), 1 = none
     int32_t chunk_rows;  // output rows of one chunk (kchunks > 1)
+    bool pdl;            // launch as a programmatic dependent of the previous kernel
 };
 
 cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_cache,

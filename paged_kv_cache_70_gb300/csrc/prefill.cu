@@ -260,6 +260,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     uint64_t* q_ready = o_ready + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
 
+    // a kernel launched after this one as its programmatic dependent may start
+    // now (it orders itself with griddepcontrol.wait where it needs to)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = kExt ? (int)blockIdx.z / a.kchunks : (int)blockIdx.z;
     const int kchunk = kExt ? (int)blockIdx.z % a.kchunks : 0;
@@ -769,6 +772,21 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(a.tiles_q, a.pair_heads ? (hq + 1) / 2 : hq, batch * a.kchunks);
+    if (ex && ex->pdl) {
+        // start as a programmatic dependent of the previous kernel (it needs
+        // none of that kernel's results)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, mq, mo, mk, mv, a);
+    }
     kern<<<grid, kThreads, kSmemBytes, stream>>>(mq, mo, mk, mv, a);
     return cudaGetLastError();
 }
