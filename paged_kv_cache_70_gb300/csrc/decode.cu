@@ -31,7 +31,20 @@
 //    Exponentials are base 2 on log2-scaled scores, which is the same merge.
 //  * The combine kernel (one warp per sequence and head) is launched as a
 //    programmatic dependent of the split kernel, so its launch overlaps the
-//    split kernel's tail.
+//    split kernel's tail.  Besides the split partials it can merge
+//      - shared-prefix partials: groups of consecutive sequences that hold a
+//        common prefix in the same blocks get that prefix's attention from
+//        the tensor-core kernel (once per group, in key chunks; normalised
+//        output and log2-sum-exp), and the split kernel then starts each
+//        sequence's tile list after its group's prefix;
+//      - the appended token ("Sayfalı dikkat" decode path, new k/v written
+//        into the cache by the kvcache call): its score is taken from k_new,
+//        it joins the merge as a one-key state, and the combine writes the
+//        new K/V row through the block table (the split kernel, which read
+//        only the keys before it, has completed).
+//  * As a programmatic dependent of an unrelated kernel (the mixed step), the
+//    split kernel holds its grid open with one otherwise idle lane waiting on
+//    griddepcontrol.wait, so that its completion implies that kernel's.
 //  * Safety.  Block ids and lengths are range-checked before any address is
 //    formed; every mbarrier wait is time-limited (PKV_FLAG_TIMEOUT).
 #include <float.h>

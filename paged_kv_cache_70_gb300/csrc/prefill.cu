@@ -41,6 +41,17 @@
 //   The epilogue divides O by l and stages the bf16 rows in the (now dead)
 //   Q tile; a full tile leaves by two TMA boxes, a ragged one with coalesced
 //   16-byte writes of its valid rows.
+// Also served by the same kernel:
+//   - packed K/V (no block table; flash-attn's varlen call without a prefix
+//     cache): request r's keys are rows cu_k[r] .. of [rows, Hkv, d] arrays,
+//     one 128-row box per K/V tile;
+//   - prefill_tc_kernel<true>, the shared-prefix pass of grouped decode: the
+//     key count and block-table row of each request come from per-request
+//     arrays, the keys may be cut into chunks (each a separate work item with
+//     its own output block), and each row's log2-sum-exp m + log2(l) is
+//     written for the merge with the rest of the keys.
+// The kernel lets programmatic dependents start at once (it writes nothing
+// they read).
 // Every mbarrier wait is time-limited; a timeout sets PKV_FLAG_TIMEOUT and the
 // CTA drains its copies and frees TMEM before returning.
 #include <cuda.h>
