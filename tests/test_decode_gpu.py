@@ -161,3 +161,26 @@ def test_workspace_and_support_errors():
     with pytest.raises(pkv.PagedKVError) as e:
         pkv.paged_decode(q, kc, kc, dev.decode_table, dev.cache_seqlens)
     assert e.value.status == -2
+
+
+def test_split_points_vary_with_the_batch():
+    """One 20000-key sequence decoded with the other sequences of the batch
+    empty (its keys spread over every CTA) and non-empty (its keys cut into
+    other shares and merged from other partial states): within tolerance of
+    the oracle each time, and of each other."""
+    others = [40000] * 3 + [5, 17, 3000] * 6
+    lens = [20000] + others
+    step = W.make_step(name="split", dtype="bf16", hq=16, hkv=8, d=128, block_size=64,
+                       decode_lens=[L - 1 for L in lens], seed=77)
+    want = oracle.decode(step.q_decode[:1], step.k_cache, step.v_cache, step.decode_table[:1],
+                         np.array([20000], np.int32), step.scale)
+    dev = DevStep(step)
+    outs = []
+    for variant in (np.zeros(len(others)), np.array(others), np.array(others[::-1]) // 3):
+        dev.cache_seqlens = to_dev(np.concatenate([[20000], variant]).astype(np.int32))
+        out = widen(dev.decode())
+        torch.cuda.synchronize()
+        assert_close(out[:1], want, "bf16", "sequence 0")
+        outs.append(out[0])
+    assert_close(outs[1], outs[0].astype(np.float64), "bf16", "split vs alone")
+    assert_close(outs[2], outs[0].astype(np.float64), "bf16", "split vs alone")
