@@ -595,16 +595,35 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const CombineArgs c
         M = fmaxf(M, s_new);
     }
     if (M != -INFINITY) {
-#pragma unroll 4
-        for (int cc = c0; cc <= c1; ++cc) {
-            const int64_t slot = (int64_t)cc + b;
-            const float2 ml = *reinterpret_cast<const float2*>(c.part_ml + (slot * hq + h) * 2);
-            const float wgt = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
-            lt += ml.y * wgt;
-            const float* src = c.part_o + (slot * hq + h) * D + lane * DPL;
+        // pieces in rounds of 32: lane i reads piece i's (m, l), so a round
+        // costs one dependent load; each piece's weight then reaches every
+        // lane by shuffle and the o rows stream in independent loads
+        float lp = 0.f;  // this lane's share of the pieces' l
+        for (int base = c0; base <= c1; base += 32) {
+            const int n = min(32, c1 - base + 1);
+            float wl = 0.f;
+            if (lane < n) {
+                const float2 ml = *reinterpret_cast<const float2*>(
+                    c.part_ml + ((int64_t)(base + lane + b) * hq + h) * 2);
+                wl = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
+                lp += ml.y * wl;
+            }
+#pragma unroll 8
+            for (int i = 0; i < n; ++i) {
+                const float wgt = __shfl_sync(0xffffffffu, wl, i);
+                const float* src = c.part_o + ((int64_t)(base + i + b) * hq + h) * D + lane * DPL;
+                if constexpr (DPL == 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(src);
+                    acc[0] += v.x * wgt; acc[1] += v.y * wgt; acc[2] += v.z * wgt; acc[3] += v.w * wgt;
+                } else {
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) acc[e] += src[e] * wgt;
+                    for (int e = 0; e < DPL; ++e) acc[e] += src[e] * wgt;
+                }
+            }
         }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) lp += __shfl_xor_sync(0xffffffffu, lp, off);
+        lt += lp;
         for (int x = 0; x < c.x_chunks; ++x) {
             const float mx = c.x_lse[x * xstride + (int64_t)b * hq + h];
             if (mx == -INFINITY) continue;
