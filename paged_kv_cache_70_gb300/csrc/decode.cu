@@ -85,6 +85,7 @@ struct DecodeArgs {
     int32_t stages;
     int32_t n_groups;
     int32_t wait_prior;  // this grid completes only after the previous kernel has
+    int32_t wait_inputs;  // wait for the previous kernel before reading any input
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -242,6 +243,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
         }
         fence_barrier_init();
     }
+    // launched as a programmatic dependent: the lengths, table and K/V may come
+    // from the kernel before (the new token's write)
+    if (a.wait_inputs) asm volatile("griddepcontrol.wait;" ::: "memory");
     scan_tiles(a, tstart);
     __syncthreads();
 
@@ -738,23 +742,9 @@ static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a,
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)plan.smem_bytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(plan.ctas, plan.head_groups);
-    if (pdl_split) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = grid;
-        cfg.blockDim = dim3(kDecodeThreads);
-        cfg.dynamicSmemBytes = plan.smem_bytes;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, kern, a);
-    } else {
-        kern<<<grid, kDecodeThreads, plan.smem_bytes, stream>>>(a);
-        e = cudaGetLastError();
-    }
+    (void)pdl_split;
+    e = launch_dependent(kern, dim3(plan.ctas, plan.head_groups), dim3(kDecodeThreads),
+                         plan.smem_bytes, stream, a);
     if (e != cudaSuccess) return e;
     // combine: programmatic dependent of the split kernel
     cudaLaunchConfig_t cfg = {};
@@ -781,6 +771,7 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
     if (batch == 0) return cudaSuccess;
     DecodeArgs a;
     a.wait_prior = (chain && chain->pdl_split) ? 1 : 0;
+    a.wait_inputs = a.wait_prior ? 0 : 1;
     a.group_cu = sp ? sp->group_cu : nullptr;
     a.group_plen = sp ? sp->group_plen : nullptr;
     a.n_groups = sp ? sp->n_groups : 0;

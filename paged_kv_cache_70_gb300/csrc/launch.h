@@ -9,6 +9,33 @@
 
 namespace pkv {
 
+// Launch `kern` as a programmatic dependent of the kernel before it on
+// `stream`: it may be scheduled while that kernel finishes, and must execute
+// griddepcontrol.wait before it touches memory that kernel (or any earlier
+// work) may produce.  After any other kind of predecessor this is an ordinary
+// stream-ordered launch.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
+// First statement of such kernels: let the next kernel launch early, then wait
+// for this one's inputs.
+#define PKV_DEPENDENT_PROLOGUE()                                  \
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); \
+    asm volatile("griddepcontrol.wait;" ::: "memory")
+
 struct DeviceInfo {
     int device;
     int num_sms;

@@ -22,6 +22,7 @@ __global__ void build_slot_mapping_kernel(const int32_t* __restrict__ table, int
                                           const int32_t* __restrict__ token_pos,
                                           int64_t num_tokens, int32_t block_size,
                                           int32_t* __restrict__ slots, unsigned int* err) {
+    PKV_DEPENDENT_PROLOGUE();
     int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (n >= num_tokens) return;
     const int32_t s = token_seq[n];
@@ -52,10 +53,9 @@ cudaError_t launch_build_slot_mapping(const int32_t* block_table, int32_t max_bl
     if (num_tokens == 0) return cudaSuccess;
     const int threads = 256;
     const int64_t blocks = (num_tokens + threads - 1) / threads;
-    build_slot_mapping_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
-        block_table, max_blocks, num_seqs, token_seq, token_pos, num_tokens, block_size,
-        slot_mapping, err);
-    return cudaGetLastError();
+    return launch_dependent(build_slot_mapping_kernel, dim3((unsigned)blocks), dim3(threads), 0,
+                            stream, block_table, max_blocks, num_seqs, token_seq, token_pos,
+                            num_tokens, block_size, slot_mapping, err);
 }
 
 // ---------------------------------------------------------------------------
@@ -69,6 +69,7 @@ kv_write_copy_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                      const int32_t* __restrict__ slots, int64_t num_tokens,
                      uint4* __restrict__ kc, uint4* __restrict__ vc, int64_t vec_per_row,
                      int64_t num_slots, unsigned int* err) {
+    PKV_DEPENDENT_PROLOGUE();
     const int lane = threadIdx.x & 31;
     const int64_t n = (int64_t)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
     if (n >= num_tokens) return;
@@ -96,6 +97,7 @@ kv_write_f32_to_bf16_kernel(const float4* __restrict__ k, const float4* __restri
                             const int32_t* __restrict__ slots, int64_t num_tokens,
                             uint4* __restrict__ kc, uint4* __restrict__ vc, int64_t groups8,
                             int64_t num_slots, unsigned int* err) {
+    PKV_DEPENDENT_PROLOGUE();
     const int lane = threadIdx.x & 31;
     const int64_t n = (int64_t)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
     if (n >= num_tokens) return;
@@ -123,6 +125,7 @@ __global__ void kv_write_scalar_kernel(const void* __restrict__ k, const void* _
                                        int64_t num_tokens, void* __restrict__ kc,
                                        void* __restrict__ vc, int cache_dtype, int64_t kv_dim,
                                        int64_t num_slots, unsigned int* err) {
+    PKV_DEPENDENT_PROLOGUE();
     const int lane = threadIdx.x & 31;
     const int64_t n = (int64_t)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
     if (n >= num_tokens) return;
@@ -168,19 +171,21 @@ cudaError_t launch_kv_write(const void* k, const void* v, int src_dtype, const i
                              aligned16(v_cache);
     const int src_elt = src_dtype == PKV_F32 ? 4 : 2;
     if (all_aligned && src_dtype == cache_dtype && (kv_dim * src_elt) % 16 == 0) {
-        kv_write_copy_kernel<<<(unsigned)grid, threads, 0, stream>>>(
-            static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens,
-            static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), kv_dim * src_elt / 16,
-            num_slots, err);
+        return launch_dependent(kv_write_copy_kernel, dim3((unsigned)grid), dim3(threads), 0,
+                                stream, static_cast<const uint4*>(k),
+                                static_cast<const uint4*>(v), slots, num_tokens,
+                                static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                                kv_dim * src_elt / 16, num_slots, err);
     } else if (all_aligned && src_dtype == PKV_F32 && cache_dtype == PKV_BF16 && kv_dim % 8 == 0) {
-        kv_write_f32_to_bf16_kernel<<<(unsigned)grid, threads, 0, stream>>>(
-            static_cast<const float4*>(k), static_cast<const float4*>(v), slots, num_tokens,
-            static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), kv_dim / 8, num_slots,
-            err);
+        return launch_dependent(kv_write_f32_to_bf16_kernel, dim3((unsigned)grid), dim3(threads),
+                                0, stream, static_cast<const float4*>(k),
+                                static_cast<const float4*>(v), slots, num_tokens,
+                                static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                                kv_dim / 8, num_slots, err);
     } else {
-        kv_write_scalar_kernel<<<(unsigned)grid, threads, 0, stream>>>(
-            k, v, src_dtype, slots, num_tokens, k_cache, v_cache, cache_dtype, kv_dim, num_slots,
-            err);
+        return launch_dependent(kv_write_scalar_kernel, dim3((unsigned)grid), dim3(threads), 0,
+                                stream, k, v, src_dtype, slots, num_tokens, k_cache, v_cache,
+                                cache_dtype, kv_dim, num_slots, err);
     }
     return cudaGetLastError();
 }
@@ -197,6 +202,7 @@ __global__ void __launch_bounds__(kCopyThreads)
 copy_blocks_kernel(uint4* __restrict__ kc, uint4* __restrict__ vc,
                    const int32_t* __restrict__ src, const int32_t* __restrict__ dst,
                    int64_t vec_per_block, int64_t num_blocks, unsigned int* err) {
+    PKV_DEPENDENT_PROLOGUE();
     const int32_t s = __ldg(src + blockIdx.y), d = __ldg(dst + blockIdx.y);
     if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
         if (threadIdx.x == 0 && blockIdx.x == 0) flag_error(err, PKV_FLAG_BAD_BLOCK);
@@ -232,6 +238,7 @@ __global__ void copy_blocks_bytes_kernel(unsigned char* __restrict__ kc,
                                          const int32_t* __restrict__ src,
                                          const int32_t* __restrict__ dst, int64_t block_bytes,
                                          int64_t num_blocks, unsigned int* err) {
+    PKV_DEPENDENT_PROLOGUE();
     const int32_t s = src[blockIdx.y], d = dst[blockIdx.y];
     if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
         if (threadIdx.x == 0 && blockIdx.x == 0) flag_error(err, PKV_FLAG_BAD_BLOCK);
@@ -252,15 +259,16 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src,
         const int64_t vec = block_bytes / 16;
         const int64_t per_cta = (int64_t)kCopyThreads * kCopyUnroll;
         const dim3 grid((unsigned)((vec + per_cta - 1) / per_cta), (unsigned)n_pairs);
-        copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(
-            static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), src, dst, vec, num_blocks,
-            err);
+        return launch_dependent(copy_blocks_kernel, grid, dim3(kCopyThreads), 0, stream,
+                                static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), src,
+                                dst, vec, num_blocks, err);
     } else {
         const dim3 grid((unsigned)std::min<int64_t>((block_bytes + 255) / 256, 64),
                         (unsigned)n_pairs);
-        copy_blocks_bytes_kernel<<<grid, 256, 0, stream>>>(
-            static_cast<unsigned char*>(k_cache), static_cast<unsigned char*>(v_cache), src, dst,
-            block_bytes, num_blocks, err);
+        return launch_dependent(copy_blocks_bytes_kernel, grid, dim3(256), 0, stream,
+                                static_cast<unsigned char*>(k_cache),
+                                static_cast<unsigned char*>(v_cache), src, dst, block_bytes,
+                                num_blocks, err);
     }
     return cudaGetLastError();
 }
