@@ -84,3 +84,22 @@ def test_position_past_the_table_is_flagged_and_not_written():
                                       before[:2].astype(np.int32), step.block_size)
     kc0.reshape(-1, *kc0.shape[2:])[slots] = step.new_k[:2]
     assert np.array_equal(kc, kc0)
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,d,B", [("f32", 8, 2, 64, 1), ("bf16", 32, 8, 128, 48),
+                                              ("f32", 16, 16, 128, 16)])
+def test_append_shapes(dtype, hq, hkv, d, B):
+    """Other dtypes, head sizes, GQA groups and block sizes (B = 1, B not a
+    power of two, Hkv above the decode kernel's warp count)."""
+    lens = [0, 1, B, 3 * B + 1, 700]
+    step = W.make_step(name="app", dtype=dtype, hq=hq, hkv=hkv, d=d, block_size=B,
+                       decode_lens=lens, seed=sum(lens) + hq + d)
+    dev = DevStep(step)
+    out = pkv.paged_decode_append(dev.q_decode, dev.new_k, dev.new_v, dev.k_cache, dev.v_cache,
+                                  dev.decode_table, to_dev(np.array(lens, np.int32)), step.scale)
+    torch.cuda.synchronize()
+    _, kc, vc = oracle_write(step)
+    assert np.array_equal(to_host(dev.k_cache), kc) and np.array_equal(to_host(dev.v_cache), vc)
+    want = oracle.decode(step.q_decode, kc, vc, step.decode_table, step.cache_seqlens, step.scale)
+    assert_close(widen(out), want, dtype, f"{dtype} {hq}/{hkv} d{d} B{B}")
+    assert pkv.paged_error_flags() == 0

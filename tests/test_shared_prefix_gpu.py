@@ -102,3 +102,19 @@ def test_prefix_not_a_whole_block_is_flagged():
                                    to_dev(lens), to_dev(gcu), to_dev(plen), 4)
     torch.cuda.synchronize()
     assert pkv.paged_error_flags() & pkv.PKV_FLAG_BAD_LENGTH
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (32, 8), (8, 2)])
+def test_group_sizes(hq, hkv):
+    """GQA group 1 (the prefix pass takes one head per work item), 4, and a
+    KV-head count below the decode kernel's warp count."""
+    rng = np.random.default_rng(hq * 7 + hkv)
+    q, kc, vc, table, lens, gcu, plen = build_groups(rng, [6, 9], [256, 512], 200, 32,
+                                                     hq=hq, hkv=hkv)
+    scale = 1 / math.sqrt(128)
+    out = pkv.paged_decode_shared_prefix(to_dev(q), to_dev(kc), to_dev(vc), to_dev(table),
+                                         to_dev(lens), to_dev(gcu), to_dev(plen), 9, scale)
+    torch.cuda.synchronize()
+    want = oracle.decode(q, kc, vc, table, lens, scale)
+    assert_close(widen(out), want, "bf16", f"{hq}/{hkv}")
+    assert pkv.paged_error_flags() == 0
