@@ -277,9 +277,12 @@ def time_steps(dev: DeviceStep, steps: int, warmup: int, flush: torch.Tensor | N
     return total, float(np.mean(attend)), float(np.median(attend))
 
 
-def time_e2e(step, dev: DeviceStep, steps: int, warmup: int, world: int):
-    """The same pass through the public API from pinned HOST buffers: every
-    step copies its inputs host->device and reads the output back."""
+def time_e2e(step, dev: DeviceStep, steps: int, warmup: int, world: int, keep_out=None):
+    """The same pass through the public API from pinned HOST buffers.  Every
+    step copies its inputs host->device and reads the output back.  The step's
+    inputs sit in one pinned host buffer (each at a 256-byte aligned offset),
+    as a serving engine stages a step's inputs, and go over in one transfer
+    into one device buffer whose slices are the tensors the calls read."""
     s = step
     host_in = {"new_k": pinned(s.new_k), "new_v": pinned(s.new_v),
                "token_seq": pinned(s.token_seq), "token_pos": pinned(s.token_pos),
@@ -288,39 +291,78 @@ def time_e2e(step, dev: DeviceStep, steps: int, warmup: int, world: int):
         host_in.update(q=pinned(s.q_decode), seqlens=pinned(s.cache_seqlens))
     else:
         host_in.update(q=pinned(s.q_prefill), cu_q=pinned(s.cu_q), cu_k=pinned(s.cu_k))
+    offs, total = {}, 0
+    for name, t in host_in.items():
+        offs[name] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(total, dtype=torch.uint8, device="cuda")
+    views = {}
+    for name, t in host_in.items():
+        nb = t.numel() * t.element_size()
+        host_buf[offs[name]:offs[name] + nb].copy_(t.reshape(-1).view(torch.uint8))
+        views[name] = dev_buf[offs[name]:offs[name] + nb].view(t.dtype).view(t.shape)
     host_out = torch.empty(dev.out.shape, dtype=dev.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d = total
     d2h = host_out.numel() * host_out.element_size()
 
+    # the calls read the slices of the staged buffer (restored afterwards)
+    saved = dict(vars(dev))
+    dev.new_k, dev.new_v = views["new_k"], views["new_v"]
+    dev.token_seq, dev.token_pos = views["token_seq"], views["token_pos"]
+    dev.table, dev.q = views["table"], views["q"]
+    if s.n_decode:
+        dev.seqlens = views["seqlens"]
+        dev.dtable = views["table"][: s.n_decode]
+    else:
+        dev.cu_q, dev.cu_k = views["cu_q"], views["cu_k"]
+        dev.ptable = views["table"][s.n_decode:]
+
+    # Two copy streams: a step's upload may run while the previous step's
+    # output is read back (the link carries both directions at once), but the
+    # step's kernels start only when its inputs have arrived and the previous
+    # output has left the device, and the upload starts only once the previous
+    # step's kernels are done with the inputs.
+    cur = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in, ev_done, ev_out = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+    ev_done.record(cur)
+    ev_out.record(cur)
+
     def one():
-        dev.new_k.copy_(host_in["new_k"], non_blocking=True)
-        dev.new_v.copy_(host_in["new_v"], non_blocking=True)
-        dev.token_seq.copy_(host_in["token_seq"], non_blocking=True)
-        dev.token_pos.copy_(host_in["token_pos"], non_blocking=True)
-        dev.table.copy_(host_in["table"], non_blocking=True)
-        dev.q.copy_(host_in["q"], non_blocking=True)
-        if s.n_decode:
-            dev.seqlens.copy_(host_in["seqlens"], non_blocking=True)
-            dev.dtable.copy_(dev.table[: s.n_decode])
-        else:
-            dev.cu_q.copy_(host_in["cu_q"], non_blocking=True)
-            dev.cu_k.copy_(host_in["cu_k"], non_blocking=True)
-            dev.ptable.copy_(dev.table[s.n_decode:])
+        up.wait_event(ev_done)
+        with torch.cuda.stream(up):
+            dev_buf.copy_(host_buf, non_blocking=True)
+        ev_in.record(up)
+        cur.wait_event(ev_in)
+        cur.wait_event(ev_out)
         dev.write()
         dev.attend()
-        host_out.copy_(dev.out, non_blocking=True)
+        ev_done.record(cur)
+        down.wait_event(ev_done)
+        with torch.cuda.stream(down):
+            host_out.copy_(dev.out, non_blocking=True)
+        ev_out.record(down)
 
-    for _ in range(warmup):
-        one()
-    torch.cuda.synchronize()
-    barrier(world)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(steps):
-        one()
-    t1.record()
-    torch.cuda.synchronize()
+    try:
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(cur)
+        ev_done.record(cur)
+        ev_out.record(cur)
+        for _ in range(steps):
+            one()
+        cur.wait_event(ev_out)
+        t1.record(cur)
+        torch.cuda.synchronize()
+    finally:
+        vars(dev).update(saved)
+    if keep_out is not None:
+        keep_out.append(host_out.clone())
     ms = max_over_ranks(t0.elapsed_time(t1), world) / steps
     return ms, h2d, d2h
 
