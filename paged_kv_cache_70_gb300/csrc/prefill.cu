@@ -361,8 +361,89 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
       if (warp == 8) {
         // ------------------------------ TMA producer ------------------------------
-        if (lane == 0) {
+        if (a.piece < BN) {
+            // Several page pieces per tile.  The whole warp: lane p finds the
+            // pool row of piece p of a tile, its block-table entry read one
+            // tile ahead so that the lookups overlap the previous tile's
+            // copies; lane 0 waits on the rings and issues every copy.
             const int pieces = BN / a.piece;
+            const uint32_t all = 0xffffffffu;
+            int issued = 0, issued_v = 0;
+            const int32_t* trow_ptr = a.table ? a.table + trow * a.max_blocks : nullptr;
+            const int32_t lane_key = lane < pieces ? lane * a.piece : INT32_MAX - BN * n_tiles;
+            const int32_t kadd = kExt ? kbase : 0;
+            // the table entry behind this lane's piece of tile j (0 if none is read)
+            auto entry = [&](int j) -> int32_t {
+                const int32_t key = j * BN + lane_key;
+                if (key >= k_len || !trow_ptr) return 0;
+                return trow_ptr[(key + kadd) / a.block_size];
+            };
+            auto row_of = [&](int j, int32_t phys) -> int32_t {
+                const int32_t key = j * BN + lane_key;
+                if (key >= k_len) return a.oob_row;  // zero-filled by TMA (and idle lanes)
+                if (!trow_ptr) return ck0 + key + kadd;  // packed K/V
+                if (phys < 0 || phys >= a.num_blocks) {
+                    flag_error(a.err, PKV_FLAG_BAD_BLOCK);
+                    return a.oob_row;
+                }
+                return phys * a.block_size + (key + kadd) % a.block_size;
+            };
+            if (lane == 0) {
+                const int nq = has_b ? 2 : 1;
+                mbar_arrive_expect_tx(q_ready, nq * kTileBytes);
+                for (int x = 0; x < nq; ++x) {
+                    unsigned char* qd = sm + OFF_Q + x * kTileBytes;
+                    tma_load_3d(qd, &tmap_q, 0, h_a + x, box_row0, q_ready);
+                    tma_load_3d(qd + kRegionBytes, &tmap_q, 64, h_a + x, box_row0, q_ready);
+                }
+            }
+            int32_t e_cur = entry(0);
+            for (int j = 0; j < n_tiles; ++j) {
+                const int sk = j % SK, sv = j % SV;
+                const int32_t e_next = j + 1 < n_tiles ? entry(j + 1) : 0;
+                const int32_t my_row = row_of(j, e_cur);
+                e_cur = e_next;
+                int ok = 1;
+                if (lane == 0) {
+                    ok = mbar_wait(&k_empty[sk], ((j / SK) & 1) ^ 1, a.err);
+                    if (ok) mbar_arrive_expect_tx(&k_full[sk], kTileBytes);
+                }
+                if (!__shfl_sync(all, ok, 0)) break;
+                for (int p = 0; p < pieces; ++p) {
+                    const int32_t row = __shfl_sync(all, my_row, p);
+                    if (lane == 0) {
+                        unsigned char* kd = sm + OFF_K + sk * kTileBytes + p * a.piece * 128;
+                        tma_load_3d(kd, &tmap_k, 0, kvh, row, &k_full[sk]);
+                        tma_load_3d(kd + kRegionBytes, &tmap_k, 64, kvh, row, &k_full[sk]);
+                    }
+                }
+                ++issued;
+                if (lane == 0) {
+                    ok = mbar_wait(&v_empty[sv], ((j / SV) & 1) ^ 1, a.err);
+                    if (ok) mbar_arrive_expect_tx(&v_full[sv], kTileBytes);
+                }
+                if (!__shfl_sync(all, ok, 0)) break;
+                for (int p = 0; p < pieces; ++p) {
+                    const int32_t row = __shfl_sync(all, my_row, p);
+                    if (lane == 0) {
+                        unsigned char* vd = sm + OFF_V + sv * kTileBytes + p * a.piece * 128;
+                        tma_load_3d(vd, &tmap_v, 0, kvh, row, &v_full[sv]);
+                        tma_load_3d(vd + kRegionBytes, &tmap_v, 64, kvh, row, &v_full[sv]);
+                    }
+                }
+                ++issued_v;
+            }
+            // drain: every issued tile has landed before the CTA can exit
+            if (lane == 0) {
+                mbar_wait(q_ready, 0, a.err);
+                for (int j = max(0, issued - SK); j < issued; ++j)
+                    mbar_wait(&k_full[j % SK], (j / SK) & 1, a.err);
+                for (int j = max(0, issued_v - SV); j < issued_v; ++j)
+                    mbar_wait(&v_full[j % SV], (j / SV) & 1, a.err);
+            }
+        } else if (lane == 0) {
+            // one page piece per tile: lane 0 alone reads the table and issues
+            const int pieces = 1;
             int issued = 0, issued_v = 0;
             auto page_row = [&](int32_t key) -> int32_t {
                 if (key >= k_len) return a.oob_row;  // zero-filled by TMA
@@ -384,16 +465,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
             }
             for (int j = 0; j < n_tiles; ++j) {
                 const int sk = j % SK, sv = j % SV;
-                if (kExt && a.table && pieces > 1 && j + 1 < n_tiles) {
-                    // the next tile's table entries towards L1 while this one waits
-                    // (entries idx0 .. idx1 of the request's row; idx0 < max_blocks
-                    // because a tile starts below k_len <= max_blocks * B)
-                    const int32_t idx0 = (kbase + (j + 1) * BN) / a.block_size;
-                    const int32_t idx1 = min(idx0 + pieces - 1, a.max_blocks - 1);
-                    const int32_t* row = a.table + trow * a.max_blocks;
-                    asm volatile("prefetch.global.L1 [%0];" ::"l"(row + idx0));
-                    asm volatile("prefetch.global.L1 [%0];" ::"l"(row + idx1));
-                }
                 if (!mbar_wait(&k_empty[sk], ((j / SK) & 1) ^ 1, a.err)) break;
                 mbar_arrive_expect_tx(&k_full[sk], kTileBytes);
                 for (int p = 0; p < pieces; ++p) {
