@@ -612,19 +612,23 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const CombineArgs c
                 wl = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
                 lp += ml.y * wl;
             }
-            // the round's o rows all in flight at once: rows past n re-read
-            // the last row (a cache hit) and get weight 0 (wl is 0 on lanes >= n)
+            // the round's o rows all in flight at once (predicated loads; rows
+            // past n are zero and their weight is 0: wl is 0 on lanes >= n)
             float v[32][DPL];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const int ii = min(i, n - 1);
-                const float* src = c.part_o + ((int64_t)(base + ii + b) * hq + h) * D + lane * DPL;
-                if constexpr (DPL == 4) {
-                    const float4 t = *reinterpret_cast<const float4*>(src);
-                    v[i][0] = t.x; v[i][1] = t.y; v[i][2] = t.z; v[i][3] = t.w;
-                } else {
-                    const float2 t = *reinterpret_cast<const float2*>(src);
-                    v[i][0] = t.x; v[i][1] = t.y;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) v[i][e] = 0.f;
+                if (i < n) {
+                    const float* src =
+                        c.part_o + ((int64_t)(base + i + b) * hq + h) * D + lane * DPL;
+                    if constexpr (DPL == 4) {
+                        const float4 t = *reinterpret_cast<const float4*>(src);
+                        v[i][0] = t.x; v[i][1] = t.y; v[i][2] = t.z; v[i][3] = t.w;
+                    } else {
+                        const float2 t = *reinterpret_cast<const float2*>(src);
+                        v[i][0] = t.x; v[i][1] = t.y;
+                    }
                 }
             }
 #pragma unroll
