@@ -363,9 +363,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         // ------------------------------ TMA producer ------------------------------
         if (a.piece < BN) {
             // Several page pieces per tile.  The whole warp: lane p finds the
-            // pool row of piece p of a tile, its block-table entry read one
-            // tile ahead so that the lookups overlap the previous tile's
-            // copies; lane 0 waits on the rings and issues every copy.
+            // pool row of piece p of a tile (its block-table entry read one
+            // tile ahead, so that the lookups overlap the previous tile's
+            // copies) and issues that piece's two box copies; lane 0 waits
+            // on the rings and sets the expected bytes.
             const int pieces = BN / a.piece;
             const uint32_t all = 0xffffffffu;
             int issued = 0, issued_v = 0;
@@ -409,13 +410,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     if (ok) mbar_arrive_expect_tx(&k_full[sk], kTileBytes);
                 }
                 if (!__shfl_sync(all, ok, 0)) break;
-                for (int p = 0; p < pieces; ++p) {
-                    const int32_t row = __shfl_sync(all, my_row, p);
-                    if (lane == 0) {
-                        unsigned char* kd = sm + OFF_K + sk * kTileBytes + p * a.piece * 128;
-                        tma_load_3d(kd, &tmap_k, 0, kvh, row, &k_full[sk]);
-                        tma_load_3d(kd + kRegionBytes, &tmap_k, 64, kvh, row, &k_full[sk]);
-                    }
+                if (lane < pieces) {
+                    unsigned char* kd = sm + OFF_K + sk * kTileBytes + lane * a.piece * 128;
+                    tma_load_3d(kd, &tmap_k, 0, kvh, my_row, &k_full[sk]);
+                    tma_load_3d(kd + kRegionBytes, &tmap_k, 64, kvh, my_row, &k_full[sk]);
                 }
                 ++issued;
                 if (lane == 0) {
@@ -423,13 +421,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     if (ok) mbar_arrive_expect_tx(&v_full[sv], kTileBytes);
                 }
                 if (!__shfl_sync(all, ok, 0)) break;
-                for (int p = 0; p < pieces; ++p) {
-                    const int32_t row = __shfl_sync(all, my_row, p);
-                    if (lane == 0) {
-                        unsigned char* vd = sm + OFF_V + sv * kTileBytes + p * a.piece * 128;
-                        tma_load_3d(vd, &tmap_v, 0, kvh, row, &v_full[sv]);
-                        tma_load_3d(vd + kRegionBytes, &tmap_v, 64, kvh, row, &v_full[sv]);
-                    }
+                if (lane < pieces) {
+                    unsigned char* vd = sm + OFF_V + sv * kTileBytes + lane * a.piece * 128;
+                    tma_load_3d(vd, &tmap_v, 0, kvh, my_row, &v_full[sv]);
+                    tma_load_3d(vd + kRegionBytes, &tmap_v, 64, kvh, my_row, &v_full[sv]);
                 }
                 ++issued_v;
             }
