@@ -138,14 +138,24 @@ __device__ __forceinline__ int32_t clamp_len(int32_t L, int32_t cap) {
 // First key of sequence b this kernel covers: 0, or in shared-prefix mode the
 // group's prefix length (a multiple of the block size, at most L; anything
 // else is flagged and rounded down to a whole tile).
-__device__ __forceinline__ int32_t seq_start(const DecodeArgs& a, int b, int32_t L) {
-    if (!a.group_cu) return 0;
-    int lo = 0, hi = a.n_groups;  // last g with group_cu[g] <= b
+// the group of sequence b: the last g with group_cu[g] <= b (binary search)
+__device__ __forceinline__ int group_of(const DecodeArgs& a, int b) {
+    int lo = 0, hi = a.n_groups;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
         if (__ldg(a.group_cu + mid) <= b) lo = mid; else hi = mid;
     }
-    int32_t s = __ldg(a.group_plen + lo);
+    return lo;
+}
+
+// First key of sequence b's own tiles (its group's prefix length, 0 without
+// groups).  g is the caller's group cursor: the group of a sequence at or
+// before b (a CTA walks its sequences in order, so it moves forward one
+// group at a time instead of searching).
+__device__ __forceinline__ int32_t seq_start(const DecodeArgs& a, int b, int32_t L, int& g) {
+    if (!a.group_cu) return 0;
+    while (g + 1 < a.n_groups && __ldg(a.group_cu + g + 1) <= b) ++g;
+    int32_t s = __ldg(a.group_plen + g);
     if (s < 0 || s > L || s % a.block_size) {
         flag_error(a.err, PKV_FLAG_BAD_LENGTH);
         s = s < 0 ? 0 : (s > L ? L : s);
@@ -162,9 +172,10 @@ __device__ void scan_tiles(const DecodeArgs& a, int32_t* tstart) {
     const int lo = tid * per, hi = min(lo + per, a.batch);
     const int32_t cap = a.max_blocks * a.block_size;
     int32_t sum = 0;
+    int g = (a.group_cu && lo < hi) ? group_of(a, lo) : 0;
     for (int b = lo; b < hi; ++b) {
         const int32_t L = clamp_len(a.seqlens[b], cap);
-        sum += (L - seq_start(a, b, L) + a.rows - 1) / a.rows;
+        sum += (L - seq_start(a, b, L, g) + a.rows - 1) / a.rows;
     }
     const int lane = tid & 31, warp = tid >> 5;
     int32_t inc = sum;
@@ -178,10 +189,11 @@ __device__ void scan_tiles(const DecodeArgs& a, int32_t* tstart) {
     int32_t base = 0;
     for (int w = 0; w < warp; ++w) base += warp_tot[w];
     int32_t run = base + inc - sum;  // exclusive prefix of this thread's first sequence
+    g = (a.group_cu && lo < hi) ? group_of(a, lo) : 0;
     for (int b = lo; b < hi; ++b) {
         tstart[b] = run;
         const int32_t L = clamp_len(a.seqlens[b], cap);
-        run += (L - seq_start(a, b, L) + a.rows - 1) / a.rows;
+        run += (L - seq_start(a, b, L, g) + a.rows - 1) / a.rows;
     }
     if (tid == nthr - 1) tstart[a.batch] = base + inc;
 }
@@ -273,13 +285,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
         if (lane != 0) return;
         const uint64_t pol = l2_evict_first_policy();
         int b = seq_of_tile(tstart, a.batch, t0);
+        int g = a.group_cu ? group_of(a, b) : 0;
         int32_t L = clamp_len(a.seqlens[b], cap);
-        int32_t st = seq_start(a, b, L);
+        int32_t st = seq_start(a, b, L, g);
         for (int32_t t = t0, k = 0; t < t1; ++t, ++k) {
             while (t >= tstart[b + 1]) {
                 ++b;
                 L = clamp_len(a.seqlens[b], cap);
-                st = seq_start(a, b, L);
+                st = seq_start(a, b, L, g);
             }
             const int s = k % S;
             if (!mbar_wait(&empty[s], ((k / S) & 1) ^ 1, a.err)) return;
@@ -328,6 +341,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
     float2 q2[G][8], o2[G][8];
     float m[G], l[G];
     int b = seq_of_tile(tstart, a.batch, t0);
+    int gcur = a.group_cu ? group_of(a, b) : 0;
     int loaded = -1;
     int32_t L = 0, st = 0;
 
@@ -335,14 +349,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
         while (t >= tstart[b + 1]) ++b;
         if (b != loaded) {
             loaded = b;
-            L = clamp_len(a.seqlens[b], cap);
-            st = seq_start(a, b, L);
-            const float2 sc2 = make_float2(a.qscale, a.qscale);
+            // the queries first: their loads overlap the length lookups
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const int64_t qb = ((int64_t)b * a.hq + (int64_t)kvh * G + g) * D;
                 load8_global<BF16>(a.q, qb + dim0, &q2[g][0]);
                 load8_global<BF16>(a.q, qb + dim1, &q2[g][4]);
+            }
+            L = clamp_len(a.seqlens[b], cap);
+            st = seq_start(a, b, L, gcur);
+            const float2 sc2 = make_float2(a.qscale, a.qscale);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     q2[g][e] = fmul2(q2[g][e], sc2);
