@@ -275,13 +275,18 @@ int paged_decode_shared_prefix(const void* q, const void* k_cache, const void* v
                                         geom->num_blocks, dev.err, stream, &ex);
     if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return PKV_ERR_CUDA;
-    // 2. each sequence's own keys after the prefix, merged with the prefix state
+    // 2. each sequence's own keys after the prefix, merged with the prefix state.
+    //    The split needs nothing from the prefix pass (only the combine does),
+    //    so it starts while the prefix pass runs and holds its grid open until
+    //    that kernel completes; the prefix pass itself started after all earlier
+    //    work on the stream.
     pkv::SharedPrefix sp{group_cu, group_prefix_len, n_groups, x_out, x_lse, kchunks};
+    pkv::DecodeChain ch{true};
     return cuda_status(pkv::launch_decode(plan, q, k_cache, v_cache, block_table,
                                           max_blocks_per_seq, cache_seqlens, batch, scale, out,
                                           workspace, geom->num_heads, geom->num_kv_heads,
                                           geom->head_dim, geom->block_size, geom->num_blocks,
-                                          geom->dtype, dev.err, stream, &sp));
+                                          geom->dtype, dev.err, stream, &sp, nullptr, &ch));
 }
 
 size_t paged_mixed_step_workspace_size(int32_t decode_batch, const pkv_geom* geom) {
