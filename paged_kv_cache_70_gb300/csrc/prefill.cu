@@ -359,19 +359,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const uint32_t tmem = *tmem_slot;
     if (warp >= 8) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
-      if (warp == 8) {
+      if (warp == 8 || (warp >= 10 && a.piece < BN)) {
         // ------------------------------ TMA producer ------------------------------
         if (a.piece < BN) {
-            // Several page pieces per tile.  The whole warp: lane p finds the
-            // pool row of piece p of a tile (its block-table entry read one
-            // tile ahead, so that the lookups overlap the previous tile's
-            // copies) and issues that piece's two box copies; lane 0 waits
-            // on the rings and sets the expected bytes.
+            // Several page pieces per tile: 2 box copies per piece, and a copy
+            // takes ~100+ cycles to issue, so warps 8, 10 and 11 share them:
+            // lane l of producer warp w takes piece 3l + w.  The lane finds
+            // the piece's pool row (its block-table entry read one tile
+            // ahead, so that the lookups overlap the previous tile's copies)
+            // and issues its two box copies once its warp's lane 0 has seen
+            // the ring slot free.  Warp 8 alone sets each slot's expected
+            // bytes (a copy may complete first: the count goes below zero
+            // until then, and the phase cannot complete without that arrive).
+            const int pw = warp == 8 ? 0 : warp - 9;  // 0, 1, 2
+            const int piece_of_lane = lane * 3 + pw;
             const int pieces = BN / a.piece;
             const uint32_t all = 0xffffffffu;
             int issued = 0, issued_v = 0;
             const int32_t* trow_ptr = a.table ? a.table + trow * a.max_blocks : nullptr;
-            const int32_t lane_key = lane < pieces ? lane * a.piece : INT32_MAX - BN * n_tiles;
+            const int32_t lane_key = piece_of_lane < pieces ? piece_of_lane * a.piece
+                                                            : INT32_MAX - BN * n_tiles;
             const int32_t kadd = kExt ? kbase : 0;
             // the table entry behind this lane's piece of tile j (0 if none is read)
             auto entry = [&](int j) -> int32_t {
@@ -389,7 +396,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 }
                 return phys * a.block_size + (key + kadd) % a.block_size;
             };
-            if (lane == 0) {
+            if (pw == 0 && lane == 0) {
                 const int nq = has_b ? 2 : 1;
                 mbar_arrive_expect_tx(q_ready, nq * kTileBytes);
                 for (int x = 0; x < nq; ++x) {
@@ -407,29 +414,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 int ok = 1;
                 if (lane == 0) {
                     ok = mbar_wait(&k_empty[sk], ((j / SK) & 1) ^ 1, a.err);
-                    if (ok) mbar_arrive_expect_tx(&k_full[sk], kTileBytes);
+                    if (ok && pw == 0) mbar_arrive_expect_tx(&k_full[sk], kTileBytes);
                 }
                 if (!__shfl_sync(all, ok, 0)) break;
-                if (lane < pieces) {
-                    unsigned char* kd = sm + OFF_K + sk * kTileBytes + lane * a.piece * 128;
+                if (piece_of_lane < pieces) {
+                    unsigned char* kd =
+                        sm + OFF_K + sk * kTileBytes + piece_of_lane * a.piece * 128;
                     tma_load_3d(kd, &tmap_k, 0, kvh, my_row, &k_full[sk]);
                     tma_load_3d(kd + kRegionBytes, &tmap_k, 64, kvh, my_row, &k_full[sk]);
                 }
                 ++issued;
                 if (lane == 0) {
                     ok = mbar_wait(&v_empty[sv], ((j / SV) & 1) ^ 1, a.err);
-                    if (ok) mbar_arrive_expect_tx(&v_full[sv], kTileBytes);
+                    if (ok && pw == 0) mbar_arrive_expect_tx(&v_full[sv], kTileBytes);
                 }
                 if (!__shfl_sync(all, ok, 0)) break;
-                if (lane < pieces) {
-                    unsigned char* vd = sm + OFF_V + sv * kTileBytes + lane * a.piece * 128;
+                if (piece_of_lane < pieces) {
+                    unsigned char* vd =
+                        sm + OFF_V + sv * kTileBytes + piece_of_lane * a.piece * 128;
                     tma_load_3d(vd, &tmap_v, 0, kvh, my_row, &v_full[sv]);
                     tma_load_3d(vd + kRegionBytes, &tmap_v, 64, kvh, my_row, &v_full[sv]);
                 }
                 ++issued_v;
             }
-            // drain: every issued tile has landed before the CTA can exit
-            if (lane == 0) {
+            // drain: every issued tile (all three warps' copies) has landed
+            // before the CTA can exit
+            if (pw == 0 && lane == 0) {
                 mbar_wait(q_ready, 0, a.err);
                 for (int j = max(0, issued - SK); j < issued; ++j)
                     mbar_wait(&k_full[j % SK], (j / SK) & 1, a.err);
