@@ -50,8 +50,10 @@
 //     arrays, the keys may be cut into chunks (each a separate work item with
 //     its own output block), and each row's log2-sum-exp m + log2(l) is
 //     written for the merge with the rest of the keys.
-// The kernel lets programmatic dependents start at once (it writes nothing
-// they read).
+// The plain prefill starts as a programmatic dependent of the kernel before
+// it and waits for it; after that it lets its own dependents start (it
+// writes nothing they read).  The shared-prefix instantiation lets them start
+// at once.
 // Every mbarrier wait is time-limited; a timeout sets PKV_FLAG_TIMEOUT and the
 // CTA drains its copies and frees TMEM before returning.
 #include <cuda.h>
@@ -271,8 +273,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     uint64_t* q_ready = o_ready + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
 
-    // a kernel launched after this one as its programmatic dependent may start
-    // now (it orders itself with griddepcontrol.wait where it needs to)
+    // The plain prefill is launched as a programmatic dependent of the kernel
+    // before it (typically the write of the new rows), so it waits for that
+    // kernel before reading anything.  Only then may a kernel launched after
+    // this one start; one that does not wait (the shared-prefix pass) thus
+    // still runs after the write.  The shared-prefix instantiation is
+    // launched after its inputs are complete and needs no wait.
+    if constexpr (!kExt) asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = kExt ? (int)blockIdx.z / a.kchunks : (int)blockIdx.z;
@@ -859,9 +866,10 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(a.tiles_q, a.pair_heads ? (hq + 1) / 2 : hq, batch * a.kchunks);
-    if (ex && ex->pdl) {
-        // start as a programmatic dependent of the previous kernel (it needs
-        // none of that kernel's results)
+    if (!ex || ex->pdl) {
+        // start as a programmatic dependent of the previous kernel: the plain
+        // prefill waits for it in the kernel; the shared-prefix pass of the
+        // mixed step needs none of its results
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
         cfg.blockDim = dim3(kThreads);
