@@ -160,12 +160,19 @@ def test_nonfinite_pool_padding_is_ignored():
     assert_close(out, run_oracle(c), "bf16", "nan padding")
 
 
-def test_bad_block_id_is_flagged():
-    c = make_case([40], [300], B=64, seed=12)
-    c["table"][0, 2] = 10_000
+@pytest.mark.parametrize("B,entry", [(64, 2), (16, 3), (16, 4), (16, 2), (16, 9), (32, 5)])
+def test_bad_block_id_is_flagged(B, entry):
+    """A table entry outside the pool is flagged and its page skipped.  With
+    several pages per 128-key tile (B < 128) the pages of a tile are shared by
+    three producer warps (page p of a tile by warp p mod 3); the cases put the
+    bad page in each of them.  Nothing waits past its time limit."""
+    c = make_case([40], [300], B=B, seed=12)
+    c["table"][0, entry] = 10_000
     run_gpu(c)
     torch.cuda.synchronize()
-    assert pkv.paged_error_flags() & pkv.PKV_FLAG_BAD_BLOCK
+    flags = pkv.paged_error_flags()
+    assert flags & pkv.PKV_FLAG_BAD_BLOCK
+    assert not flags & pkv.PKV_FLAG_TIMEOUT
 
 
 def test_unsupported_combinations():
