@@ -239,8 +239,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
     float* mscratch = reinterpret_cast<float*>(smem + 256 + kTstartBytes);
     unsigned char* stage_base = smem + decode_fixed_smem(G, D);
 
-    // the combine kernel may be scheduled now; it waits for this grid's results
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = a.stages, R = a.rows, HC = a.hc;
@@ -258,6 +256,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
     // launched as a programmatic dependent: the lengths, table and K/V may come
     // from the kernel before (the new token's write)
     if (a.wait_inputs) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Kernels launched after this one may be scheduled now (the combine waits
+    // for this grid's results).  After the wait above, so that one that does
+    // not wait would still start only after everything before this grid.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     scan_tiles(a, tstart);
     __syncthreads();
 
