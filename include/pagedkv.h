@@ -24,6 +24,15 @@
  * (pkv_geom is read on the host).  The caller owns every buffer; the library
  * allocates no device memory.  Calls are asynchronous on `stream` and never
  * synchronise the host, except paged_error_flags.
+ * Ordering.  Work enqueued on `stream` before a call completes before the
+ * call reads anything, and work enqueued after it sees all of its results,
+ * as for any stream-ordered launch.  The library's kernels are launched as
+ * programmatic dependents of the kernel before them and let the next kernel
+ * launch early (programmatic dependent launch).  This matters only to a
+ * caller kernel that is itself launched after a call with the
+ * programmatic-stream-serialization attribute: it may start before the call's
+ * kernels finish, and must execute griddepcontrol.wait
+ * (cudaGridDependencySynchronize) before it reads their results.
  * Layouts (row-major, contiguous):
  *   K/V pools  [num_blocks, block_size, num_kv_heads, head_dim]; the element
  *              offset of logical position p of a sequence whose block-table row
