@@ -770,12 +770,11 @@ bool plan_decode(const DeviceInfo& dev, int32_t batch, int hq, int hkv, int d, i
 
 template <int D, bool BF16, int G>
 static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a,
-                                   const CombineArgs& c, bool pdl_split, cudaStream_t stream) {
+                                   const CombineArgs& c, cudaStream_t stream) {
     auto kern = decode_split_kernel<D, BF16, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)plan.smem_bytes);
     if (e != cudaSuccess) return e;
-    (void)pdl_split;
     e = launch_dependent(kern, dim3(plan.ctas, plan.head_groups), dim3(kDecodeThreads),
                          plan.smem_bytes, stream, a);
     if (e != cudaSuccess) return e;
@@ -864,7 +863,7 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
     c.err = err;
 #define PKV_DECODE_CASE(DD, BB, GG) \
     if (d == DD && bf == BB && G == GG) \
-        return launch_decode_t<DD, BB, GG>(plan, a, c, a.wait_prior != 0, stream);
+        return launch_decode_t<DD, BB, GG>(plan, a, c, stream);
     PKV_DECODE_CASE(128, true, 1) PKV_DECODE_CASE(128, true, 2) PKV_DECODE_CASE(128, true, 4)
     PKV_DECODE_CASE(128, false, 1) PKV_DECODE_CASE(128, false, 2) PKV_DECODE_CASE(128, false, 4)
     PKV_DECODE_CASE(64, true, 1) PKV_DECODE_CASE(64, true, 2) PKV_DECODE_CASE(64, true, 4)
