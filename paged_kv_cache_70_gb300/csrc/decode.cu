@@ -56,6 +56,20 @@ namespace pkv {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+// With 9 warps an SM sub-partition holds 3 of a CTA's warps, which caps a
+// thread at 168 registers: enough for GQA groups of 1 and 2.  A group of 4
+// keeps 4 heads' q and o per lane, so that kernel runs 12 warps (8 consumers,
+// the producer, 3 that only complete its warpgroup) and moves registers from
+// the producer warpgroup to the consumers with setmaxnreg: 8 x 208 + 4 x 88 =
+// 2016 <= 12 x 168 per thread-lane, and 208 + 208 + 88 <= 512 per
+// sub-partition lane.
+template <int G>
+constexpr int decode_threads() { return G >= 4 ? 12 * 32 : kDecodeThreads; }
+constexpr int kDecodeMaxWarps = 12;
+constexpr int kConsumerRegs4 = 208;
+constexpr int kProducerRegs4 = 88;
+static_assert(8 * kConsumerRegs4 + 4 * kProducerRegs4 <= 12 * 168,
+              "register split exceeds the launch");
 constexpr int kMaxStages = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -166,7 +180,7 @@ __device__ __forceinline__ int32_t seq_start(const DecodeArgs& a, int b, int32_t
 
 // Exclusive scan of per-sequence tile counts into tstart[0..batch] (all threads).
 __device__ void scan_tiles(const DecodeArgs& a, int32_t* tstart) {
-    __shared__ int32_t warp_tot[kDecodeThreads / 32];
+    __shared__ int32_t warp_tot[kDecodeMaxWarps];
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int per = (a.batch + nthr - 1) / nthr;
     const int lo = tid * per, hi = min(lo + per, a.batch);
@@ -227,7 +241,7 @@ __device__ __forceinline__ void online_update(float s, const float2* v, float& m
 }
 
 template <int D, bool BF16, int G>
-__global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(const DecodeArgs a) {
     constexpr int ELT = BF16 ? 2 : 4;
     constexpr int TG = D / 16;    // lanes per key row
     constexpr int GPW = 32 / TG;  // key rows processed side by side by a warp
@@ -278,7 +292,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
     if (t0 >= t1) return;
     const int head0 = blockIdx.y * HC;  // first KV head of this CTA
 
-    if (warp == kConsumerWarps) {
+    if (warp >= kConsumerWarps) {
+        if constexpr (G >= 4) {
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs4));
+            if (warp > kConsumerWarps) return;  // only completed the producer's warpgroup
+        }
         // ------------------------------ producer ------------------------------
         // an otherwise idle lane holds the grid open until the kernel launched
         // before it has completed (the combine waits for this grid)
@@ -330,6 +348,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(const D
     }
 
     // ------------------------------- consumers --------------------------------
+    if constexpr (G >= 4) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs4));
     const int hc = warp % HC;     // local KV head of this warp
     const int wrank = warp / HC;  // rank among the warps sharing this head
     const int WH = kConsumerWarps / HC;
@@ -775,7 +794,7 @@ static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a,
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)plan.smem_bytes);
     if (e != cudaSuccess) return e;
-    e = launch_dependent(kern, dim3(plan.ctas, plan.head_groups), dim3(kDecodeThreads),
+    e = launch_dependent(kern, dim3(plan.ctas, plan.head_groups), dim3(decode_threads<G>()),
                          plan.smem_bytes, stream, a);
     if (e != cudaSuccess) return e;
     // combine: programmatic dependent of the split kernel

@@ -63,6 +63,9 @@ CASES = [
     ("f32", 16, 8, 128, 32, [1, 31, 64, 100]),
     ("bf16", 8, 8, 128, 64, [3, 130, 700]),        # G = 1
     ("bf16", 32, 8, 128, 16, [77, 500, 1]),         # G = 4
+    ("f32", 16, 4, 64, 16, [5, 700, 33]),           # G = 4, fp32, d = 64
+    ("bf16", 4, 1, 128, 32, [1, 63, 2000]),         # G = 4, Hkv = 1 (8 warps share the head)
+    ("bf16", 32, 8, 128, 256, [20000, 3]),          # G = 4, long context
     ("f32", 4, 1, 64, 32, [30, 32, 70, 0]),         # Hkv = 1 (warps share a head)
     ("bf16", 4, 2, 64, 48, [47, 48, 49, 200]),      # B not a power of two
     ("bf16", 8, 4, 64, 1, [1, 2, 9]),               # B = 1
