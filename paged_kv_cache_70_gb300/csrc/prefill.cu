@@ -244,7 +244,15 @@ struct PrefillArgs {
     int32_t oob_row;  // a row index beyond the pools (zero-filled by TMA)
     int32_t tiles_q;
     int32_t causal;
+    int32_t pair_tiles;  // 1: a CTA takes query tiles qt and qt - 1 of one head
 };
+
+// v[x] for a runtime x in {0, 1} without indexing the array (which would
+// put it in local memory)
+template <typename T>
+__device__ __forceinline__ T pick(const T (&v)[2], int x) {
+    return x ? v[1] : v[0];
+}
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* err) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
@@ -284,9 +292,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = kExt ? (int)blockIdx.z / a.kchunks : (int)blockIdx.z;
     const int kchunk = kExt ? (int)blockIdx.z % a.kchunks : 0;
-    const int qt = a.tiles_q - 1 - (int)blockIdx.x;  // later (heavier) tiles first
     const int h_a = a.pair_heads ? 2 * (int)blockIdx.y : (int)blockIdx.y;
-    const bool has_b = a.pair_heads && h_a + 1 < a.hq;
     const int32_t cq0 = a.cu_q[r], cq1 = a.cu_q[r + 1];
     const int32_t ck0 = a.cu_k[r], ck1 = a.cu_k[r + 1];
     int32_t q_len = cq1 - cq0, k_len = (kExt && a.req_klen) ? a.req_klen[r] : ck1 - ck0;
@@ -307,30 +313,58 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         kbase = kchunk * per;
         k_len = max(0, min(per, k_len - kbase));
     }
-    const int32_t q0 = qt * BM;
-    if (q0 >= q_len) return;
-    const int rows = min(BM, q_len - q0);
-    // The Q box always ends at the tile's last query row, so a ragged tile
-    // (rows < 128) starts `shift` rows early: smem row / TMEM lane t holds
-    // query q0 + t - shift, and lanes below `shift` are not stored.
-    const int shift = BM - rows;
-    const int32_t box_row0 = cq0 + q0 + rows - BM;  // negative rows arrive zero-filled
+    // The CTA's two Q tiles, A (x = 0) and B (x = 1), share every K/V tile:
+    //   - pair_heads: one 128-row query tile for query heads h_a and h_a + 1
+    //     (the same KV head);
+    //   - pair_tiles (one query head per KV head): query tiles qt and qt - 1
+    //     of head h_a, A the later one (it sees the most keys; a last key
+    //     tile beyond B's rows is fully masked for B); B is absent at qt = 0;
+    //   - otherwise A alone.
+    // Later (heavier) tiles come first in the grid.
+    int qt, qt_b;
+    if (a.pair_tiles) {
+        qt = (q_len + BM - 1) / BM - 1 - 2 * (int)blockIdx.x;
+        qt_b = qt - 1;
+    } else {
+        qt = a.tiles_q - 1 - (int)blockIdx.x;
+        qt_b = qt;
+    }
+    if (qt < 0 || qt * BM >= q_len) return;
+    const bool has_b = a.pair_tiles ? qt_b >= 0 : (a.pair_heads && h_a + 1 < a.hq);
+    // Per Q tile: first query row, rows, head and output row.  The Q box
+    // always ends at the tile's last query row, so a ragged tile (rows < 128;
+    // only a request's last tile) starts `shift` rows early: smem row / TMEM
+    // lane t holds query q0 + t - shift, and lanes below `shift` are not
+    // stored.
+    int32_t tq0[2], trows[2], tshift[2], tbox[2], thead[2];
+    int64_t tout[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        const int q = x == 0 ? qt : max(qt_b, 0);
+        tq0[x] = q * BM;
+        trows[x] = min(BM, q_len - tq0[x]);
+        tshift[x] = BM - trows[x];
+        tbox[x] = cq0 + tq0[x] + trows[x] - BM;  // negative rows arrive zero-filled
+        thead[x] = a.pair_tiles ? h_a : h_a + x;
+        tout[x] = (int64_t)cq0 + tq0[x] + (kExt ? (int64_t)kchunk * a.chunk_rows : 0);
+    }
     const int32_t diag = k_len - q_len;  // query i sees key j <= i + diag
     int32_t last_key = k_len - 1;
-    if (a.causal) last_key = min(last_key, q0 + rows - 1 + diag);
+    if (a.causal) last_key = min(last_key, tq0[0] + trows[0] - 1 + diag);
     const int n_tiles = last_key < 0 ? 0 : last_key / BN + 1;
-    const int64_t out_row0 = (int64_t)cq0 + q0 + (kExt ? (int64_t)kchunk * a.chunk_rows : 0);
 
-    if (n_tiles == 0) {  // no query row of this tile sees a key: output 0
+    if (n_tiles == 0) {  // no query row of these tiles sees a key: output 0
         const int nh = has_b ? 2 : 1;
-        if (kExt && a.lse)
-            for (int i = threadIdx.x; i < nh * rows; i += blockDim.x)
-                a.lse[(out_row0 + i % rows) * a.hq + h_a + i / rows] = -INFINITY;
-        for (int i = threadIdx.x; i < nh * rows * (HD / 8); i += blockDim.x) {
-            const int x = i / (rows * (HD / 8)), rem = i % (rows * (HD / 8));
-            const int rr = rem / (HD / 8), c = rem % (HD / 8);
-            *reinterpret_cast<uint4*>(a.out + ((out_row0 + rr) * a.hq + h_a + x) * HD + c * 8) =
-                make_uint4(0, 0, 0, 0);
+        for (int x = 0; x < nh; ++x) {
+            if (kExt && a.lse)
+                for (int i = threadIdx.x; i < pick(trows, x); i += blockDim.x)
+                    a.lse[(pick(tout, x) + i) * a.hq + pick(thead, x)] = -INFINITY;
+            for (int i = threadIdx.x; i < pick(trows, x) * (HD / 8); i += blockDim.x) {
+                const int rr = i / (HD / 8), c = i % (HD / 8);
+                const int64_t row = pick(tout, x) + rr;
+                *reinterpret_cast<uint4*>(a.out + (row * a.hq + pick(thead, x)) * HD + c * 8) =
+                    make_uint4(0, 0, 0, 0);
+            }
         }
         return;
     }
@@ -408,8 +442,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 mbar_arrive_expect_tx(q_ready, nq * kTileBytes);
                 for (int x = 0; x < nq; ++x) {
                     unsigned char* qd = sm + OFF_Q + x * kTileBytes;
-                    tma_load_3d(qd, &tmap_q, 0, h_a + x, box_row0, q_ready);
-                    tma_load_3d(qd + kRegionBytes, &tmap_q, 64, h_a + x, box_row0, q_ready);
+                    const int hh = pick(thead, x), row = pick(tbox, x);
+                    tma_load_3d(qd, &tmap_q, 0, hh, row, q_ready);
+                    tma_load_3d(qd + kRegionBytes, &tmap_q, 64, hh, row, q_ready);
                 }
             }
             int32_t e_cur = entry(0);
@@ -472,8 +507,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
             mbar_arrive_expect_tx(q_ready, nq * kTileBytes);
             for (int x = 0; x < nq; ++x) {
                 unsigned char* qd = sm + OFF_Q + x * kTileBytes;
-                tma_load_3d(qd, &tmap_q, 0, h_a + x, box_row0, q_ready);
-                tma_load_3d(qd + kRegionBytes, &tmap_q, 64, h_a + x, box_row0, q_ready);
+                const int hh = pick(thead, x), row = pick(tbox, x);
+                tma_load_3d(qd, &tmap_q, 0, hh, row, q_ready);
+                tma_load_3d(qd + kRegionBytes, &tmap_q, 64, hh, row, q_ready);
             }
             for (int j = 0; j < n_tiles; ++j) {
                 const int sk = j % SK, sv = j % SV;
@@ -569,11 +605,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         // ------------------------------ softmax warps ------------------------------
         const int x = warp >> 2;        // Q tile: 0 = A, 1 = B
         const int t = threadIdx.x & 127;  // query row in the tile == TMEM lane
-        const int h = h_a + x;
+        const int h = pick(thead, x);
+        const int shift = pick(tshift, x);
+        const int64_t out_row0 = pick(tout, x);
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tm_s = tmem + x * 128 + lane_base;
         const uint32_t tm_o = tmem + 256 + x * 128 + lane_base;
-        const int32_t row_i = q0 + t - shift;  // query index within the request
+        const int32_t row_i = pick(tq0, x) + t - shift;  // query index within the request
         int32_t lim = k_len - 1;
         if (a.causal) lim = min(lim, row_i + diag);
         const float sl = a.scale_log2;
@@ -856,6 +894,9 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
     a.hq = hq;
     a.group = hq / hkv;
     a.pair_heads = (a.group % 2 == 0) ? 1 : 0;
+    // one query head per KV head: the CTA's second Q tile is the query tile
+    // before the first (same head, same keys) instead of a second head
+    a.pair_tiles = (!ex && !a.pair_heads) ? 1 : 0;
     a.block_size = block_size;
     a.piece = piece;
     a.oob_row = (int32_t)rows;
@@ -865,7 +906,8 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.tiles_q, a.pair_heads ? (hq + 1) / 2 : hq, batch * a.kchunks);
+    dim3 grid(a.pair_tiles ? (a.tiles_q + 1) / 2 : a.tiles_q, a.pair_heads ? (hq + 1) / 2 : hq,
+              batch * a.kchunks);
     if (!ex || ex->pdl) {
         // start as a programmatic dependent of the previous kernel: the plain
         // prefill waits for it in the kernel; the shared-prefix pass of the

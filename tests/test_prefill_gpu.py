@@ -85,6 +85,23 @@ def test_gqa_groups(hq, hkv):
     assert_close(widen(run_gpu(c)), run_oracle(c), "bf16", f"{hq}/{hkv}")
 
 
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (12, 4)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_query_tile_pairs(hq, hkv, causal):
+    """An odd GQA group (1, 3): a CTA takes two consecutive query tiles of one
+    head instead of two heads.  Query lengths give odd and even tile counts,
+    ragged last tiles and a single tile; cached keys shift the causal
+    diagonal, and a request with fewer keys than queries leaves rows that see
+    no key."""
+    qlens = [1, 127, 128, 129, 255, 256, 300, 513]
+    klens = [40, 127, 300, 129, 600, 256, 1000, 300]
+    c = make_case(qlens, klens, B=64, hq=hq, hkv=hkv, seed=hq + hkv + int(causal))
+    out = run_gpu(c, causal)
+    torch.cuda.synchronize()
+    assert_close(widen(out), run_oracle(c, causal), "bf16", f"{hq}/{hkv} causal={causal}")
+    assert pkv.paged_error_flags() == 0
+
+
 @pytest.mark.parametrize("causal", [True, False])
 def test_causal_flag(causal):
     c = make_case([131, 7, 256], [131, 300, 600], B=32, seed=5)
