@@ -22,7 +22,9 @@
 //    mbarriers; ~128 KiB stay in flight per SM.  The block-table entry is read
 //    and range-checked once per tile, by the producer.
 //  * Math.  Eight consumer warps; each warp owns one KV head and its G query
-//    heads (the K/V tile is shared across the GQA group).  Within a warp,
+//    heads (the K/V tile is shared across the GQA group).  For G = 4 the CTA
+//    has 12 warps and setmaxnreg moves registers from the producer's
+//    warpgroup to the consumers, which hold 4 heads' q and o.  Within a warp,
 //    groups of D/16 lanes take key rows, every lane holding 16 of the D
 //    dimensions of q (pre-scaled by scale*log2 e) and of o as fp32 pairs; a
 //    group handles two key rows at a time with packed fp32x2 FMAs (four

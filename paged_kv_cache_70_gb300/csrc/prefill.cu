@@ -12,8 +12,10 @@
 //   out = softmax(scale * Q K^T) V over the visible keys, 0 for a row that
 //   sees none.
 //
-// GB300 design, one CTA per (128-query tile, pair of query heads of one KV
-// head, request) -- two Q tiles A and B that read the same K/V stream:
+// GB300 design, one CTA per request and two Q tiles A and B that read the
+// same K/V stream: one 128-query tile of a pair of query heads of one KV head
+// (even GQA group), or two consecutive 128-query tiles of one head (odd group,
+// e.g. MHA); later (heavier) tiles first:
 //   warp 8   TMA producer: first the two Q tiles (one box per 64 dims,
 //            ending at the tile's last query row so that a ragged tile never
 //            reads past its request), then K and V tiles of 128 keys x 128
@@ -21,7 +23,8 @@
 //            128-byte swizzle; a K/V tile is assembled from one box per page
 //            piece (min(B,128) rows) addressed through the block table; boxes
 //            past the request's keys use an out-of-range row and arrive
-//            zero-filled.
+//            zero-filled.  With several pieces per tile (B < 128) warps 8, 10
+//            and 11 share the copies and read the table one tile ahead.
 //   warp 9   owns TMEM (512 columns: S_A, S_B, O_A, O_B, 128 each) and issues
 //            every tcgen05.mma: S_X = Q_X K^T (both operands K-major in shared
 //            memory), O_X += P_X V with P_X read from TMEM (the bf16 P tile
