@@ -123,30 +123,18 @@ def test_single_query_equals_decode():
 
 @pytest.mark.parametrize("cfg", [5, 4])
 def test_config_prefill(cfg):
-    """Workload step: write the new tokens, then prefill.  Workload 5 is
-    compared on every row; workload 4 on sampled rows of every request (tile
-    edges, first/last rows and a stride) and every head."""
+    """Workload step: write the new tokens, then prefill, compared with the
+    oracle on every query row and head (workload 4: 17,928 rows, a few seconds
+    of the multi-threaded oracle)."""
     step = W.config(cfg)
     dev = DevStep(step)
     dev.write()
     out = dev.prefill()
     torch.cuda.synchronize()
     _, kc, vc = oracle_write(step)
-    got = widen(out)
-    if cfg == 5:
-        rows = None
-    else:
-        rows = []
-        for r in range(step.n_prefill):
-            a, b = int(step.cu_q[r]), int(step.cu_q[r + 1])
-            cand = {a, b - 1, a + 1, b - 2} | set(range(a, b, 61))
-            cand |= {a + t for t in (127, 128, 255, 256, 1023, 1024) if a + t < b}
-            rows += sorted(x for x in cand if a <= x < b)
-        rows = np.array(rows, np.int32)
     want = oracle.prefill(step.q_prefill, kc, vc, step.cu_q, step.cu_k, step.scale, causal=True,
-                          block_table=step.prefill_table, block_size=step.block_size,
-                          row_subset=rows)
-    assert_close(got if rows is None else got[rows], want, "bf16", f"cfg{cfg}")
+                          block_table=step.prefill_table, block_size=step.block_size)
+    assert_close(widen(out), want, "bf16", f"cfg{cfg}")
     assert pkv.paged_error_flags() == 0
 
 
