@@ -84,8 +84,7 @@ def test_parts_alone():
     want_d = oracle.decode(step.q_decode, okc, ovc, step.decode_table, step.cache_seqlens,
                            step.scale)
     assert_close(widen(dout), want_d, "bf16", "decode part")
-    rows = np.arange(0, int(step.cu_q[-1]), 37, dtype=np.int32)
     want_p = oracle.prefill(step.q_prefill, okc, ovc, step.cu_q, step.cu_k, step.scale,
                             causal=True, block_table=step.prefill_table,
-                            block_size=step.block_size, row_subset=rows)
-    assert_close(widen(pout)[rows], want_p, "bf16", "prefill part")
+                            block_size=step.block_size)
+    assert_close(widen(pout), want_p, "bf16", "prefill part")
