@@ -62,6 +62,38 @@ def test_host_side_argument_checks(lib):
     assert lib.paged_kv_write(None, None, 1, None, 1, None, None, ctypes.byref(huge), None) == -2
 
 
+def test_host_side_checks_of_the_step_calls(lib):
+    """Shared-prefix decode, decode with append, prefill, the mixed step and
+    the block copies reject bad arguments (-1) and unsupported combinations
+    (-2) before any CUDA call, and accept empty work (0).  Pointer arguments
+    are a non-null dummy: the host checks never dereference them."""
+    g = ctypes.byref(pkv.Geom(16, 8, 128, 16, 100, pkv.PKV_BF16))
+    f32 = ctypes.byref(pkv.Geom(16, 8, 128, 16, 100, pkv.PKV_F32))
+    d64 = ctypes.byref(pkv.Geom(16, 8, 64, 16, 100, pkv.PKV_BF16))
+    p = ctypes.c_void_p(256)
+    shared = lib.paged_decode_shared_prefix
+    assert shared(p, p, p, p, 4, p, 2, p, p, 0, 1, 1.0, p, p, 0, g, None) == -1  # no groups
+    assert shared(None, p, p, p, 4, p, 2, p, p, 1, 2, 1.0, p, p, 0, g, None) == -1  # q null
+    assert shared(p, p, p, p, 4, p, 2, p, p, 1, 2, 1.0, p, p, 0, f32, None) == -2  # bf16 only
+    assert shared(None, None, None, None, 4, None, 0, None, None, 0, 0, 1.0, None, None, 0, g,
+                  None) == 0  # empty batch
+    append = lib.paged_decode_append
+    assert append(None, p, p, p, p, p, 4, p, 2, 1.0, p, p, 0, g, None) == -1
+    assert append(None, None, None, None, None, None, 4, None, 0, 1.0, None, None, 0, g, None) == 0
+    prefill = lib.paged_varlen_prefill
+    assert prefill(None, p, p, p, p, 2, 4, 4, p, 4, 1, 1.0, p, None, 0, g, None) == -1
+    assert prefill(p, p, p, p, p, 2, 4, 4, p, 4, 1, 1.0, p, None, 0, f32, None) == -2
+    assert prefill(p, p, p, p, p, 2, 4, 4, p, 4, 1, 1.0, p, None, 0, d64, None) == -2
+    assert prefill(None, None, None, None, None, 0, 0, 0, None, 4, 1, 1.0, None, None, 0, g,
+                   None) == 0
+    assert lib.paged_mixed_step(None, p, p, None, 0, g, None) == -1
+    assert lib.paged_copy_blocks(p, p, p, p, -1, g, None) == -1
+    assert lib.paged_copy_blocks(p, p, None, p, 3, g, None) == -1
+    assert lib.paged_copy_blocks(p, p, p, p, 70000, g, None) == -2
+    assert lib.paged_copy_blocks(None, None, None, None, 0, g, None) == 0
+    assert lib.paged_decode_noalloc(None, None, None, None, 4, None, 0, 1.0, None, g, None) == 0
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not found"):
         pkv.load_library(str(tmp_path / "missing.so"))
