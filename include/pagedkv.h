@@ -194,8 +194,8 @@ size_t paged_varlen_prefill_workspace_size(int32_t batch, int32_t max_seqlen_q,
  * * geom->block_size (any factorisation, e.g. block_size 1), and request r's
  * keys are rows cu_seqlens_k[r] .. cu_seqlens_k[r+1]-1; max_blocks_per_seq is
  * ignored.  Keys past row `rows` are flagged PKV_FLAG_BAD_LENGTH.
- * Supported: bf16, head_dim 128, Hq/Hkv in {1, 2, 4, 8, ...}; paged mode: a
- * block_size that is a multiple of 128 or divides 128 and is >= 8.
+ * Supported: bf16, head_dim 64 or 128, Hq/Hkv in {1, 2, 4, 8, ...}; paged
+ * mode: a block_size that is a multiple of 128 or divides 128 and is >= 8.
  */
 int paged_varlen_prefill(const void* q, const void* k_cache, const void* v_cache,
                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,

@@ -197,7 +197,8 @@ int paged_varlen_prefill(const void* q, const void* k_cache, const void* v_cache
         return PKV_ERR_INVALID;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
         return PKV_ERR_INVALID;
-    if (geom->dtype != PKV_BF16 || geom->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (geom->dtype != PKV_BF16 || (geom->head_dim != 128 && geom->head_dim != 64))
+        return PKV_ERR_UNSUPPORTED;
     const size_t need = pkv::prefill_workspace_bytes(batch, max_seqlen_q, geom->num_heads);
     if (need && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
         return PKV_ERR_WORKSPACE;

@@ -72,8 +72,7 @@ namespace pkv {
 namespace {
 
 constexpr int BM = 128;  // query rows per Q tile
-constexpr int BN = 128;  // keys per K/V tile
-constexpr int HD = 128;  // head_dim
+constexpr int BN = 128;  // keys per K/V tile (head_dim HD is a template parameter: 64 or 128)
 constexpr int SK = 3;    // K ring depth
 constexpr int SV = 2;    // V ring depth
 constexpr int kThreads = 384;  // 8 softmax warps, TMA warp, MMA warp, 2 spare
@@ -85,27 +84,34 @@ constexpr int kRegsLow = 88;
 constexpr int kRegsHigh = 208;
 static_assert(8 * kRegsHigh + 4 * kRegsLow <= 12 * 168, "register split exceeds the launch");
 constexpr int kTmemCols = 512;
-constexpr uint32_t kTileBytes = BN * HD * 2;  // 32 KiB: one Q, K or V tile
 constexpr uint32_t kRegionBytes = BN * 128;   // 16 KiB: 64 dims (128 B) x 128 rows
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // rescale when the row max grows by > 2^8
 
 
-// shared memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t OFF_Q = 0;  // Q_A, Q_B
-constexpr uint32_t OFF_K = OFF_Q + 2 * kTileBytes;
-constexpr uint32_t OFF_V = OFF_K + SK * kTileBytes;
-constexpr uint32_t OFF_BAR = OFF_V + SV * kTileBytes;
 constexpr uint32_t BAR_BYTES = 256;
-constexpr size_t kSmemBytes = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
 
-// instruction descriptors: D fp32, A/B bf16, M = N = 128
-constexpr uint32_t idesc(uint32_t b_mn_major) {
+// instruction descriptors: D fp32, A/B bf16, M = 128, N = n
+constexpr uint32_t idesc(uint32_t b_mn_major, int n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (b_mn_major << 16) |
-           ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
-constexpr uint32_t IDESC_QK = idesc(0);
-constexpr uint32_t IDESC_PV = idesc(1);
+constexpr uint32_t IDESC_QK = idesc(0, BN);  // S = Q K^T: N = 128 keys
+
+// Per head_dim: a Q, K or V tile is 128 rows of HD bf16 in HD / 64 swizzled
+// 128-byte regions; the shared memory map (offsets from a 1024-byte aligned
+// base) and the PV descriptor (N = HD).
+template <int HD>
+struct Shape {
+    static_assert(HD == 64 || HD == 128, "head_dim 64 or 128");
+    static constexpr uint32_t kTileBytes = BN * HD * 2;  // 16 or 32 KiB
+    static constexpr uint32_t OFF_Q = 0;                 // Q_A, Q_B
+    static constexpr uint32_t OFF_K = OFF_Q + 2 * kTileBytes;
+    static constexpr uint32_t OFF_V = OFF_K + SK * kTileBytes;
+    static constexpr uint32_t OFF_BAR = OFF_V + SV * kTileBytes;
+    static constexpr size_t kSmemBytes = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
+    static constexpr uint32_t IDESC_PV = idesc(1, HD);
+};
 
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -264,7 +270,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsign
 // kExt: the per-request key counts / table rows, key chunks and log2-sum-exp
 // output of PrefillArgs are in use (a separate instantiation, so the plain
 // prefill compiles without them)
-template <bool kExt>
+template <bool kExt, int HD>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_o,
@@ -273,7 +279,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    using Sh = Shape<HD>;
+    constexpr uint32_t kTileBytes = Sh::kTileBytes;
+    constexpr uint32_t OFF_Q = Sh::OFF_Q, OFF_K = Sh::OFF_K, OFF_V = Sh::OFF_V;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Sh::OFF_BAR);
     uint64_t* k_full = bars;             // [SK]
     uint64_t* k_empty = k_full + SK;     // [SK]
     uint64_t* v_full = k_empty + SK;     // [SV]
@@ -447,7 +456,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     unsigned char* qd = sm + OFF_Q + x * kTileBytes;
                     const int hh = pick(thead, x), row = pick(tbox, x);
                     tma_load_3d(qd, &tmap_q, 0, hh, row, q_ready);
-                    tma_load_3d(qd + kRegionBytes, &tmap_q, 64, hh, row, q_ready);
+                    if constexpr (HD > 64)
+                        tma_load_3d(qd + kRegionBytes, &tmap_q, 64, hh, row, q_ready);
                 }
             }
             int32_t e_cur = entry(0);
@@ -466,7 +476,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     unsigned char* kd =
                         sm + OFF_K + sk * kTileBytes + piece_of_lane * a.piece * 128;
                     tma_load_3d(kd, &tmap_k, 0, kvh, my_row, &k_full[sk]);
-                    tma_load_3d(kd + kRegionBytes, &tmap_k, 64, kvh, my_row, &k_full[sk]);
+                    if constexpr (HD > 64)
+                        tma_load_3d(kd + kRegionBytes, &tmap_k, 64, kvh, my_row, &k_full[sk]);
                 }
                 ++issued;
                 if (lane == 0) {
@@ -478,7 +489,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     unsigned char* vd =
                         sm + OFF_V + sv * kTileBytes + piece_of_lane * a.piece * 128;
                     tma_load_3d(vd, &tmap_v, 0, kvh, my_row, &v_full[sv]);
-                    tma_load_3d(vd + kRegionBytes, &tmap_v, 64, kvh, my_row, &v_full[sv]);
+                    if constexpr (HD > 64)
+                        tma_load_3d(vd + kRegionBytes, &tmap_v, 64, kvh, my_row, &v_full[sv]);
                 }
                 ++issued_v;
             }
@@ -512,7 +524,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 unsigned char* qd = sm + OFF_Q + x * kTileBytes;
                 const int hh = pick(thead, x), row = pick(tbox, x);
                 tma_load_3d(qd, &tmap_q, 0, hh, row, q_ready);
-                tma_load_3d(qd + kRegionBytes, &tmap_q, 64, hh, row, q_ready);
+                if constexpr (HD > 64)
+                    tma_load_3d(qd + kRegionBytes, &tmap_q, 64, hh, row, q_ready);
             }
             for (int j = 0; j < n_tiles; ++j) {
                 const int sk = j % SK, sv = j % SV;
@@ -522,7 +535,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     const int32_t row = page_row(j * BN + p * a.piece);
                     unsigned char* kd = sm + OFF_K + sk * kTileBytes + p * a.piece * 128;
                     tma_load_3d(kd, &tmap_k, 0, kvh, row, &k_full[sk]);
-                    tma_load_3d(kd + kRegionBytes, &tmap_k, 64, kvh, row, &k_full[sk]);
+                    if constexpr (HD > 64)
+                        tma_load_3d(kd + kRegionBytes, &tmap_k, 64, kvh, row, &k_full[sk]);
                 }
                 ++issued;
                 if (!mbar_wait(&v_empty[sv], ((j / SV) & 1) ^ 1, a.err)) break;
@@ -531,7 +545,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     const int32_t row = page_row(j * BN + p * a.piece);
                     unsigned char* vd = sm + OFF_V + sv * kTileBytes + p * a.piece * 128;
                     tma_load_3d(vd, &tmap_v, 0, kvh, row, &v_full[sv]);
-                    tma_load_3d(vd + kRegionBytes, &tmap_v, 64, kvh, row, &v_full[sv]);
+                    if constexpr (HD > 64)
+                        tma_load_3d(vd + kRegionBytes, &tmap_v, 64, kvh, row, &v_full[sv]);
                 }
                 ++issued_v;
             }
@@ -570,7 +585,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 const uint32_t vb = v_lo0 + sv * (kTileBytes >> 4);
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k)
-                    mma_ts(tm_o[x], tm_s[x] + k * 8, vb + k * (2048 >> 4), IDESC_PV,
+                    mma_ts(tm_o[x], tm_s[x] + k * 8, vb + k * (2048 >> 4), Sh::IDESC_PV,
                            (!first || k > 0) ? 1u : 0u);
                 if (last) mma_commit(&o_ready[x]);
             };
@@ -735,7 +750,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 if (key0 + t >= k_len) {
                     unsigned char* vs = sm + OFF_V + sv * kTileBytes;
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
+                    for (int c = 0; c < HD / 8; ++c)
                         *reinterpret_cast<uint4*>(vs + swz(t, c)) = make_uint4(0, 0, 0, 0);
                 }
                 fence_async_smem();
@@ -778,14 +793,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
             // a full tile: two TMA boxes (64 dims x 128 rows each)
             if (t == 0) {
                 tma_store_3d(&tmap_o, stage, 0, h, (int32_t)out_row0);
-                tma_store_3d(&tmap_o, stage + kRegionBytes, 64, h, (int32_t)out_row0);
+                if constexpr (HD > 64)
+                    tma_store_3d(&tmap_o, stage + kRegionBytes, 64, h, (int32_t)out_row0);
                 asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                 asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             }
         } else if (ok) {
 #pragma unroll 4
             for (int i = t; i < BM * (HD / 8); i += 128) {
-                const int rr = i >> 4, c = i & 15;
+                const int rr = i / (HD / 8), c = i % (HD / 8);
                 if (rr >= shift)
                     *reinterpret_cast<uint4*>(a.out + ((out_row0 + rr - shift) * a.hq + h) * HD +
                                               c * 8) =
@@ -826,14 +842,15 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [rows, heads, 128] bf16 viewed as 3-D (dim, head, row); box (64 dims, 1
+// [rows, heads, hd] bf16 viewed as 3-D (dim, head, row); box (64 dims, 1
 // head, piece rows), 128-byte swizzle.  Serves the K/V pools (rows = slots)
 // and q (rows = query tokens, piece = 128).
-bool make_rows_map(CUtensorMap* map, const void* base, int hkv, int64_t rows, int piece) {
+bool make_rows_map(CUtensorMap* map, const void* base, int hkv, int64_t rows, int piece,
+                   int hd) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)hkv, (cuuint64_t)rows};
-    cuuint64_t strides[2] = {(cuuint64_t)HD * 2, (cuuint64_t)hkv * HD * 2};
+    cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)hkv, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)hkv * hd * 2};
     cuuint32_t box[3] = {64, 1, (cuuint32_t)piece};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
@@ -856,14 +873,16 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
                            cudaStream_t stream, const PrefillExtra* ex) {
     (void)max_seqlen_k;
     (void)workspace;
-    if (d != HD) return cudaErrorNotSupported;
+    // head_dim 128, or 64 for the plain prefill
+    if (!(d == 128 || (d == 64 && !ex))) return cudaErrorNotSupported;
+    const size_t smem = d == 128 ? Shape<128>::kSmemBytes : Shape<64>::kSmemBytes;
     // a TMA box of min(B,128) rows must tile 128 keys on 1024-byte boundaries
     // (packed K/V: one 128-row box per tile, any block_size)
     const bool packed = block_table == nullptr;
     const bool b_ok = packed || ((block_size >= 128) ? (block_size % 128 == 0)
                                                      : (block_size >= 8 && 128 % block_size == 0));
     if (!b_ok || batch > 65535 || hq > 65535) return cudaErrorNotSupported;
-    if (dev.max_smem_optin < kSmemBytes) return cudaErrorNotSupported;
+    if (dev.max_smem_optin < smem) return cudaErrorNotSupported;
     const int64_t rows = num_blocks * block_size;
     if (rows + 128 > 0x7fffffffLL) return cudaErrorNotSupported;
     const int piece = (packed || block_size >= BN) ? BN : block_size;
@@ -876,9 +895,9 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
     // output rows: kchunks stacked outputs of chunk_rows rows each
     const int64_t o_rows =
         kchunks > 1 ? std::min<int64_t>((int64_t)kchunks * ex->chunk_rows, 0x7fffffffLL) : q_rows;
-    if (!make_rows_map(&mq, q, hq, q_rows, BM) || !make_rows_map(&mo, out, hq, o_rows, BM) ||
-        !make_rows_map(&mk, k_cache, hkv, rows, piece) ||
-        !make_rows_map(&mv, v_cache, hkv, rows, piece))
+    if (!make_rows_map(&mq, q, hq, q_rows, BM, d) || !make_rows_map(&mo, out, hq, o_rows, BM, d) ||
+        !make_rows_map(&mk, k_cache, hkv, rows, piece, d) ||
+        !make_rows_map(&mv, v_cache, hkv, rows, piece, d))
         return cudaErrorInvalidValue;
     PrefillArgs a;
     a.out = static_cast<uint16_t*>(out);
@@ -905,9 +924,10 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
     a.oob_row = (int32_t)rows;
     a.tiles_q = (max_seqlen_q + BM - 1) / BM;
     a.causal = causal ? 1 : 0;
-    auto kern = ex ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+    auto kern = ex ? prefill_tc_kernel<true, 128>
+                   : (d == 128 ? prefill_tc_kernel<false, 128> : prefill_tc_kernel<false, 64>);
     cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.pair_tiles ? (a.tiles_q + 1) / 2 : a.tiles_q, a.pair_heads ? (hq + 1) / 2 : hq,
               batch * a.kchunks);
@@ -918,7 +938,7 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -927,7 +947,7 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
         cfg.numAttrs = 1;
         return cudaLaunchKernelEx(&cfg, kern, mq, mo, mk, mv, a);
     }
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(mq, mo, mk, mv, a);
+    kern<<<grid, kThreads, smem, stream>>>(mq, mo, mk, mv, a);
     return cudaGetLastError();
 }
 

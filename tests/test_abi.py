@@ -69,7 +69,7 @@ def test_host_side_checks_of_the_step_calls(lib):
     are a non-null dummy: the host checks never dereference them."""
     g = ctypes.byref(pkv.Geom(16, 8, 128, 16, 100, pkv.PKV_BF16))
     f32 = ctypes.byref(pkv.Geom(16, 8, 128, 16, 100, pkv.PKV_F32))
-    d64 = ctypes.byref(pkv.Geom(16, 8, 64, 16, 100, pkv.PKV_BF16))
+    d96 = ctypes.byref(pkv.Geom(16, 8, 96, 16, 100, pkv.PKV_BF16))
     p = ctypes.c_void_p(256)
     shared = lib.paged_decode_shared_prefix
     assert shared(p, p, p, p, 4, p, 2, p, p, 0, 1, 1.0, p, p, 0, g, None) == -1  # no groups
@@ -83,7 +83,7 @@ def test_host_side_checks_of_the_step_calls(lib):
     prefill = lib.paged_varlen_prefill
     assert prefill(None, p, p, p, p, 2, 4, 4, p, 4, 1, 1.0, p, None, 0, g, None) == -1
     assert prefill(p, p, p, p, p, 2, 4, 4, p, 4, 1, 1.0, p, None, 0, f32, None) == -2
-    assert prefill(p, p, p, p, p, 2, 4, 4, p, 4, 1, 1.0, p, None, 0, d64, None) == -2
+    assert prefill(p, p, p, p, p, 2, 4, 4, p, 4, 1, 1.0, p, None, 0, d96, None) == -2
     assert prefill(None, None, None, None, None, 0, 0, 0, None, 4, 1, 1.0, None, None, 0, g,
                    None) == 0
     assert lib.paged_mixed_step(None, p, p, None, 0, g, None) == -1

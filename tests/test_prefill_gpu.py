@@ -85,6 +85,20 @@ def test_gqa_groups(hq, hkv):
     assert_close(widen(run_gpu(c)), run_oracle(c), "bf16", f"{hq}/{hkv}")
 
 
+@pytest.mark.parametrize("hq,hkv,B", [(16, 8, 16), (8, 8, 256), (32, 8, 64)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_head_dim_64(hq, hkv, B, causal):
+    """head_dim 64: one 64-dim swizzled region per tile row, PV with N = 64;
+    with paired heads (16/8, 32/8) and paired query tiles (8/8)."""
+    qlens = [1, 127, 128, 129, 300, 700]
+    klens = [1, 300, 128, 500, 300, 900]
+    c = make_case(qlens, klens, B=B, hq=hq, hkv=hkv, d=64, seed=hq + B + int(causal))
+    out = run_gpu(c, causal)
+    torch.cuda.synchronize()
+    assert_close(widen(out), run_oracle(c, causal), "bf16", f"d64 {hq}/{hkv} B={B} {causal}")
+    assert pkv.paged_error_flags() == 0
+
+
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (12, 4)])
 @pytest.mark.parametrize("causal", [True, False])
 def test_query_tile_pairs(hq, hkv, causal):
@@ -181,7 +195,7 @@ def test_bad_block_id_is_flagged(B, entry):
 
 
 def test_unsupported_combinations():
-    c = make_case([4], [4], B=16, d=64, seed=1)
+    c = make_case([4], [4], B=16, d=96, seed=1)
     with pytest.raises(pkv.PagedKVError) as e:
         run_gpu(c)
     assert e.value.status == -2
