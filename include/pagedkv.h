@@ -253,8 +253,8 @@ int paged_decode_shared_prefix(const void* q, const void* k_cache, const void* v
  * programmatic dependents of the prefill kernel, which they do not read: they
  * start on SMs the prefill leaves free instead of after it.  Arguments mean
  * what they mean in the single calls; all pointers in the struct are DEVICE
- * pointers.  Supported as the single calls; with a prefill part or groups:
- * bf16 and head_dim 128.  workspace: at least
+ * pointers.  Supported as the single calls; with a prefill part: bf16 and
+ * head_dim 64 or 128; with groups: bf16 and head_dim 128.  workspace: at least
  * paged_mixed_step_workspace_size(decode_batch, geom) bytes, 256-byte aligned.
  */
 typedef struct pkv_mixed_step {

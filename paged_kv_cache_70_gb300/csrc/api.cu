@@ -308,8 +308,9 @@ int paged_mixed_step(const pkv_mixed_step* s, void* k_cache, void* v_cache, void
     const bool dec = s->decode_batch > 0;
     const bool grp = dec && s->n_groups > 0;
     if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return PKV_ERR_INVALID;
-    if ((pf || grp) && (geom->dtype != PKV_BF16 || geom->head_dim != 128))
+    if (pf && (geom->dtype != PKV_BF16 || (geom->head_dim != 128 && geom->head_dim != 64)))
         return PKV_ERR_UNSUPPORTED;
+    if (grp && (geom->dtype != PKV_BF16 || geom->head_dim != 128)) return PKV_ERR_UNSUPPORTED;
     if (s->prefill_new_tokens > 0 &&
         (!s->prefill_k_new || !s->prefill_v_new || !s->prefill_slots))
         return PKV_ERR_INVALID;

@@ -34,6 +34,35 @@ def split_step(step):
     return dec_rows, pf_rows, slots
 
 
+def test_head_dim_64_without_groups():
+    """A step with head_dim 64 (prefill part on the head_dim-64 tensor-core
+    kernel, decode with append), no shared prefixes."""
+    step = W.make_step(name="mix64", dtype="bf16", hq=16, hkv=8, d=64, block_size=16,
+                       decode_lens=[5, 300, 1000, 16], prefill_q=[200, 1, 129],
+                       prefill_cached=[0, 64, 300], seed=64)
+    dec_rows, pf_rows, slots = split_step(step)
+    kc, vc = to_dev(step.k_cache), to_dev(step.v_cache)
+    decode = dict(q=to_dev(step.q_decode), k_new=to_dev(step.new_k[dec_rows]),
+                  v_new=to_dev(step.new_v[dec_rows]), table=to_dev(step.decode_table.copy()),
+                  seqlens=to_dev(step.cache_seqlens - 1))
+    prefill = dict(k_new=to_dev(step.new_k[pf_rows]), v_new=to_dev(step.new_v[pf_rows]),
+                   slots=to_dev(slots[pf_rows]), q=to_dev(step.q_prefill), cu_q=to_dev(step.cu_q),
+                   cu_k=to_dev(step.cu_k), max_q=step.max_seqlen_q, max_k=step.max_seqlen_k,
+                   table=to_dev(step.prefill_table.copy()))
+    pout, dout = pkv.paged_mixed_step(kc, vc, step.scale, prefill=prefill, decode=decode)
+    torch.cuda.synchronize()
+    _, okc, ovc = oracle_write(step)
+    assert np.array_equal(to_host(kc), okc) and np.array_equal(to_host(vc), ovc)
+    want_d = oracle.decode(step.q_decode, okc, ovc, step.decode_table, step.cache_seqlens,
+                           step.scale)
+    assert_close(widen(dout), want_d, "bf16", "d64 mixed decode")
+    want_p = oracle.prefill(step.q_prefill, okc, ovc, step.cu_q, step.cu_k, step.scale,
+                            causal=True, block_table=step.prefill_table,
+                            block_size=step.block_size)
+    assert_close(widen(pout), want_p, "bf16", "d64 mixed prefill")
+    assert pkv.paged_error_flags() == 0
+
+
 @pytest.mark.parametrize("grouped", [True, False])
 def test_continuous_batching_step(grouped):
     step = W.config(5)
