@@ -222,7 +222,7 @@ int paged_varlen_prefill(const void* q, const void* k_cache, const void* v_cache
  * prefix part is the attention of the group's queries over the prefix keys
  * (one pass over them, on the tensor cores), the rest the decode of each
  * sequence's own keys, merged with §11.2's boxed rule.
- * Supported: bf16, head_dim 128, Hq/Hkv in {1, 2, 4}, block_size a multiple of
+ * Supported: bf16, head_dim 64 or 128, Hq/Hkv in {1, 2, 4}, block_size a multiple of
  * 128 or a divisor of 128 (>= 8).  workspace: at least
  * paged_decode_shared_prefix_workspace_size(batch, geom) bytes, 256-byte
  * aligned.  A prefix length that is negative, longer than a member's keys or
@@ -253,8 +253,8 @@ int paged_decode_shared_prefix(const void* q, const void* k_cache, const void* v
  * programmatic dependents of the prefill kernel, which they do not read: they
  * start on SMs the prefill leaves free instead of after it.  Arguments mean
  * what they mean in the single calls; all pointers in the struct are DEVICE
- * pointers.  Supported as the single calls; with a prefill part: bf16 and
- * head_dim 64 or 128; with groups: bf16 and head_dim 128.  workspace: at least
+ * pointers.  Supported as the single calls; with a prefill part or groups:
+ * bf16 and head_dim 64 or 128.  workspace: at least
  * paged_mixed_step_workspace_size(decode_batch, geom) bytes, 256-byte aligned.
  */
 typedef struct pkv_mixed_step {

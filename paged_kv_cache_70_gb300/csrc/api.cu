@@ -247,7 +247,8 @@ int paged_decode_shared_prefix(const void* q, const void* k_cache, const void* v
         return PKV_ERR_INVALID;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
         return PKV_ERR_INVALID;
-    if (geom->dtype != PKV_BF16 || geom->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (geom->dtype != PKV_BF16 || (geom->head_dim != 128 && geom->head_dim != 64))
+        return PKV_ERR_UNSUPPORTED;
     DeviceInfo dev;
     if (pkv::current_device_info(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     pkv::DecodePlan plan;
@@ -308,9 +309,9 @@ int paged_mixed_step(const pkv_mixed_step* s, void* k_cache, void* v_cache, void
     const bool dec = s->decode_batch > 0;
     const bool grp = dec && s->n_groups > 0;
     if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return PKV_ERR_INVALID;
-    if (pf && (geom->dtype != PKV_BF16 || (geom->head_dim != 128 && geom->head_dim != 64)))
+    if ((pf || grp) &&
+        (geom->dtype != PKV_BF16 || (geom->head_dim != 128 && geom->head_dim != 64)))
         return PKV_ERR_UNSUPPORTED;
-    if (grp && (geom->dtype != PKV_BF16 || geom->head_dim != 128)) return PKV_ERR_UNSUPPORTED;
     if (s->prefill_new_tokens > 0 &&
         (!s->prefill_k_new || !s->prefill_v_new || !s->prefill_slots))
         return PKV_ERR_INVALID;

@@ -873,8 +873,7 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
                            cudaStream_t stream, const PrefillExtra* ex) {
     (void)max_seqlen_k;
     (void)workspace;
-    // head_dim 128, or 64 for the plain prefill
-    if (!(d == 128 || (d == 64 && !ex))) return cudaErrorNotSupported;
+    if (d != 128 && d != 64) return cudaErrorNotSupported;
     const size_t smem = d == 128 ? Shape<128>::kSmemBytes : Shape<64>::kSmemBytes;
     // a TMA box of min(B,128) rows must tile 128 keys on 1024-byte boundaries
     // (packed K/V: one 128-row box per tile, any block_size)
@@ -924,7 +923,7 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
     a.oob_row = (int32_t)rows;
     a.tiles_q = (max_seqlen_q + BM - 1) / BM;
     a.causal = causal ? 1 : 0;
-    auto kern = ex ? prefill_tc_kernel<true, 128>
+    auto kern = ex ? (d == 128 ? prefill_tc_kernel<true, 128> : prefill_tc_kernel<true, 64>)
                    : (d == 128 ? prefill_tc_kernel<false, 128> : prefill_tc_kernel<false, 64>);
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -118,3 +118,16 @@ def test_group_sizes(hq, hkv):
     want = oracle.decode(q, kc, vc, table, lens, scale)
     assert_close(widen(out), want, "bf16", f"{hq}/{hkv}")
     assert pkv.paged_error_flags() == 0
+
+
+def test_head_dim_64():
+    """head_dim 64: the prefix pass on the head_dim-64 tensor-core kernel."""
+    rng = np.random.default_rng(64)
+    q, kc, vc, table, lens, gcu, plen = build_groups(rng, [5, 40], [128, 512], 300, 16, d=64)
+    scale = 1 / math.sqrt(64)
+    out = pkv.paged_decode_shared_prefix(to_dev(q), to_dev(kc), to_dev(vc), to_dev(table),
+                                         to_dev(lens), to_dev(gcu), to_dev(plen), 40, scale)
+    torch.cuda.synchronize()
+    want = oracle.decode(q, kc, vc, table, lens, scale)
+    assert_close(widen(out), want, "bf16", "head_dim 64")
+    assert pkv.paged_error_flags() == 0
