@@ -1,12 +1,25 @@
 #!/usr/bin/env python
 """Benchmark of the paged KV-cache hot path on GB300.
 
-One decode step of the long-context workload (write the new token of every
-sequence through slot_mapping, then paged decode with split-KV over 16K-40K
-cached keys; batch 8, GQA 16/8, head_dim 128, block 256, bf16) is the headline
-(decode KV GB/s); the same run also measures one chunked-prefill step of the
-varlen workload (write 16 requests' new tokens, then causal varlen prefill over
-cached + new keys; TFLOP/s of the visible query-key pairs).
+The headline is one decode step of the long-context workload (batch 8,
+16K-40K cached keys, GQA 16/8, head_dim 128, block 256, bf16): every
+sequence's new token is written into the cache and attended to together with
+the cached keys in one paged_decode_append call (the kvcache call of "Sayfalı
+dikkat"), reported as decode KV GB/s.  The same run measures, each as a
+sub-object of the JSON line:
+
+  decode_qwen3            the Qwen3-0.6B-shaped decode (batch 64, L~U[128,4096],
+                          block 16), the same one-call step;
+  decode_separate_write   the headline step as slot_mapping build + write +
+                          paged_decode (four launches);
+  kv_write                the slot_mapping write of the chunked-prefill
+                          workload's 17,928 new rows (paged_kv_write alone);
+  prefill                 one chunked-prefill step (write the new rows, then
+                          causal varlen prefill; TFLOP/s of visible pairs), and
+  prefill_contiguous      the same attention over packed K/V;
+  copy_blocks             the copy-on-write block copies;
+  decode_shared_prefix    the decode half of the continuous-batching workload;
+  mixed_step              the whole continuous-batching step in one call.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -14,13 +27,16 @@ Prints one JSON line.  With torchrun (N > 1) every rank runs its own replica of
 the workload on its own GPU (no collective on the data path; "replicas only"),
 and timing is the max over ranks.  ``--impl reference`` times the CPU oracle (the
 reference arm of this build) on a bounded sample of the same workload.
+
+Between timed steps L2 is flushed (untimed): a 256 MiB buffer is written and
+then another 256 MiB buffer is read, so that the dirty lines of the write go
+back to HBM before the next timed step starts instead of inside it.
 """
 from __future__ import annotations
 
 import argparse
 import ctypes
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -35,7 +51,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode KV GB/s & % HBM peak; varlen prefill TFLOP/s & % bf16 peak"
-DECODE_CFG, PREFILL_CFG = 3, 4
+DECODE_CFG, QWEN_CFG, PREFILL_CFG, MIXED_CFG = 3, 2, 4, 5
+PARTS = ("all", "decode", "qwen3", "write", "prefill", "copy", "shared", "mixed")
 
 
 def parse_args():
@@ -45,10 +62,11 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--only", choices=["all", "decode", "prefill", "copy", "shared", "mixed"],
-                   default="all",
-                   help="measure one half only (profiling runs)")
-    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    p.add_argument("--only", choices=PARTS, default="all",
+                   help="measure one part only (profiling runs)")
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end passes")
+    p.add_argument("--no-soak", action="store_true",
+                   help="skip the untimed clock-sampling passes (a fixed launch count for ncu)")
     return p.parse_args()
 
 
@@ -99,12 +117,29 @@ def decode_kernel_bytes(step) -> int:
     return kv + qo + table + step.n_decode * 4
 
 
+def decode_append_bytes(step) -> int:
+    """Bytes paged_decode_append must move: K and V of every cached key, the
+    new token's K and V rows read and written once, q, out, the block-table
+    entries of every page touched, and cache_seqlens."""
+    L = step.cache_seqlens.astype(np.int64) - 1  # keys cached before the step
+    row = step.kv_dim * step.elt * 2              # K + V of one key
+    qo = 2 * step.n_decode * step.hq * step.d * step.elt
+    table = int(np.sum(-(-(L + 1) // step.block_size))) * 4
+    return int(L.sum()) * row + 2 * step.n_decode * row + qo + table + step.n_decode * 4
+
+
+def slot_build_bytes(step) -> int:
+    """paged_build_slot_mapping: token_seq, token_pos and one table entry read,
+    the slot written, per row."""
+    return len(step.token_seq) * 16
+
+
 def write_bytes(step) -> int:
-    """slot_mapping build (token_seq, token_pos read, slot written) and the
-    K/V rows of every non-padding token read and written once."""
+    """paged_kv_write: the slot of every row read; K and V of every non-padding
+    row read once and written once."""
     n_rows = len(step.token_seq)
     n_real = int((step.token_seq >= 0).sum())
-    return n_rows * 12 + n_real * 4 + n_real * step.kv_dim * step.elt * 2 * 2 + n_rows * 4
+    return n_rows * 4 + n_real * step.kv_dim * step.elt * 2 * 2
 
 
 def prefill_pairs(step) -> int:
@@ -161,6 +196,7 @@ class Clocks:
         os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
         def num(x):
             try:
                 return float(x)
@@ -176,7 +212,7 @@ class Clocks:
 
 
 # ---------------------------------------------------------------------------
-# device-side workload
+# device-side workloads
 # ---------------------------------------------------------------------------
 def to_dev(a: np.ndarray) -> torch.Tensor:
     if a.dtype == np.uint16:
@@ -192,105 +228,175 @@ def pinned(a: np.ndarray) -> torch.Tensor:
     return t.pin_memory()
 
 
-class DeviceStep:
-    """Device-resident copy of a synthetic step and the calls of one pass."""
+class L2Flush:
+    """Evicts the previous step from L2 (untimed): writes a 256 MiB buffer,
+    then reads another 256 MiB buffer so that the written lines are back in
+    HBM and L2 holds only clean lines of an unrelated buffer."""
+
+    def __init__(self):
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        self.r = torch.ones((256 << 20) // 8, dtype=torch.int64, device="cuda")
+        self.sink = torch.empty((), dtype=torch.int64, device="cuda")
+
+    def __call__(self, i: int):
+        self.w.fill_(i & 0xff)
+        torch.sum(self.r, dim=0, out=self.sink)
+
+
+class DecodeStep:
+    """A decode step with the in-place append, resident on the device: every
+    sequence's new token (k_new/v_new row b) is written at position
+    cache_seqlens[b] - 1 and attended to together with the cached keys in one
+    paged_decode_append call (split kernel + combine)."""
+
+    launches = 2
 
     def __init__(self, step, pkv):
-        self.s, self.pkv = step, pkv
-        self.table = to_dev(step.table)
-        self.k_cache = to_dev(step.k_cache)
-        self.v_cache = to_dev(step.v_cache)
-        self.new_k, self.new_v = to_dev(step.new_k), to_dev(step.new_v)
-        self.token_seq, self.token_pos = to_dev(step.token_seq), to_dev(step.token_pos)
-        self.slots = torch.empty(len(step.token_seq), dtype=torch.int32, device="cuda")
-        if step.n_decode:
-            self.q = to_dev(step.q_decode)
-            self.seqlens = to_dev(step.cache_seqlens)
-            self.dtable = self.table[: step.n_decode].contiguous()
-            self.out = torch.empty_like(self.q)
-            self.ws = torch.empty(max(1, pkv.paged_decode_workspace_size(
-                step.n_decode, step.hq, self.k_cache)), dtype=torch.uint8, device="cuda")
-        if step.n_prefill:
-            self.q = to_dev(step.q_prefill)
-            self.cu_q, self.cu_k = to_dev(step.cu_q), to_dev(step.cu_k)
-            self.ptable = self.table[step.n_decode:].contiguous()
-            self.out = torch.empty_like(self.q)
-            need = pkv.paged_varlen_prefill_workspace_size(step.n_prefill, step.max_seqlen_q,
-                                                          step.hq, self.k_cache)
-            self.ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
+        s = step
+        nd = s.n_decode
+        # the workloads put decode sequence b's new row first, in order
+        assert np.array_equal(s.token_seq[:nd], np.arange(nd))
+        assert np.array_equal(s.token_pos[:nd], s.cache_seqlens - 1)
+        self.s, self.pkv = s, pkv
+        self.host = {"q": s.q_decode, "k_new": s.new_k[:nd], "v_new": s.new_v[:nd],
+                     "table": s.decode_table, "seqlens": (s.cache_seqlens - 1).astype(np.int32)}
+        self.dev = {k: to_dev(v) for k, v in self.host.items()}
+        self.k_cache, self.v_cache = to_dev(s.k_cache), to_dev(s.v_cache)
+        self.out = torch.empty_like(self.dev["q"])
+        self.ws = torch.empty(max(1, pkv.paged_decode_workspace_size(nd, s.hq, self.k_cache)),
+                              dtype=torch.uint8, device="cuda")
 
-    def write(self):
-        pkv, s = self.pkv, self.s
-        pkv.paged_build_slot_mapping(self.table, self.token_seq, self.token_pos, s.block_size,
-                                     out=self.slots)
-        pkv.paged_kv_write(self.new_k, self.new_v, self.slots, self.k_cache, self.v_cache)
-
-    def attend(self):
-        pkv, s = self.pkv, self.s
-        if s.n_decode:
-            pkv.paged_decode(self.q, self.k_cache, self.v_cache, self.dtable, self.seqlens,
-                             s.scale, out=self.out, workspace=self.ws)
-        else:
-            pkv.paged_varlen_prefill(self.q, self.k_cache, self.v_cache, self.cu_q, self.cu_k,
-                                     s.max_seqlen_q, s.max_seqlen_k, self.ptable,
-                                     causal=s.causal, scale=s.scale, out=self.out,
+    def run(self, t=None):
+        t = self.dev if t is None else t
+        self.pkv.paged_decode_append(t["q"], t["k_new"], t["v_new"], self.k_cache, self.v_cache,
+                                     t["table"], t["seqlens"], self.s.scale, out=self.out,
                                      workspace=self.ws)
 
 
-def soak(dev: DeviceStep, seconds: float = 0.5):
+class WriteDecodeStep:
+    """The same decode step as three calls: slot_mapping build, paged_kv_write
+    of the new rows, paged_decode over the cached keys including the new one."""
+
+    def __init__(self, step, pkv):
+        s = step
+        self.s, self.pkv = s, pkv
+        self.table = to_dev(s.table)
+        self.dtable = self.table[: s.n_decode].contiguous()
+        self.k_cache, self.v_cache = to_dev(s.k_cache), to_dev(s.v_cache)
+        self.new_k, self.new_v = to_dev(s.new_k), to_dev(s.new_v)
+        self.token_seq, self.token_pos = to_dev(s.token_seq), to_dev(s.token_pos)
+        self.slots = torch.empty(len(s.token_seq), dtype=torch.int32, device="cuda")
+        self.q, self.seqlens = to_dev(s.q_decode), to_dev(s.cache_seqlens)
+        self.out = torch.empty_like(self.q)
+        self.ws = torch.empty(max(1, pkv.paged_decode_workspace_size(s.n_decode, s.hq,
+                                                                     self.k_cache)),
+                              dtype=torch.uint8, device="cuda")
+
+    def write(self):
+        self.pkv.paged_build_slot_mapping(self.table, self.token_seq, self.token_pos,
+                                          self.s.block_size, out=self.slots)
+        self.pkv.paged_kv_write(self.new_k, self.new_v, self.slots, self.k_cache, self.v_cache)
+
+    def attend(self):
+        self.pkv.paged_decode(self.q, self.k_cache, self.v_cache, self.dtable, self.seqlens,
+                              self.s.scale, out=self.out, workspace=self.ws)
+
+
+class PrefillStep:
+    """A chunked-prefill step resident on the device: slot_mapping build and
+    write of the requests' new rows, then causal varlen prefill over cached +
+    new keys through the block table."""
+
+    launches = 3
+
+    def __init__(self, step, pkv):
+        s = step
+        assert s.n_decode == 0
+        self.s, self.pkv = s, pkv
+        self.host = {"new_k": s.new_k, "new_v": s.new_v, "token_seq": s.token_seq,
+                     "token_pos": s.token_pos, "table": s.prefill_table, "q": s.q_prefill,
+                     "cu_q": s.cu_q, "cu_k": s.cu_k}
+        self.dev = {k: to_dev(v) for k, v in self.host.items()}
+        self.k_cache, self.v_cache = to_dev(s.k_cache), to_dev(s.v_cache)
+        self.slots = torch.empty(len(s.token_seq), dtype=torch.int32, device="cuda")
+        self.out = torch.empty_like(self.dev["q"])
+        need = pkv.paged_varlen_prefill_workspace_size(s.n_prefill, s.max_seqlen_q, s.hq,
+                                                      self.k_cache)
+        self.ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
+
+    def slot_build(self, t=None):
+        t = self.dev if t is None else t
+        self.pkv.paged_build_slot_mapping(t["table"], t["token_seq"], t["token_pos"],
+                                          self.s.block_size, out=self.slots)
+
+    def write(self, t=None):
+        t = self.dev if t is None else t
+        self.pkv.paged_kv_write(t["new_k"], t["new_v"], self.slots, self.k_cache, self.v_cache)
+
+    def attend(self, t=None):
+        t = self.dev if t is None else t
+        s = self.s
+        self.pkv.paged_varlen_prefill(t["q"], self.k_cache, self.v_cache, t["cu_q"], t["cu_k"],
+                                      s.max_seqlen_q, s.max_seqlen_k, t["table"],
+                                      causal=s.causal, scale=s.scale, out=self.out,
+                                      workspace=self.ws)
+
+    def run(self, t=None):
+        self.slot_build(t)
+        self.write(t)
+        self.attend(t)
+
+
+def time_parts(parts, steps: int, warmup: int, world: int, flush=None):
+    """Warm up, then time `steps` passes of the callables in `parts` (run in
+    order) with CUDA events on the current stream, an event between
+    consecutive parts.  Returns (mean ms of a pass, [(mean, median) per part])
+    with the pass mean taken as the max over ranks."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for f in parts:
+            f()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)]
+           for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush(i)
+        evs[i][0].record(stream)
+        for j, f in enumerate(parts):
+            f()
+            evs[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    total = max_over_ranks(float(np.mean([e[0].elapsed_time(e[-1]) for e in evs])), world)
+    per = []
+    for j in range(len(parts)):
+        ms = [e[j].elapsed_time(e[j + 1]) for e in evs]
+        per.append((max_over_ranks(float(np.mean(ms)), world), float(np.median(ms))))
+    return total, per
+
+
+def soak(fn, seconds: float = 0.5):
     """Keep running the same pass (untimed) so the clock sampler sees the GPU
     under this load for longer than the timed region itself lasts."""
     t_end = time.perf_counter() + seconds
     while time.perf_counter() < t_end:
         for _ in range(20):
-            dev.write()
-            dev.attend()
+            fn()
         torch.cuda.synchronize()
 
 
-def time_steps(dev: DeviceStep, steps: int, warmup: int, flush: torch.Tensor | None, world: int):
-    """Warm up, then time `steps` passes (write + attend) with CUDA events on
-    the current stream.  Returns (total ms of the passes, mean ms of attend)."""
-    stream = torch.cuda.current_stream()
-    for _ in range(warmup):
-        dev.write()
-        dev.attend()
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    mids = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    for i in range(steps):
-        if flush is not None:
-            flush.fill_(i & 0xff)  # evict the previous pass from L2 (not timed)
-        starts[i].record(stream)
-        dev.write()
-        mids[i].record(stream)
-        dev.attend()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    total = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
-    attend = [m.elapsed_time(e) for m, e in zip(mids, ends)]
-    return total, float(np.mean(attend)), float(np.median(attend))
-
-
-def time_e2e(step, dev: DeviceStep, steps: int, warmup: int, world: int, keep_out=None):
-    """The same pass through the public API from pinned HOST buffers.  Every
-    step copies its inputs host->device and reads the output back.  The step's
+def time_e2e(dstep, steps: int, warmup: int, world: int):
+    """The step through the public API from pinned HOST buffers.  Every step
+    copies its inputs host->device and reads the output back.  The step's
     inputs sit in one pinned host buffer (each at a 256-byte aligned offset),
     as a serving engine stages a step's inputs, and go over in one transfer
-    into one device buffer whose slices are the tensors the calls read."""
-    s = step
-    host_in = {"new_k": pinned(s.new_k), "new_v": pinned(s.new_v),
-               "token_seq": pinned(s.token_seq), "token_pos": pinned(s.token_pos),
-               "table": pinned(s.table)}
-    if s.n_decode:
-        host_in.update(q=pinned(s.q_decode), seqlens=pinned(s.cache_seqlens))
-    else:
-        host_in.update(q=pinned(s.q_prefill), cu_q=pinned(s.cu_q), cu_k=pinned(s.cu_k))
+    into one device buffer whose slices are the tensors the calls read.
+    Returns (ms per step, h2d bytes, d2h bytes)."""
+    host_in = {k: pinned(v) for k, v in dstep.host.items()}
     offs, total = {}, 0
     for name, t in host_in.items():
         offs[name] = total
@@ -302,21 +408,9 @@ def time_e2e(step, dev: DeviceStep, steps: int, warmup: int, world: int, keep_ou
         nb = t.numel() * t.element_size()
         host_buf[offs[name]:offs[name] + nb].copy_(t.reshape(-1).view(torch.uint8))
         views[name] = dev_buf[offs[name]:offs[name] + nb].view(t.dtype).view(t.shape)
-    host_out = torch.empty(dev.out.shape, dtype=dev.out.dtype).pin_memory()
+    host_out = torch.empty(dstep.out.shape, dtype=dstep.out.dtype).pin_memory()
     h2d = total
     d2h = host_out.numel() * host_out.element_size()
-
-    # the calls read the slices of the staged buffer (restored afterwards)
-    saved = dict(vars(dev))
-    dev.new_k, dev.new_v = views["new_k"], views["new_v"]
-    dev.token_seq, dev.token_pos = views["token_seq"], views["token_pos"]
-    dev.table, dev.q = views["table"], views["q"]
-    if s.n_decode:
-        dev.seqlens = views["seqlens"]
-        dev.dtable = views["table"][: s.n_decode]
-    else:
-        dev.cu_q, dev.cu_k = views["cu_q"], views["cu_k"]
-        dev.ptable = views["table"][s.n_decode:]
 
     # Two copy streams: a step's upload may run while the previous step's
     # output is read back (the link carries both directions at once), but the
@@ -336,52 +430,48 @@ def time_e2e(step, dev: DeviceStep, steps: int, warmup: int, world: int, keep_ou
         ev_in.record(up)
         cur.wait_event(ev_in)
         cur.wait_event(ev_out)
-        dev.write()
-        dev.attend()
+        dstep.run(views)
         ev_done.record(cur)
         down.wait_event(ev_done)
         with torch.cuda.stream(down):
-            host_out.copy_(dev.out, non_blocking=True)
+            host_out.copy_(dstep.out, non_blocking=True)
         ev_out.record(down)
 
-    try:
-        for _ in range(warmup):
-            one()
-        torch.cuda.synchronize()
-        barrier(world)
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(cur)
-        ev_done.record(cur)
-        ev_out.record(cur)
-        for _ in range(steps):
-            one()
-        cur.wait_event(ev_out)
-        t1.record(cur)
-        torch.cuda.synchronize()
-    finally:
-        vars(dev).update(saved)
-    if keep_out is not None:
-        keep_out.append(host_out.clone())
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(cur)
+    ev_done.record(cur)
+    ev_out.record(cur)
+    for _ in range(steps):
+        one()
+    cur.wait_event(ev_out)
+    t1.record(cur)
+    torch.cuda.synchronize()
     ms = max_over_ranks(t0.elapsed_time(t1), world) / steps
     return ms, h2d, d2h
 
 
-def traffic_of(kernel: str):
-    """DRAM bytes per launch from the committed ncu capture of `kernel`, or None
-    when the kernel's source has changed since the capture."""
+def traffic_of(key: str):
+    """DRAM bytes per call from the committed ncu capture of workload `key`
+    (the sum over the call's kernels), or None when a kernel's source file has
+    changed since the capture."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    rec = json.load(open(p)).get(kernel)
+    rec = json.load(open(p)).get(key)
     if not rec:
         return None
-    src = os.path.join(ROOT, rec["source"])
-    if not os.path.exists(src):
-        return None
-    if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != rec["source_sha256_16"]:
-        return None
+    for src, h in rec["sources"].items():
+        path = os.path.join(ROOT, src)
+        if not os.path.exists(path):
+            return None
+        if hashlib.sha256(open(path, "rb").read()).hexdigest()[:16] != h:
+            return None
     return rec["dram_bytes_per_launch"]
 
 
@@ -391,6 +481,14 @@ def load_peaks():
         d = json.load(open(p))
         return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
     return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def hbm_roofline(kernel, nbytes, mean, med, peak, src, traffic_key):
+    gbs = nbytes / (mean * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": kernel, "achieved": round(gbs, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(gbs / peak, 4), "peak_source": src,
+            "traffic": traffic_of(traffic_key), "algorithmic_bytes_per_launch": nbytes,
+            "mean_ms": round(mean, 5), "median_ms": round(med, 5)}
 
 
 # ---------------------------------------------------------------------------
@@ -468,39 +566,35 @@ def main():
         return
     import paged_kv_cache_70_gb300 as pkv
     from paged_kv_cache_70_gb300 import workloads as W
-    hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
+    peaks = load_peaks()
+    flush = L2Flush()
 
     line = {"metric": METRIC, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "gpu_launches": 0,
             "error_flags": 0}
     dstep = None
-    if args.only in ("all", "decode"):
-        dstep = run_decode(args, world, pkv, W, hbm_peak, peak_src, line)
-    if args.only in ("all", "prefill"):
-        run_prefill(args, world, pkv, W, bf16_peak, peak_src, line)
-    if args.only in ("all", "copy"):
-        run_copy(args, world, pkv, hbm_peak, peak_src, line)
-    if args.only in ("all", "shared"):
-        run_shared_prefix(args, world, pkv, W, hbm_peak, peak_src, line)
-    if args.only in ("all", "mixed"):
-        run_mixed_step(args, world, pkv, W, hbm_peak, peak_src, line)
-    if args.only == "prefill":  # headline comes from the prefill half
-        line["metric"] = "varlen prefill TFLOP/s"
-        line["value"], line["unit"] = line["prefill"].get("value"), "TFLOP/s"
-        line["ms_per_step"] = line["prefill"].get("ms_per_step")
-    if args.only == "mixed":
-        line["metric"] = line["mixed_step"]["metric"]
-        line["value"] = line["mixed_step"]["value"]
-        line["ms_per_step"] = line["mixed_step"]["ms_per_step"]
-    if args.only == "shared":
-        line["metric"] = line["decode_shared_prefix"]["metric"]
-        line["value"] = line["decode_shared_prefix"]["value"]
-        line["ms_per_step"] = line["decode_shared_prefix"]["ms_per_step"]
-    if args.only == "copy":
-        line["metric"] = line["copy_blocks"]["metric"]
-        line["value"] = line["copy_blocks"]["value"]
-        line["ms_per_step"] = line["copy_blocks"]["ms_per_step"]
+    only = args.only
+    if only in ("all", "decode"):
+        dstep = run_decode(args, world, pkv, W, peaks, flush, line)
+    if only in ("all", "qwen3"):
+        run_qwen3(args, world, pkv, W, peaks, flush, line)
+    if only in ("all", "write"):
+        run_write(args, world, pkv, W, peaks, flush, line)
+    if only in ("all", "prefill"):
+        run_prefill(args, world, pkv, W, peaks, flush, line)
+    if only in ("all", "copy"):
+        run_copy(args, world, pkv, peaks, line)
+    if only in ("all", "shared"):
+        run_shared_prefix(args, world, pkv, W, peaks, flush, line)
+    if only in ("all", "mixed"):
+        run_mixed_step(args, world, pkv, W, peaks, flush, line)
+    sub = {"qwen3": "decode_qwen3", "write": "kv_write", "prefill": "prefill",
+           "copy": "copy_blocks", "shared": "decode_shared_prefix", "mixed": "mixed_step"}
+    if only in sub and "value" in line.get(sub[only], {}):
+        part = line[sub[only]]
+        line["metric"], line["value"] = part["metric"], part["value"]
+        line["unit"], line["ms_per_step"] = part["unit"], part["ms_per_step"]
     cpu_baseline(args, world, rank, W, dstep, line)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -509,55 +603,129 @@ def main():
         dist.destroy_process_group()
 
 
-def run_decode(args, world, pkv, W, hbm_peak, peak_src, line):
+def run_decode(args, world, pkv, W, peaks, flush, line):
+    """Headline: the long-context decode step in one paged_decode_append call."""
+    hbm_peak, _, _, peak_src = peaks
     dstep = W.config(DECODE_CFG)
-    ddev = DeviceStep(dstep, pkv)
+    ddev = DecodeStep(dstep, pkv)
     clocks = Clocks(torch.cuda.current_device())
     clocks.start()  # warm-up + timed region + a short untimed soak of the same step
-    total_ms, dec_mean, dec_med = time_steps(ddev, args.steps, args.warmup, None, world)
-    soak(ddev)
+    ms_step, per = time_parts([ddev.run], args.steps, args.warmup, world, flush)
+    if not args.no_soak:
+        soak(ddev.run)
     clk = clocks.stop()
     clk["window"] = "warm-up, timed region, then 0.5 s more of the same step (untimed)"
-    total_ms = max_over_ranks(total_ms, world)
-    ms_step = total_ms / args.steps
-    dbytes = decode_kernel_bytes(dstep)
-    wbytes = write_bytes(dstep)
-    step_bytes = dbytes + wbytes
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
-    # workspace traffic of the split (partials written and read back)
+    nbytes = decode_append_bytes(dstep)
+    value = world * nbytes / (ms_step * 1e-3) / 1e9
     ctas = torch.cuda.get_device_properties(0).multi_processor_count
     part = (ctas + dstep.n_decode) * dstep.hq * (dstep.d + 2) * 4 * 2
-    achieved = dbytes / (dec_mean * 1e-3) / 1e9
     line.update({
         "value": round(value, 2), "ms_per_step": round(ms_step, 5),
-        "config": {"workload": W.CONFIG_NAMES[DECODE_CFG] + "; step = slot_mapping build + "
-                               "new-token write + paged decode (split-KV + combine)",
+        "config": {"workload": W.CONFIG_NAMES[DECODE_CFG] + "; step = one paged_decode_append "
+                               "call: the new token of every sequence written into the cache "
+                               "and attended to with the cached keys (split-KV + combine)",
                    "batch": dstep.n_decode, "seq_lens_total": int(dstep.cache_seqlens.sum()),
                    "block_size": dstep.block_size, "num_heads": dstep.hq,
                    "num_kv_heads": dstep.hkv, "head_dim": dstep.d, "seed": 1000 + DECODE_CFG,
-                   "bytes_per_step": step_bytes,
-                   "l2": "inputs larger than L2 (%.0f MB of K/V per step)" % (dbytes / 1e6),
+                   "bytes_per_step": nbytes,
+                   "l2": "flushed between steps (256 MiB written, then 256 MiB read; untimed); "
+                         "K/V per step %.0f MB, larger than L2" % (nbytes / 1e6),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": "paged_decode (split kernel + combine)",
-                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
-                     "traffic": traffic_of("decode_split_kernel"),
-                     "algorithmic_bytes_per_launch": dbytes,
-                     "workspace_bytes_per_launch": part,
-                     "mean_ms": round(dec_mean, 5), "median_ms": round(dec_med, 5)},
+        "roofline": hbm_roofline("paged_decode_append (split kernel + combine)", nbytes,
+                                 per[0][0], per[0][1], hbm_peak, peak_src,
+                                 "long_context_decode"),
         "clocks": clk,
     })
-    line["gpu_launches"] += 4 * args.steps
-    run_decode_append(args, world, pkv, dstep, ddev, step_bytes, hbm_peak, peak_src, line)
+    line["roofline"]["workspace_bytes_per_launch"] = part
+    line["gpu_launches"] += DecodeStep.launches * args.steps
     if not args.no_e2e:
-        e2e_ms, h2d, d2h = time_e2e(dstep, ddev, args.steps, args.warmup, world)
-        line["e2e"] = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2),
+        e2e_ms, h2d, d2h = time_e2e(ddev, args.steps, args.warmup, world)
+        line["e2e"] = {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2),
                        "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        line["gpu_launches"] += DecodeStep.launches * args.steps
     line["error_flags"] |= pkv.paged_error_flags()
     del ddev
     torch.cuda.empty_cache()
+    run_separate_write(args, world, pkv, W, dstep, peaks, flush, line)
     return dstep
+
+
+def run_separate_write(args, world, pkv, W, dstep, peaks, flush, line):
+    """The headline step as slot_mapping build + paged_kv_write + paged_decode."""
+    hbm_peak, _, _, peak_src = peaks
+    dev = WriteDecodeStep(dstep, pkv)
+    ms_step, per = time_parts([dev.write, dev.attend], args.steps, args.warmup, world, flush)
+    dbytes = decode_kernel_bytes(dstep)
+    nbytes = dbytes + slot_build_bytes(dstep) + write_bytes(dstep)
+    line["decode_separate_write"] = {
+        "metric": "decode KV GB/s, step as slot_mapping build + write + paged_decode",
+        "unit": "GB/s", "value": round(world * nbytes / (ms_step * 1e-3) / 1e9, 2),
+        "ms_per_step": round(ms_step, 5), "bytes_per_step": nbytes,
+        "workload": W.CONFIG_NAMES[DECODE_CFG] + "; L2 flushed between steps",
+        "write_ms": round(per[0][0], 5),
+        "roofline": hbm_roofline("paged_decode (split kernel + combine)", dbytes, per[1][0],
+                                 per[1][1], hbm_peak, peak_src, "long_context_decode_plain")}
+    line["gpu_launches"] += 4 * args.steps
+    line["error_flags"] |= pkv.paged_error_flags()
+    del dev
+    torch.cuda.empty_cache()
+
+
+def run_qwen3(args, world, pkv, W, peaks, flush, line):
+    """The Qwen3-0.6B-shaped decode (batch 64, L~U[128,4096], block 16): the
+    same one-call step as the headline."""
+    hbm_peak, _, _, peak_src = peaks
+    s = W.config(QWEN_CFG)
+    dev = DecodeStep(s, pkv)
+    ms_step, per = time_parts([dev.run], args.steps, args.warmup, world, flush)
+    nbytes = decode_append_bytes(s)
+    part = {
+        "metric": "decode KV GB/s (Qwen3-0.6B-shaped decode)", "unit": "GB/s",
+        "value": round(world * nbytes / (ms_step * 1e-3) / 1e9, 2),
+        "ms_per_step": round(ms_step, 5), "bytes_per_step": nbytes,
+        "workload": W.CONFIG_NAMES[QWEN_CFG] + "; step = one paged_decode_append call; "
+                    "L2 flushed between steps",
+        "seq_lens_total": int(s.cache_seqlens.sum()),
+        "roofline": hbm_roofline("paged_decode_append (split kernel + combine)", nbytes,
+                                 per[0][0], per[0][1], hbm_peak, peak_src, "qwen3_decode")}
+    line["gpu_launches"] += DecodeStep.launches * args.steps
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = time_e2e(dev, args.steps, args.warmup, world)
+        part["e2e"] = {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2),
+                       "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        line["gpu_launches"] += DecodeStep.launches * args.steps
+    line["decode_qwen3"] = part
+    line["error_flags"] |= pkv.paged_error_flags()
+    del dev
+    torch.cuda.empty_cache()
+
+
+def run_write(args, world, pkv, W, peaks, flush, line):
+    """The slot_mapping write of the chunked-prefill workload's new rows
+    (17,928 rows of 2 KiB each for K and V): slot build and paged_kv_write
+    timed separately, the write against the HBM roofline."""
+    hbm_peak, _, _, peak_src = peaks
+    s = W.config(PREFILL_CFG)
+    dev = PrefillStep(s, pkv)
+    ms_step, per = time_parts([dev.slot_build, dev.write], args.steps, args.warmup, world,
+                              flush)
+    wb, sb = write_bytes(s), slot_build_bytes(s)
+    line["kv_write"] = {
+        "metric": "slot_mapping KV-cache write GB/s", "unit": "GB/s",
+        "value": round(world * (wb + sb) / (ms_step * 1e-3) / 1e9, 2),
+        "ms_per_step": round(ms_step, 5), "bytes_per_step": wb + sb,
+        "workload": f"the chunked-prefill workload's {len(s.token_seq)} new rows "
+                    f"(Hkv=8, d=128, bf16, B=256); step = paged_build_slot_mapping + "
+                    f"paged_kv_write; L2 flushed between steps",
+        "slot_build_ms": round(per[0][0], 5),
+        "roofline": hbm_roofline("kv_write_copy_kernel (paged_kv_write)", wb, per[1][0],
+                                 per[1][1], hbm_peak, peak_src, "kv_write")}
+    line["gpu_launches"] += 2 * args.steps
+    line["error_flags"] |= pkv.paged_error_flags()
+    del dev
+    torch.cuda.empty_cache()
 
 
 W_NAME_PACKED = ("causal varlen prefill over packed K/V: the chunked-prefill workload's 16 "
@@ -566,284 +734,52 @@ W_NAME_PACKED = ("causal varlen prefill over packed K/V: the chunked-prefill wor
 COPY_PAIRS, COPY_GEOM = 8192, (16, 8, 128)  # block pairs; B, Hkv, d (bf16)
 
 
-def run_decode_append(args, world, pkv, dstep, ddev, step_bytes, hbm_peak, peak_src, line):
-    """The same decode step in one call: paged_decode_append writes the new
-    token's K/V and attends over the cached keys plus the new one (split +
-    combine, two launches instead of four)."""
-    before = to_dev((dstep.cache_seqlens - 1).astype(np.int32))
-    out = torch.empty_like(ddev.q)
-    call = lambda: pkv.paged_decode_append(ddev.q, ddev.new_k, ddev.new_v, ddev.k_cache,
-                                           ddev.v_cache, ddev.dtable, before, dstep.scale,
-                                           out=out, workspace=ddev.ws)
-    for _ in range(args.warmup):
-        call()
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    for a, b in ev:
-        a.record(stream)
-        call()
-        b.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    ms = [a.elapsed_time(b) for a, b in ev]
-    mean = max_over_ranks(float(np.mean(ms)), world)
-    gbs = step_bytes / (mean * 1e-3) / 1e9
-    line["decode_append"] = {
-        "metric": "decode KV GB/s, step as one call with the in-place append", "unit": "GB/s",
-        "value": round(world * gbs, 2), "ms_per_step": round(mean, 5),
-        "workload": "the headline long-context decode step (same bytes per step)",
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_append (split + combine with the "
-                     "appended key and its cache write)", "achieved": round(gbs, 1),
-                     "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
-                     "peak_source": peak_src, "traffic": None, "mean_ms": round(mean, 5),
-                     "median_ms": round(float(np.median(ms)), 5)}}
-    line["gpu_launches"] += 2 * args.steps
-
-
-def run_copy(args, world, pkv, hbm_peak, peak_src, line):
-    """paged_copy_blocks: the copies of copy-on-write.  8192 block pairs of a
-    B=16, Hkv=8, d=128 bf16 pool (32 KiB per block per pool): 512 MiB read and
-    512 MiB written per launch, far beyond L2."""
-    B, hkv, d = COPY_GEOM
-    nb = 2 * COPY_PAIRS + 16
-    g = torch.Generator().manual_seed(1099)
-    k = torch.randint(-32768, 32767, (nb, B, hkv, d), generator=g, dtype=torch.int16)
-    k_cache = k.view(torch.bfloat16).cuda()
-    v_cache = torch.roll(k, 1, 0).view(torch.bfloat16).cuda()
-    perm = torch.randperm(nb, generator=g)
-    src = perm[:COPY_PAIRS].to(torch.int32).cuda()
-    dst = perm[COPY_PAIRS: 2 * COPY_PAIRS].to(torch.int32).cuda()
-    block_bytes = B * hkv * d * 2
-    nbytes = COPY_PAIRS * block_bytes * 2 * 2  # K and V, read and written
-    stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
-        pkv.paged_copy_blocks(k_cache, v_cache, src, dst)
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    for a, b in ev:
-        a.record(stream)
-        pkv.paged_copy_blocks(k_cache, v_cache, src, dst)
-        b.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    ms = [a.elapsed_time(b) for a, b in ev]
-    mean = max_over_ranks(float(np.mean(ms)), world)
-    gbs = nbytes / (mean * 1e-3) / 1e9
-    line["copy_blocks"] = {
-        "metric": "copy-on-write block copies GB/s", "unit": "GB/s",
-        "value": round(world * gbs, 1), "ms_per_step": round(mean, 5),
-        "workload": f"{COPY_PAIRS} block pairs, B={B}, Hkv={hkv}, d={d}, bf16 "
-                    f"({block_bytes // 1024} KiB per block per pool); step = one paged_copy_blocks",
-        "roofline": {"bound": "hbm", "kernel": "copy_blocks_kernel", "achieved": round(gbs, 1),
-                     "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
-                     "peak_source": peak_src, "traffic": traffic_of("copy_blocks_kernel"),
-                     "algorithmic_bytes_per_launch": nbytes, "mean_ms": round(mean, 5),
-                     "median_ms": round(float(np.median(ms)), 5)},
-        "l2": "inputs larger than L2 (512 MiB read per launch)"}
-    line["gpu_launches"] += args.steps
-    line["error_flags"] |= pkv.paged_error_flags()
-    del k_cache, v_cache
-    torch.cuda.empty_cache()
-
-
-def run_shared_prefix(args, world, pkv, W, hbm_peak, peak_src, line):
-    """Decode half of the continuous-batching workload: 256 sequences in 8
-    groups of 32 that share a 2048-token prefix (128 blocks of 16), suffixes
-    U[0,512] plus the new token.  Shared-prefix decode (each prefix block read
-    once per group) against plain paged decode of the same step.  The roofline
-    counts UNIQUE bytes: the prefixes once, every suffix, q and out."""
-    s = W.config(5)
-    nd = s.n_decode
-    dev = lambda a: to_dev(a)
-    k_cache, v_cache = dev(s.k_cache), dev(s.v_cache)
-    q, table, lens = dev(s.q_decode), dev(s.decode_table.copy()), dev(s.cache_seqlens)
-    groups = 8
-    gcu = dev(np.arange(0, nd + 1, nd // groups, dtype=np.int32))
-    plen = dev(np.full(groups, 2048, np.int32))
-    out = torch.empty_like(q)
-    row = s.hkv * s.d * 2 * 2  # K + V bytes per key
-    unique = (groups * 2048 + int((s.cache_seqlens - 2048).sum())) * row + 2 * q.numel() * 2
-    logical = int(s.cache_seqlens.sum()) * row + 2 * q.numel() * 2
-    ws = torch.empty(pkv._binding.load_library().paged_decode_shared_prefix_workspace_size(
-        nd, ctypes.byref(pkv.geom_of(k_cache, s.hq))), dtype=torch.uint8, device="cuda")
-    wsp = torch.empty(max(1, pkv.paged_decode_workspace_size(nd, s.hq, k_cache)),
-                      dtype=torch.uint8, device="cuda")
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-    shared = lambda: pkv.paged_decode_shared_prefix(q, k_cache, v_cache, table, lens, gcu, plen,
-                                                    nd // groups, s.scale, out=out, workspace=ws)
-    plain = lambda: pkv.paged_decode(q, k_cache, v_cache, table, lens, s.scale, out=out,
-                                     workspace=wsp)
-
-    def timed(fn):
-        for _ in range(args.warmup):
-            fn()
-        torch.cuda.synchronize()
-        barrier(world)
-        torch.cuda.synchronize()
-        stream = torch.cuda.current_stream()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-        for i, (a, b) in enumerate(ev):
-            flush.fill_(i & 0xff)
-            a.record(stream)
-            fn()
-            b.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        ms = [a.elapsed_time(b) for a, b in ev]
-        return max_over_ranks(float(np.mean(ms)), world), float(np.median(ms))
-
-    sh_ms, sh_med = timed(shared)
-    pl_ms, _ = timed(plain)
-    gbs = unique / (sh_ms * 1e-3) / 1e9
-    line["decode_shared_prefix"] = {
-        "metric": "shared-prefix decode GB/s of unique K/V", "unit": "GB/s",
-        "value": round(world * gbs, 1), "ms_per_step": round(sh_ms, 5),
-        "workload": "decode half of the continuous-batching step: 256 sequences, 8 groups of "
-                    "32 sharing a 2048-token prefix (B=16), suffixes U[0,512]+1, GQA 16/8, "
-                    "d=128, bf16; L2 flushed between steps",
-        "unique_bytes": unique, "logical_bytes": logical,
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_shared_prefix (prefix on the "
-                     "tensor cores + suffix split + combine)", "achieved": round(gbs, 1),
-                     "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
-                     "peak_source": peak_src, "traffic": None, "mean_ms": round(sh_ms, 5),
-                     "median_ms": round(sh_med, 5)},
-        "plain_decode_same_step": {"ms": round(pl_ms, 5),
-                                   "logical_GBps": round(logical / (pl_ms * 1e-3) / 1e9, 1),
-                                   "speedup_of_shared": round(pl_ms / sh_ms, 3)}}
-    line["gpu_launches"] += 3 * args.steps
-    line["error_flags"] |= pkv.paged_error_flags()
-    del k_cache, v_cache, ws, wsp, flush
-    torch.cuda.empty_cache()
-
-
-def run_mixed_step(args, world, pkv, W, hbm_peak, peak_src, line):
-    """The whole continuous-batching step in one paged_mixed_step call: 2304
-    new rows (+5 % padding) written, causal prefill of 4 x 512 tokens, and
-    the in-place append + shared-prefix decode of 256 sequences.  Bytes
-    counted once each: K/V of every key read (shared prefixes once), the new
-    rows read and written, q and out."""
-    s = W.config(5)
-    nd = s.n_decode
-    is_dec = (s.token_seq >= 0) & (s.token_seq < nd)
-    dec_rows = np.where(is_dec)[0]
-    dec_rows = dec_rows[np.argsort(s.token_seq[dec_rows])]
-    pf_rows = np.where(~is_dec)[0]
-    B = s.block_size
-    seq = s.token_seq
-    slots = np.full(len(seq), -1, np.int32)
-    ok = seq >= 0
-    slots[ok] = s.table[seq[ok], s.token_pos[ok] // B] * B + s.token_pos[ok] % B
-    kc, vc = to_dev(s.k_cache), to_dev(s.v_cache)
-    decode = dict(q=to_dev(s.q_decode), k_new=to_dev(s.new_k[dec_rows]),
-                  v_new=to_dev(s.new_v[dec_rows]), table=to_dev(s.decode_table.copy()),
-                  seqlens=to_dev(s.cache_seqlens - 1),
-                  group_cu=to_dev(np.arange(0, nd + 1, nd // 8, dtype=np.int32)),
-                  group_prefix_len=to_dev(np.full(8, 2048, np.int32)), max_group_size=nd // 8,
-                  out=torch.empty(s.q_decode.shape, dtype=torch.bfloat16, device="cuda"))
-    prefill = dict(k_new=to_dev(s.new_k[pf_rows]), v_new=to_dev(s.new_v[pf_rows]),
-                   slots=to_dev(slots[pf_rows]), q=to_dev(s.q_prefill), cu_q=to_dev(s.cu_q),
-                   cu_k=to_dev(s.cu_k), max_q=s.max_seqlen_q, max_k=s.max_seqlen_k,
-                   table=to_dev(s.prefill_table.copy()),
-                   out=torch.empty(s.q_prefill.shape, dtype=torch.bfloat16, device="cuda"))
-    ws = torch.empty(pkv._binding.load_library().paged_mixed_step_workspace_size(
-        nd, ctypes.byref(pkv.geom_of(kc, s.hq))), dtype=torch.uint8, device="cuda")
-    row = s.hkv * s.d * 2 * 2
-    n_new = int((s.token_seq >= 0).sum())
-    nbytes = ((8 * 2048 + int((s.cache_seqlens - 1 - 2048).sum())) * row  # decode keys once
-              + int(s.cu_k[-1]) * row                                    # prefill keys
-              + 2 * n_new * row                                           # new rows r + w
-              + 2 * (s.q_decode.size + s.q_prefill.size) * 2)             # q and out
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-    call = lambda: pkv.paged_mixed_step(kc, vc, s.scale, prefill=prefill, decode=decode,
-                                        workspace=ws)
-    for _ in range(args.warmup):
-        call()
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    for i, (a, b) in enumerate(ev):
-        flush.fill_(i & 0xff)
-        a.record(stream)
-        call()
-        b.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    ms = [a.elapsed_time(b) for a, b in ev]
-    mean = max_over_ranks(float(np.mean(ms)), world)
-    gbs = nbytes / (mean * 1e-3) / 1e9
-    line["mixed_step"] = {
-        "metric": "continuous-batching step GB/s of unique bytes", "unit": "GB/s",
-        "value": round(world * gbs, 1), "ms_per_step": round(mean, 5),
-        "workload": W.CONFIG_NAMES[5] + "; one paged_mixed_step call; L2 flushed between steps",
-        "unique_bytes": nbytes,
-        "roofline": {"bound": "hbm", "kernel": "paged_mixed_step (write, prefill, shared-prefix "
-                     "pass, split, combine with append)", "achieved": round(gbs, 1),
-                     "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
-                     "peak_source": peak_src, "traffic": None, "mean_ms": round(mean, 5),
-                     "median_ms": round(float(np.median(ms)), 5)}}
-    line["gpu_launches"] += 5 * args.steps
-    line["error_flags"] |= pkv.paged_error_flags()
-    del kc, vc, ws, flush
-    torch.cuda.empty_cache()
-
-
-def run_prefill(args, world, pkv, W, bf16_peak, peak_src, line):
+def run_prefill(args, world, pkv, W, peaks, flush, line):
+    _, bf16_peak, _, peak_src = peaks
     pstep = W.config(PREFILL_CFG)
-    pdev = DeviceStep(pstep, pkv)
+    pdev = PrefillStep(pstep, pkv)
     try:
         pdev.attend()
-        ok = True
     except pkv.PagedKVError as e:
-        ok = False
         line["prefill"] = {"unavailable": str(e)}
-    if ok:
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-        clocks = Clocks(torch.cuda.current_device())
-        clocks.start()
-        ptotal, pmean, pmed = time_steps(pdev, args.steps, args.warmup, flush, world)
-        soak(pdev)
-        pclk = clocks.stop()
-        pclk["window"] = "warm-up, timed region, then 0.5 s more of the same step (untimed)"
-        ptotal = max_over_ranks(ptotal, world)
-        flops = prefill_flops(pstep)
-        p_ms = ptotal / args.steps
-        tflops = flops / (pmean * 1e-3) / 1e12
-        line["prefill"] = {
-            "metric": "varlen prefill TFLOP/s", "workload": W.CONFIG_NAMES[PREFILL_CFG],
-            "value": round(world * flops / (p_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-            "ms_per_step": round(p_ms, 5),
-            "step": "slot_mapping build + write of 16 requests' new K/V + causal varlen "
-                    "prefill (L2 flushed between steps, not timed)",
-            "flops_per_step": flops, "visible_pairs": prefill_pairs(pstep),
-            "roofline": {"bound": "tensor", "kernel": "paged_varlen_prefill",
-                         "achieved": round(tflops, 1), "peak": bf16_peak,
-                         "unit": "TFLOP/s", "frac": round(tflops / bf16_peak, 4),
-                         "peak_source": peak_src + " (bf16 burst)",
-                         "traffic": traffic_of("prefill_tc_kernel"),
-                         "mean_ms": round(pmean, 5), "median_ms": round(pmed, 5)},
-            "clocks": pclk,
-        }
-        if not args.no_e2e:
-            pe2e_ms, ph2d, pd2h = time_e2e(pstep, pdev, args.steps, args.warmup, world)
-            line["prefill"]["e2e"] = {
-                "value": round(world * flops / (pe2e_ms * 1e-3) / 1e12, 2),
-                "unit": "TFLOP/s", "ms_per_step": round(pe2e_ms, 5),
-                "h2d_bytes_per_step": ph2d, "d2h_bytes_per_step": pd2h}
-        line["gpu_launches"] += 3 * args.steps
-        line["error_flags"] |= pkv.paged_error_flags()
-        run_prefill_packed(args, world, pkv, pstep, pdev, flops, flush, bf16_peak, peak_src,
-                           line)
+        return
+    clocks = Clocks(torch.cuda.current_device())
+    clocks.start()
+    p_ms, per = time_parts([pdev.slot_build, pdev.write, pdev.attend], args.steps, args.warmup,
+                           world, flush)
+    if not args.no_soak:
+        soak(pdev.run)
+    pclk = clocks.stop()
+    pclk["window"] = "warm-up, timed region, then 0.5 s more of the same step (untimed)"
+    flops = prefill_flops(pstep)
+    pmean, pmed = per[2]
+    tflops = flops / (pmean * 1e-3) / 1e12
+    line["prefill"] = {
+        "metric": "varlen prefill TFLOP/s", "workload": W.CONFIG_NAMES[PREFILL_CFG],
+        "value": round(world * flops / (p_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "ms_per_step": round(p_ms, 5),
+        "step": "slot_mapping build + write of 16 requests' new K/V + causal varlen "
+                "prefill (L2 flushed between steps, not timed)",
+        "slot_build_ms": round(per[0][0], 5), "write_ms": round(per[1][0], 5),
+        "flops_per_step": flops, "visible_pairs": prefill_pairs(pstep),
+        "roofline": {"bound": "tensor", "kernel": "paged_varlen_prefill",
+                     "achieved": round(tflops, 1), "peak": bf16_peak,
+                     "unit": "TFLOP/s", "frac": round(tflops / bf16_peak, 4),
+                     "peak_source": peak_src + " (bf16 burst)",
+                     "traffic": traffic_of("chunked_prefill"),
+                     "mean_ms": round(pmean, 5), "median_ms": round(pmed, 5)},
+        "clocks": pclk,
+    }
+    line["gpu_launches"] += PrefillStep.launches * args.steps
+    if not args.no_e2e:
+        pe2e_ms, ph2d, pd2h = time_e2e(pdev, args.steps, args.warmup, world)
+        line["prefill"]["e2e"] = {
+            "value": round(world * flops / (pe2e_ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "ms_per_step": round(pe2e_ms, 5),
+            "h2d_bytes_per_step": ph2d, "d2h_bytes_per_step": pd2h}
+        line["gpu_launches"] += PrefillStep.launches * args.steps
+    line["error_flags"] |= pkv.paged_error_flags()
+    run_prefill_packed(args, world, pkv, pstep, pdev, flops, flush, bf16_peak, peak_src, line)
     del pdev
     torch.cuda.empty_cache()
 
@@ -861,26 +797,12 @@ def run_prefill_packed(args, world, pkv, pstep, pdev, flops, flush, bf16_peak, p
     idx = torch.from_numpy(np.concatenate(rows)).cuda()
     kp = pdev.k_cache.view(-1, s.hkv, s.d)[idx].contiguous()
     vp = pdev.v_cache.view(-1, s.hkv, s.d)[idx].contiguous()
-    call = lambda: pkv.paged_varlen_prefill(pdev.q, kp, vp, pdev.cu_q, pdev.cu_k,
+    t = pdev.dev
+    call = lambda: pkv.paged_varlen_prefill(t["q"], kp, vp, t["cu_q"], t["cu_k"],
                                             s.max_seqlen_q, s.max_seqlen_k, None,
                                             causal=s.causal, scale=s.scale, out=pdev.out)
-    for _ in range(args.warmup):
-        call()
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    for i, (a, b) in enumerate(ev):
-        flush.fill_(i & 0xff)
-        a.record(stream)
-        call()
-        b.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    ms = [a.elapsed_time(b) for a, b in ev]
-    mean = max_over_ranks(float(np.mean(ms)), world)
+    _, per = time_parts([call], args.steps, args.warmup, world, flush)
+    mean, med = per[0]
     tf = flops / (mean * 1e-3) / 1e12
     line["prefill_contiguous"] = {
         "metric": "varlen prefill TFLOP/s (packed K/V, block_table = NULL)",
@@ -889,11 +811,149 @@ def run_prefill_packed(args, world, pkv, pstep, pdev, flops, flush, bf16_peak, p
         "roofline": {"bound": "tensor", "kernel": "paged_varlen_prefill (packed)",
                      "achieved": round(tf, 1), "peak": bf16_peak, "unit": "TFLOP/s",
                      "frac": round(tf / bf16_peak, 4), "peak_source": peak_src + " (bf16 burst)",
-                     "traffic": None, "mean_ms": round(mean, 5),
-                     "median_ms": round(float(np.median(ms)), 5)}}
+                     "traffic": None, "mean_ms": round(mean, 5), "median_ms": round(med, 5)}}
     line["gpu_launches"] += args.steps
     line["error_flags"] |= pkv.paged_error_flags()
     del kp, vp
+
+
+def run_copy(args, world, pkv, peaks, line):
+    """paged_copy_blocks: the copies of copy-on-write.  8192 block pairs of a
+    B=16, Hkv=8, d=128 bf16 pool (32 KiB per block per pool): 512 MiB read and
+    512 MiB written per launch, far beyond L2."""
+    hbm_peak, _, _, peak_src = peaks
+    B, hkv, d = COPY_GEOM
+    nb = 2 * COPY_PAIRS + 16
+    g = torch.Generator().manual_seed(1099)
+    k = torch.randint(-32768, 32767, (nb, B, hkv, d), generator=g, dtype=torch.int16)
+    k_cache = k.view(torch.bfloat16).cuda()
+    v_cache = torch.roll(k, 1, 0).view(torch.bfloat16).cuda()
+    perm = torch.randperm(nb, generator=g)
+    src = perm[:COPY_PAIRS].to(torch.int32).cuda()
+    dst = perm[COPY_PAIRS: 2 * COPY_PAIRS].to(torch.int32).cuda()
+    block_bytes = B * hkv * d * 2
+    nbytes = COPY_PAIRS * block_bytes * 2 * 2  # K and V, read and written
+    call = lambda: pkv.paged_copy_blocks(k_cache, v_cache, src, dst)
+    _, per = time_parts([call], args.steps, args.warmup, world)
+    mean, med = per[0]
+    gbs = nbytes / (mean * 1e-3) / 1e9
+    line["copy_blocks"] = {
+        "metric": "copy-on-write block copies GB/s", "unit": "GB/s",
+        "value": round(world * gbs, 1), "ms_per_step": round(mean, 5),
+        "workload": f"{COPY_PAIRS} block pairs, B={B}, Hkv={hkv}, d={d}, bf16 "
+                    f"({block_bytes // 1024} KiB per block per pool); step = one paged_copy_blocks",
+        "roofline": hbm_roofline("copy_blocks_kernel", nbytes, mean, med, hbm_peak, peak_src,
+                                 "copy_blocks"),
+        "l2": "inputs larger than L2 (512 MiB read per launch)"}
+    line["gpu_launches"] += args.steps
+    line["error_flags"] |= pkv.paged_error_flags()
+    del k_cache, v_cache
+    torch.cuda.empty_cache()
+
+
+def run_shared_prefix(args, world, pkv, W, peaks, flush, line):
+    """Decode half of the continuous-batching workload: 256 sequences in 8
+    groups of 32 that share a 2048-token prefix (128 blocks of 16), suffixes
+    U[0,512] plus the new token.  Shared-prefix decode (each prefix block read
+    once per group) against plain paged decode of the same step.  The roofline
+    counts UNIQUE bytes: the prefixes once, every suffix, q and out."""
+    hbm_peak, _, _, peak_src = peaks
+    s = W.config(MIXED_CFG)
+    nd = s.n_decode
+    k_cache, v_cache = to_dev(s.k_cache), to_dev(s.v_cache)
+    q, table, lens = to_dev(s.q_decode), to_dev(s.decode_table.copy()), to_dev(s.cache_seqlens)
+    groups = 8
+    gcu = to_dev(np.arange(0, nd + 1, nd // groups, dtype=np.int32))
+    plen = to_dev(np.full(groups, 2048, np.int32))
+    out = torch.empty_like(q)
+    row = s.hkv * s.d * 2 * 2  # K + V bytes per key
+    unique = (groups * 2048 + int((s.cache_seqlens - 2048).sum())) * row + 2 * q.numel() * 2
+    logical = int(s.cache_seqlens.sum()) * row + 2 * q.numel() * 2
+    ws = torch.empty(pkv._binding.load_library().paged_decode_shared_prefix_workspace_size(
+        nd, ctypes.byref(pkv.geom_of(k_cache, s.hq))), dtype=torch.uint8, device="cuda")
+    wsp = torch.empty(max(1, pkv.paged_decode_workspace_size(nd, s.hq, k_cache)),
+                      dtype=torch.uint8, device="cuda")
+    shared = lambda: pkv.paged_decode_shared_prefix(q, k_cache, v_cache, table, lens, gcu, plen,
+                                                    nd // groups, s.scale, out=out, workspace=ws)
+    plain = lambda: pkv.paged_decode(q, k_cache, v_cache, table, lens, s.scale, out=out,
+                                     workspace=wsp)
+    _, per = time_parts([shared], args.steps, args.warmup, world, flush)
+    sh_ms, sh_med = per[0]
+    _, per = time_parts([plain], args.steps, args.warmup, world, flush)
+    pl_ms = per[0][0]
+    gbs = unique / (sh_ms * 1e-3) / 1e9
+    line["decode_shared_prefix"] = {
+        "metric": "shared-prefix decode GB/s of unique K/V", "unit": "GB/s",
+        "value": round(world * gbs, 1), "ms_per_step": round(sh_ms, 5),
+        "workload": "decode half of the continuous-batching step: 256 sequences, 8 groups of "
+                    "32 sharing a 2048-token prefix (B=16), suffixes U[0,512]+1, GQA 16/8, "
+                    "d=128, bf16; L2 flushed between steps",
+        "unique_bytes": unique, "logical_bytes": logical,
+        "roofline": hbm_roofline("paged_decode_shared_prefix (every kernel of the call)", unique,
+                                 sh_ms, sh_med, hbm_peak, peak_src, "shared_prefix_decode"),
+        "plain_decode_same_step": {"ms": round(pl_ms, 5),
+                                   "logical_GBps": round(logical / (pl_ms * 1e-3) / 1e9, 1),
+                                   "speedup_of_shared": round(pl_ms / sh_ms, 3)}}
+    line["gpu_launches"] += 5 * args.steps
+    line["error_flags"] |= pkv.paged_error_flags()
+    del k_cache, v_cache, ws, wsp
+    torch.cuda.empty_cache()
+
+
+def run_mixed_step(args, world, pkv, W, peaks, flush, line):
+    """The whole continuous-batching step in one paged_mixed_step call: 2304
+    new rows (+5 % padding) written, causal prefill of 4 x 512 tokens, and
+    the in-place append + shared-prefix decode of 256 sequences.  Bytes
+    counted once each: K/V of every key read (shared prefixes once), the new
+    rows read and written, q and out."""
+    hbm_peak, _, _, peak_src = peaks
+    s = W.config(MIXED_CFG)
+    nd = s.n_decode
+    is_dec = (s.token_seq >= 0) & (s.token_seq < nd)
+    dec_rows = np.where(is_dec)[0]
+    dec_rows = dec_rows[np.argsort(s.token_seq[dec_rows])]
+    pf_rows = np.where(~is_dec)[0]
+    kc, vc = to_dev(s.k_cache), to_dev(s.v_cache)
+    # the prefill rows' slots, built by the library (set-up, not timed)
+    slots = pkv.paged_build_slot_mapping(to_dev(s.table), to_dev(s.token_seq),
+                                         to_dev(s.token_pos), s.block_size)
+    pf_idx = torch.from_numpy(pf_rows).cuda()
+    decode = dict(q=to_dev(s.q_decode), k_new=to_dev(s.new_k[dec_rows]),
+                  v_new=to_dev(s.new_v[dec_rows]), table=to_dev(s.decode_table.copy()),
+                  seqlens=to_dev(s.cache_seqlens - 1),
+                  group_cu=to_dev(np.arange(0, nd + 1, nd // 8, dtype=np.int32)),
+                  group_prefix_len=to_dev(np.full(8, 2048, np.int32)), max_group_size=nd // 8,
+                  out=torch.empty(s.q_decode.shape, dtype=torch.bfloat16, device="cuda"))
+    prefill = dict(k_new=to_dev(s.new_k[pf_rows]), v_new=to_dev(s.new_v[pf_rows]),
+                   slots=slots[pf_idx].contiguous(), q=to_dev(s.q_prefill), cu_q=to_dev(s.cu_q),
+                   cu_k=to_dev(s.cu_k), max_q=s.max_seqlen_q, max_k=s.max_seqlen_k,
+                   table=to_dev(s.prefill_table.copy()),
+                   out=torch.empty(s.q_prefill.shape, dtype=torch.bfloat16, device="cuda"))
+    ws = torch.empty(pkv._binding.load_library().paged_mixed_step_workspace_size(
+        nd, ctypes.byref(pkv.geom_of(kc, s.hq))), dtype=torch.uint8, device="cuda")
+    row = s.hkv * s.d * 2 * 2
+    n_new = int((s.token_seq >= 0).sum())
+    nbytes = ((8 * 2048 + int((s.cache_seqlens - 1 - 2048).sum())) * row  # decode keys once
+              + int(s.cu_k[-1]) * row                                    # prefill keys
+              + 2 * n_new * row                                           # new rows r + w
+              + 2 * (s.q_decode.size + s.q_prefill.size) * 2)             # q and out
+    call = lambda: pkv.paged_mixed_step(kc, vc, s.scale, prefill=prefill, decode=decode,
+                                        workspace=ws)
+    _, per = time_parts([call], args.steps, args.warmup, world, flush)
+    mean, med = per[0]
+    gbs = nbytes / (mean * 1e-3) / 1e9
+    line["mixed_step"] = {
+        "metric": "continuous-batching step GB/s of unique bytes", "unit": "GB/s",
+        "value": round(world * gbs, 1), "ms_per_step": round(mean, 5),
+        "workload": W.CONFIG_NAMES[MIXED_CFG] + "; one paged_mixed_step call; L2 flushed "
+                    "between steps",
+        "unique_bytes": nbytes,
+        "roofline": hbm_roofline("paged_mixed_step (every kernel of the call)", nbytes, mean,
+                                 med, hbm_peak, peak_src, "mixed_step")}
+    line["gpu_launches"] += 5 * args.steps
+    line["error_flags"] |= pkv.paged_error_flags()
+    del kc, vc, ws
+    torch.cuda.empty_cache()
 
 
 def cpu_baseline(args, world, rank, W, dstep, line):

@@ -119,7 +119,10 @@ int paged_kv_write(const void* k, const void* v, int32_t kv_dtype, const int32_t
 /*
  * paged_decode_workspace_size -- bytes of device scratch paged_decode needs for
  * `batch` sequences on the CURRENT device (the split plan depends on its SM
- * count).  Returns 0 for invalid arguments.
+ * count).  Returns 0 for invalid arguments.  There is no max_seqlen_k
+ * argument: the keys of all sequences are cut into one share per CTA, so the
+ * scratch holds (CTAs + batch) partial states whatever the lengths are, and
+ * the lengths themselves are device data the host need not know.
  */
 size_t paged_decode_workspace_size(int32_t batch, const pkv_geom* geom);
 
@@ -136,6 +139,8 @@ size_t paged_decode_workspace_size(int32_t batch, const pkv_geom* geom);
  * merges the shares of each sequence with the same rule and normalises.
  * Supported: head_dim 64 or 128; fp32 or bf16; Hq/Hkv in {1, 2, 4}; Hkv in
  * {1, 2, 4, 8} or a multiple of 8; any block_size >= 1; batch <= 4096.
+ * Like its workspace-size call it takes no max_seqlen_k: nothing in the launch
+ * depends on the longest sequence.
  * workspace: device scratch of at least paged_decode_workspace_size(batch, geom)
  * bytes, 256-byte aligned, contents irrelevant on entry; it must not be used by
  * another call that runs concurrently.
@@ -307,14 +312,21 @@ int paged_mixed_step(const pkv_mixed_step* step, void* k_cache, void* v_cache, v
  *     minus workspace / workspace_bytes.
  *   - Returns PKV_ERR_WORKSPACE when the problem needs more scratch than the
  *     array holds, i.e. when paged_decode_workspace_size(batch, geom) >
- *     PKV_NOALLOC_SCRATCH_BYTES (about 1000 sequences for Hq=16, head_dim=128
- *     on a 152-SM GPU).
+ *     PKV_NOALLOC_SCRATCH_BYTES.  That size is about
+ *     (SMs + batch) * Hq * (head_dim + 2) * 4 bytes, so the limit is
+ *     batch <= PKV_NOALLOC_SCRATCH_BYTES / (Hq * (head_dim + 2) * 4) - SMs:
+ *     about 850 sequences for Hq=16, head_dim=128 on a 152-SM GPU.
  *   - All calls share the one array, and it keeps the previous call's contents
  *     (nothing in it needs to start at zero).  Calls that overlap on the GPU
  *     race on it: order them on one stream or with events.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (cudaGetSymbolAddress) with that device current.  Under lazy
+ *     module loading (the CUDA default) that lookup also loads the module that
+ *     holds the array, which may allocate and synchronise.  A call with
+ *     batch 0 does this set-up alone (and nothing else): make it once per
+ *     device at initialisation, before any stream capture, or run with
+ *     CUDA_MODULE_LOADING=EAGER.  The looked-up address is cached; after
+ *     cudaDeviceReset the library must not be used on that device again.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (8u << 20)
 int paged_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
@@ -325,8 +337,12 @@ int paged_decode_noalloc(const void* q, const void* k_cache, const void* v_cache
 /*
  * paged_error_flags -- read (and with clear != 0, reset) the device error word
  * of the current device: an OR of PKV_FLAG_* bits set by kernels since the
- * last clear.  Synchronises with the device.  *flags (host pointer) receives
- * the word.
+ * last clear.  *flags (host pointer) receives the word.
+ * This call SYNCHRONISES with the device (it copies the word to the host with
+ * cudaMemcpy), unlike every other call here: use it between steps, not on a
+ * latency-critical path.  It replaces a plain int-returning "last error"
+ * call: the word is a set of independent flag bits, so it is returned through
+ * a pointer beside the status, and reading without clearing is possible.
  */
 int paged_error_flags(uint32_t* flags, int32_t clear);
 

@@ -73,6 +73,37 @@ def build(force: bool = False, verbose: bool = False, extra: tuple[str, ...] = (
     return LIB
 
 
+def build_variant(tag: str, defines: tuple[str, ...], variant_sources: tuple[str, ...]) -> str:
+    """A library built with extra `defines` in the translation units named in
+    `variant_sources` (file names under csrc/) and the default objects for the
+    rest, at _build/<tag>/libpagedkv.so.  Used by tests that need a kernel
+    compiled differently (e.g. a shorter wait limit); the default library is
+    untouched."""
+    build()
+    out_dir = os.path.join(BUILD, tag)
+    os.makedirs(out_dir, exist_ok=True)
+    nvcc = _nvcc()
+    objs = []
+    for src in sources():
+        name = os.path.basename(src)
+        if name in variant_sources:
+            obj = os.path.join(out_dir, name[:-3] + ".o")
+            cmd = [nvcc, *ARCH, *FLAGS, *defines, "-I", INCLUDE, "-c", src, "-o", obj]
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                sys.stderr.write(r.stdout + r.stderr)
+                raise RuntimeError(f"nvcc failed: {' '.join(cmd)}")
+        else:
+            obj = os.path.join(BUILD, name[:-3] + ".o")
+        objs.append(obj)
+    lib = os.path.join(out_dir, "libpagedkv.so")
+    r = subprocess.run([nvcc, *ARCH, "-shared", "-o", lib, *objs], capture_output=True, text=True)
+    if r.returncode != 0:
+        sys.stderr.write(r.stdout + r.stderr)
+        raise RuntimeError(f"link of {lib} failed")
+    return lib
+
+
 if __name__ == "__main__":
     defines = tuple(a for a in sys.argv[1:] if a.startswith("-D"))
     print(build(force="--force" in sys.argv or bool(defines), verbose="-v" in sys.argv,

@@ -44,17 +44,6 @@ cudaError_t current_device_info(DeviceInfo* info) {
     return cudaSuccess;
 }
 
-}  // namespace pkv
-
-using pkv::DeviceInfo;
-
-namespace {
-
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-int elt_size(int dtype) { return dtype == PKV_F32 ? 4 : (dtype == PKV_BF16 ? 2 : 0); }
-
-// common geometry checks; returns PKV_OK or an error code
 int check_geom(const pkv_geom* g) {
     if (!g) return PKV_ERR_INVALID;
     if (g->num_heads <= 0 || g->num_kv_heads <= 0 || g->head_dim <= 0 || g->block_size <= 0 ||
@@ -66,6 +55,15 @@ int check_geom(const pkv_geom* g) {
     if ((double)g->num_blocks * g->block_size > 2147483647.0) return PKV_ERR_UNSUPPORTED;
     return PKV_OK;
 }
+
+}  // namespace pkv
+
+using pkv::DeviceInfo;
+using pkv::aligned;
+using pkv::check_geom;
+using pkv::elt_size;
+
+namespace {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
 

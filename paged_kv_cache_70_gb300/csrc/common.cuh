@@ -12,8 +12,12 @@
 namespace pkv {
 
 // A pipeline wait that has not completed after this long gives up: the kernel
-// records PKV_FLAG_TIMEOUT and returns instead of hanging the GPU.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// records PKV_FLAG_TIMEOUT and returns instead of hanging the GPU.  2 s; a
+// test build may shorten it (PKV_WAIT_LIMIT_NS).
+#ifndef PKV_WAIT_LIMIT_NS
+#define PKV_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = PKV_WAIT_LIMIT_NS;
 
 __device__ __forceinline__ void flag_error(unsigned int* err, unsigned int bit) {
     if (err) atomicOr(err, bit);

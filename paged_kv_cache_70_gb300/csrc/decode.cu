@@ -48,7 +48,10 @@
 //    split kernel holds its grid open with one otherwise idle lane waiting on
 //    griddepcontrol.wait, so that its completion implies that kernel's.
 //  * Safety.  Block ids and lengths are range-checked before any address is
-//    formed; every mbarrier wait is time-limited (PKV_FLAG_TIMEOUT).
+//    formed; every mbarrier wait is time-limited (PKV_FLAG_TIMEOUT).  After
+//    a timeout the consumers stop waiting but still meet at every named
+//    barrier, and the producer waits (time-limited) for its last copies to
+//    land before the CTA exits.
 #include <float.h>
 
 #include "common.cuh"
@@ -305,19 +308,24 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
         if (a.wait_prior && lane == 31 && blockIdx.x == 0 && blockIdx.y == 0)
             asm volatile("griddepcontrol.wait;" ::: "memory");
         if (lane != 0) return;
+#ifdef PKV_TEST_SPLIT_PRODUCER_IDLE
+        // test-only build: issue nothing, so the consumers' first wait runs out
+        return;
+#endif
         const uint64_t pol = l2_evict_first_policy();
         int b = seq_of_tile(tstart, a.batch, t0);
         int g = a.group_cu ? group_of(a, b) : 0;
         int32_t L = clamp_len(a.seqlens[b], cap);
         int32_t st = seq_start(a, b, L, g);
-        for (int32_t t = t0, k = 0; t < t1; ++t, ++k) {
+        int32_t k = 0;  // stages filled so far
+        for (int32_t t = t0; t < t1; ++t, ++k) {
             while (t >= tstart[b + 1]) {
                 ++b;
                 L = clamp_len(a.seqlens[b], cap);
                 st = seq_start(a, b, L, g);
             }
             const int s = k % S;
-            if (!mbar_wait(&empty[s], ((k / S) & 1) ^ 1, a.err)) return;
+            if (!mbar_wait(&empty[s], ((k / S) & 1) ^ 1, a.err)) break;
             const int32_t pos0 = st + (t - tstart[b]) * R;
             const int32_t rows = min(R, L - pos0);
             const int32_t phys = a.table[(int64_t)b * a.max_blocks + pos0 / a.block_size];
@@ -346,6 +354,12 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
                 }
             }
         }
+        // The CTA must not exit while a copy into its shared memory is in
+        // flight: wait (time-limited) for the last fill of every stage.  In a
+        // normal run the consumers wait for the same phases, so this costs
+        // nothing; after a timeout the consumers may have stopped waiting.
+        for (int32_t j = k > S ? k - S : 0; j < k; ++j)
+            if (!mbar_wait(&full[j % S], (j / S) & 1, a.err)) break;
         return;
     }
 
@@ -368,6 +382,10 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
     int loaded = -1;
     int32_t L = 0, st = 0;
 
+    // After a timed-out wait the warp stops waiting, reading shared memory and
+    // releasing stages, but keeps walking the same tiles so that it meets the
+    // other consumer warps at every named barrier below.
+    bool live = true;
     for (int32_t t = t0, k = 0; t < t1; ++t, ++k) {
         while (t >= tstart[b + 1]) ++b;
         if (b != loaded) {
@@ -394,9 +412,9 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
             }
         }
         const int s = k % S;
-        if (!mbar_wait(&full[s], (k / S) & 1, a.err)) return;
+        if (live) live = __all_sync(0xffffffffu, mbar_wait(&full[s], (k / S) & 1, a.err));
         const int32_t rows = min(R, L - st - (t - tstart[b]) * R);
-        if (stage_ok[s]) {
+        if (live && stage_ok[s]) {
             const unsigned char* ks = stage_base + (size_t)s * 2 * half_bytes;
             const unsigned char* vs = ks + half_bytes;
             // warp-uniform loop over pairs of rows (ra, rb = ra + row_step)
@@ -450,7 +468,7 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (live && lane == 0) mbar_arrive(&empty[s]);
 
         // end of this CTA's piece of sequence b: merge and store the partial state
         const bool seg_end = (t + 1 == t1) || (t + 1 >= tstart[b + 1]);

@@ -12,6 +12,15 @@
 // the caller must order them (one stream, or events between streams).  The
 // kernels write every scratch byte they later read, so nothing needs clearing
 // between calls.
+//
+// The first call on a device resolves the array's device address.  The
+// library is built without relocatable device code, so under lazy module
+// loading (the CUDA default) that lookup is also what loads this file's module
+// and backs the array, which can allocate and synchronise.  Callers that must
+// avoid that inside their serving loop make one call with batch 0 at set-up
+// time (or run with CUDA_MODULE_LOADING=EAGER).  The cached address is not
+// refreshed after cudaDeviceReset; a process that resets a device must not use
+// the library on it afterwards.
 #include <mutex>
 
 #include "common.cuh"
@@ -52,27 +61,25 @@ extern "C" int paged_decode_noalloc(const void* q, const void* k_cache, const vo
                                     const int32_t* block_table, int32_t max_blocks_per_seq,
                                     const int32_t* cache_seqlens, int32_t batch, float scale,
                                     void* out, const pkv_geom* geom, cudaStream_t stream) {
-    if (!geom || geom->num_heads <= 0 || geom->num_kv_heads <= 0 || geom->head_dim <= 0 ||
-        geom->block_size <= 0 || geom->num_blocks < 0 || geom->num_heads % geom->num_kv_heads)
-        return PKV_ERR_INVALID;
-    if (geom->dtype != PKV_F32 && geom->dtype != PKV_BF16) return PKV_ERR_INVALID;
-    if ((double)geom->num_blocks * geom->block_size > 2147483647.0) return PKV_ERR_UNSUPPORTED;
+    // the same argument checks as paged_decode (api.cu)
+    const int st = pkv::check_geom(geom);
+    if (st != PKV_OK) return st;
     if (batch < 0 || max_blocks_per_seq < 0) return PKV_ERR_INVALID;
-    if (batch == 0) return PKV_OK;
+    // batch 0 does the per-device set-up only (a warm-up call: see pagedkv.h)
+    void* scratch = nullptr;
+    if (batch == 0) return pkv::scratch_address(&scratch) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
     if (!q || !k_cache || !v_cache || !block_table || !cache_seqlens || !out)
         return PKV_ERR_INVALID;
-    auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
-    if (misaligned(q) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out))
+    if (!pkv::aligned(q, 16) || !pkv::aligned(k_cache, 16) || !pkv::aligned(v_cache, 16) ||
+        !pkv::aligned(out, 16))
         return PKV_ERR_INVALID;
     pkv::DeviceInfo dev;
     if (pkv::current_device_info(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     pkv::DecodePlan plan;
-    const int elt = geom->dtype == PKV_F32 ? 4 : 2;
     if (!pkv::plan_decode(dev, batch, geom->num_heads, geom->num_kv_heads, geom->head_dim,
-                          geom->block_size, elt, &plan))
+                          geom->block_size, pkv::elt_size(geom->dtype), &plan))
         return PKV_ERR_UNSUPPORTED;
     if (plan.ws_bytes > (size_t)PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;
-    void* scratch = nullptr;
     if (pkv::scratch_address(&scratch) != cudaSuccess) return PKV_ERR_CUDA;
     cudaError_t e = pkv::launch_decode(plan, q, k_cache, v_cache, block_table, max_blocks_per_seq,
                                        cache_seqlens, batch, scale, out, scratch,

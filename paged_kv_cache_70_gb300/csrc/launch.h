@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/pagedkv.h"
+
 namespace pkv {
 
 // Launch `kern` as a programmatic dependent of the kernel before it on
@@ -35,6 +37,19 @@ cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, siz
 #define PKV_DEPENDENT_PROLOGUE()                                  \
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); \
     asm volatile("griddepcontrol.wait;" ::: "memory")
+
+// ---- argument checks shared by the entry points -----------------------------
+inline bool aligned(const void* p, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+// bytes per element of a pkv_dtype, 0 for an unknown code
+inline int elt_size(int dtype) { return dtype == PKV_F32 ? 4 : (dtype == PKV_BF16 ? 2 : 0); }
+
+// Geometry checks common to every call taking a pkv_geom (api.cu): PKV_OK,
+// PKV_ERR_INVALID (null, non-positive sizes, Hq % Hkv != 0, unknown dtype) or
+// PKV_ERR_UNSUPPORTED (more than 2^31 - 1 slots: slot ids are int32).
+int check_geom(const pkv_geom* g);
 
 struct DeviceInfo {
     int device;

@@ -58,7 +58,8 @@
 // writes nothing they read).  The shared-prefix instantiation lets them start
 // at once.
 // Every mbarrier wait is time-limited; a timeout sets PKV_FLAG_TIMEOUT and the
-// CTA drains its copies and frees TMEM before returning.
+// CTA drains its copies, waits for its issued MMAs and frees TMEM before
+// returning.
 #include <cuda.h>
 
 #include <algorithm>
@@ -291,7 +292,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     uint64_t* p_full = s_full + 2;       // [2]
     uint64_t* o_ready = p_full + 2;      // [2] last PV of the tile done
     uint64_t* q_ready = o_ready + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
+    uint64_t* mma_done = q_ready + 1;    // every MMA of the CTA complete
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
     // The plain prefill is launched as a programmatic dependent of the kernel
     // before it (typically the write of the new rows), so it waits for that
@@ -397,6 +399,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
             mbar_init(&o_ready[x], 1);
         }
         mbar_init(q_ready, 1);
+        mbar_init(mma_done, 1);
         fence_barrier_init();
     }
     if (warp == 9) {
@@ -615,6 +618,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 mma_commit(&v_empty[sv]);
                 if (more) mma_commit(&k_empty[sk1]);
             }
+            // TMEM is freed below: first let every MMA this thread issued
+            // complete (after a timed-out wait some may still be running)
+            mma_commit(mma_done);
+            mbar_wait(mma_done, 0, a.err);
         }
     }
     } else {
