@@ -109,13 +109,17 @@ struct DecodeArgs {
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-constexpr size_t kTstartBytes = align_up((kDecodeMaxBatch + 1) * sizeof(int32_t), 128);
 __host__ __device__ constexpr size_t merge_bytes(int G, int D) {
     return align_up((size_t)kConsumerWarps * G * (D + 2) * sizeof(float), 128);
 }
-// [barriers 128 B][stage valid flags 128 B][tile starts][merge scratch][stages]
-__host__ __device__ constexpr size_t decode_fixed_smem(int G, int D) {
-    return 256 + kTstartBytes + merge_bytes(G, D);
+// per-sequence tables in shared memory: tile starts [batch + 1], first keys
+// [batch], clamped lengths [batch]
+__host__ __device__ constexpr size_t seq_table_bytes(int batch) {
+    return align_up((size_t)(batch + 1) * 4, 128) + 2 * align_up((size_t)batch * 4, 128);
+}
+// [barriers 128 B][stage valid flags 128 B][sequence tables][merge scratch][stages]
+__host__ __device__ constexpr size_t decode_fixed_smem(int G, int D, int batch) {
+    return 256 + seq_table_bytes(batch) + merge_bytes(G, D);
 }
 
 // two bf16 packed in a word -> (element 2i, element 2i+1) as fp32 (exact)
@@ -154,48 +158,50 @@ __device__ __forceinline__ int32_t clamp_len(int32_t L, int32_t cap) {
     return L < 0 ? 0 : (L > cap ? cap : L);
 }
 
-// First key of sequence b this kernel covers: 0, or in shared-prefix mode the
-// group's prefix length (a multiple of the block size, at most L; anything
-// else is flagged and rounded down to a whole tile).
-// the group of sequence b: the last g with group_cu[g] <= b (binary search)
-__device__ __forceinline__ int group_of(const DecodeArgs& a, int b) {
-    int lo = 0, hi = a.n_groups;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(a.group_cu + mid) <= b) lo = mid; else hi = mid;
-    }
-    return lo;
-}
-
-// First key of sequence b's own tiles (its group's prefix length, 0 without
-// groups).  g is the caller's group cursor: the group of a sequence at or
-// before b (a CTA walks its sequences in order, so it moves forward one
-// group at a time instead of searching).
-__device__ __forceinline__ int32_t seq_start(const DecodeArgs& a, int b, int32_t L, int& g) {
-    if (!a.group_cu) return 0;
-    while (g + 1 < a.n_groups && __ldg(a.group_cu + g + 1) <= b) ++g;
-    int32_t s = __ldg(a.group_plen + g);
-    if (s < 0 || s > L || s % a.block_size) {
-        flag_error(a.err, PKV_FLAG_BAD_LENGTH);
-        s = s < 0 ? 0 : (s > L ? L : s);
-        s -= s % a.rows;
-    }
-    return s;
-}
-
-// Exclusive scan of per-sequence tile counts into tstart[0..batch] (all threads).
-__device__ void scan_tiles(const DecodeArgs& a, int32_t* tstart) {
+// Per-sequence plan of the CTA, in shared memory (all threads take part):
+//   slen[b]   cache_seqlens[b] clamped to [0, the table's capacity];
+//   sfirst[b] first key of b's own tiles: 0, or in shared-prefix mode its
+//             group's prefix length (a multiple of the block size, at most
+//             L; anything else is flagged and rounded down to a whole tile);
+//   tstart[b] exclusive prefix sum of the tile counts, tstart[batch] = total.
+// All global loads of a step are issued together (the group bounds first,
+// then every sequence's length and prefix length), so the plan costs about
+// two memory round trips.
+__device__ void plan_tiles(const DecodeArgs& a, int32_t* tstart, int32_t* sfirst,
+                           int32_t* slen) {
     __shared__ int32_t warp_tot[kDecodeMaxWarps];
     const int tid = threadIdx.x, nthr = blockDim.x;
+    const int32_t cap = a.max_blocks * a.block_size;
+    if (a.group_cu) {
+        // group bounds into tstart (scratch until the scan below)
+        for (int g = tid; g <= a.n_groups; g += nthr) tstart[g] = __ldg(a.group_cu + g);
+        __syncthreads();
+    }
+    for (int b = tid; b < a.batch; b += nthr) {
+        const int32_t L = clamp_len(a.seqlens[b], cap);
+        int32_t st = 0;
+        if (a.group_cu) {
+            int lo = 0, hi = a.n_groups;  // the last g with group_cu[g] <= b
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (tstart[mid] <= b) lo = mid; else hi = mid;
+            }
+            st = __ldg(a.group_plen + lo);
+            if (st < 0 || st > L || st % a.block_size) {
+                flag_error(a.err, PKV_FLAG_BAD_LENGTH);
+                st = st < 0 ? 0 : (st > L ? L : st);
+                st -= st % a.rows;
+            }
+        }
+        slen[b] = L;
+        sfirst[b] = st;
+    }
+    __syncthreads();
+    // block-wide exclusive scan of the tile counts
     const int per = (a.batch + nthr - 1) / nthr;
     const int lo = tid * per, hi = min(lo + per, a.batch);
-    const int32_t cap = a.max_blocks * a.block_size;
     int32_t sum = 0;
-    int g = (a.group_cu && lo < hi) ? group_of(a, lo) : 0;
-    for (int b = lo; b < hi; ++b) {
-        const int32_t L = clamp_len(a.seqlens[b], cap);
-        sum += (L - seq_start(a, b, L, g) + a.rows - 1) / a.rows;
-    }
+    for (int b = lo; b < hi; ++b) sum += (slen[b] - sfirst[b] + a.rows - 1) / a.rows;
     const int lane = tid & 31, warp = tid >> 5;
     int32_t inc = sum;
 #pragma unroll
@@ -208,11 +214,9 @@ __device__ void scan_tiles(const DecodeArgs& a, int32_t* tstart) {
     int32_t base = 0;
     for (int w = 0; w < warp; ++w) base += warp_tot[w];
     int32_t run = base + inc - sum;  // exclusive prefix of this thread's first sequence
-    g = (a.group_cu && lo < hi) ? group_of(a, lo) : 0;
     for (int b = lo; b < hi; ++b) {
         tstart[b] = run;
-        const int32_t L = clamp_len(a.seqlens[b], cap);
-        run += (L - seq_start(a, b, L, g) + a.rows - 1) / a.rows;
+        run += (slen[b] - sfirst[b] + a.rows - 1) / a.rows;
     }
     if (tid == nthr - 1) tstart[a.batch] = base + inc;
 }
@@ -255,9 +259,10 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
     uint64_t* empty = full + kMaxStages;
     int32_t* stage_ok = reinterpret_cast<int32_t*>(smem + 128);
     int32_t* tstart = reinterpret_cast<int32_t*>(smem + 256);
-    float* mscratch = reinterpret_cast<float*>(smem + 256 + kTstartBytes);
-    unsigned char* stage_base = smem + decode_fixed_smem(G, D);
-
+    int32_t* sfirst = tstart + align_up((size_t)(a.batch + 1) * 4, 128) / 4;
+    int32_t* slen = sfirst + align_up((size_t)a.batch * 4, 128) / 4;
+    float* mscratch = reinterpret_cast<float*>(smem + 256 + seq_table_bytes(a.batch));
+    unsigned char* stage_base = smem + decode_fixed_smem(G, D, a.batch);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = a.stages, R = a.rows, HC = a.hc;
@@ -279,9 +284,13 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
     // for this grid's results).  After the wait above, so that one that does
     // not wait would still start only after everything before this grid.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    scan_tiles(a, tstart);
+    plan_tiles(a, tstart, sfirst, slen);
     __syncthreads();
 
+    // Holding the grid open (see DecodeArgs::wait_prior): block (0, 0) does
+    // not exit before the kernel launched before this one has completed.
+    // Its producer waits after issuing its copies; with no work it waits here.
+    const bool holder = a.wait_prior && blockIdx.x == 0 && blockIdx.y == 0;
     const int32_t total = tstart[a.batch];
     if (blockIdx.x == 0 && blockIdx.y == 0) {
         for (int b = threadIdx.x; b <= a.batch; b += blockDim.x) a.tstart_out[b] = tstart[b];
@@ -290,11 +299,13 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
             if (L < 0 || L > cap) flag_error(a.err, PKV_FLAG_BAD_LENGTH);
         }
     }
-    if (total == 0) return;
-    const int32_t chunk = (total + gridDim.x - 1) / gridDim.x;
+    const int32_t chunk = total > 0 ? (total + gridDim.x - 1) / gridDim.x : 0;
     const int32_t t0 = blockIdx.x * chunk;
     const int32_t t1 = min(t0 + chunk, total);
-    if (t0 >= t1) return;
+    if (t0 >= t1) {
+        if (holder && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+        return;
+    }
     const int head0 = blockIdx.y * HC;  // first KV head of this CTA
 
     if (warp >= kConsumerWarps) {
@@ -303,63 +314,77 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
             if (warp > kConsumerWarps) return;  // only completed the producer's warpgroup
         }
         // ------------------------------ producer ------------------------------
-        // an otherwise idle lane holds the grid open until the kernel launched
-        // before it has completed (the combine waits for this grid)
-        if (a.wait_prior && lane == 31 && blockIdx.x == 0 && blockIdx.y == 0)
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-        if (lane != 0) return;
+        // The 32 lanes prepare 32 tiles at a time (sequence, first key, rows,
+        // block-table entry: the entries of a batch are read together); lane 0
+        // waits for ring slots and issues the copies.
+        const uint64_t pol = l2_evict_first_policy();
+        const unsigned all = 0xffffffffu;
 #ifdef PKV_TEST_SPLIT_PRODUCER_IDLE
         // test-only build: issue nothing, so the consumers' first wait runs out
+        if (holder && lane == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
         return;
 #endif
-        const uint64_t pol = l2_evict_first_policy();
-        int b = seq_of_tile(tstart, a.batch, t0);
-        int g = a.group_cu ? group_of(a, b) : 0;
-        int32_t L = clamp_len(a.seqlens[b], cap);
-        int32_t st = seq_start(a, b, L, g);
-        int32_t k = 0;  // stages filled so far
-        for (int32_t t = t0; t < t1; ++t, ++k) {
-            while (t >= tstart[b + 1]) {
-                ++b;
-                L = clamp_len(a.seqlens[b], cap);
-                st = seq_start(a, b, L, g);
+        int32_t k = 0;  // stages filled so far (lane 0)
+        bool stop = false;
+        for (int32_t tb = t0; tb < t1; tb += 32) {
+            // lane i: tile tb + i's block-table entry and (first key's slot in
+            // the block) * 64 + rows (rows <= 32); the batch's table reads are
+            // covered by the stages still queued in the ring
+            int32_t my_phys = 0, my_slot_rows = 0;
+            if (tb + lane < t1) {
+                const int32_t t = tb + lane;
+                const int bb = seq_of_tile(tstart, a.batch, t);
+                const int32_t pos0 = sfirst[bb] + (t - tstart[bb]) * R;
+                my_slot_rows = (pos0 % a.block_size) * 64 + min(R, slen[bb] - pos0);
+                my_phys = a.table[(int64_t)bb * a.max_blocks + pos0 / a.block_size];
             }
-            const int s = k % S;
-            if (!mbar_wait(&empty[s], ((k / S) & 1) ^ 1, a.err)) break;
-            const int32_t pos0 = st + (t - tstart[b]) * R;
-            const int32_t rows = min(R, L - pos0);
-            const int32_t phys = a.table[(int64_t)b * a.max_blocks + pos0 / a.block_size];
-            if (phys < 0 || phys >= a.num_blocks) {
-                flag_error(a.err, PKV_FLAG_BAD_BLOCK);
-                stage_ok[s] = 0;
-                mbar_arrive(&full[s]);
-                continue;
-            }
-            stage_ok[s] = 1;
-            const int64_t row0 = (int64_t)phys * a.block_size + pos0 % a.block_size;
-            unsigned char* kd = stage_base + (size_t)s * 2 * half_bytes;
-            unsigned char* vd = kd + half_bytes;
-            const uint32_t bytes = (uint32_t)(rows * row_bytes);
-            mbar_arrive_expect_tx(&full[s], 2 * bytes);
-            if (HC == a.hkv) {
-                const size_t off = (size_t)row0 * row_bytes;
-                bulk_g2s(kd, a.k_cache + off, bytes, &full[s], pol);
-                bulk_g2s(vd, a.v_cache + off, bytes, &full[s], pol);
-            } else {
-                const size_t pool_row = (size_t)a.hkv * D * ELT;
-                for (int r = 0; r < rows; ++r) {
-                    const size_t off = (size_t)(row0 + r) * pool_row + (size_t)head0 * D * ELT;
-                    bulk_g2s(kd + r * row_bytes, a.k_cache + off, (uint32_t)row_bytes, &full[s], pol);
-                    bulk_g2s(vd + r * row_bytes, a.v_cache + off, (uint32_t)row_bytes, &full[s], pol);
+            const int n = min(32, t1 - tb);
+            for (int i = 0; i < n; ++i) {
+                const int32_t phys = __shfl_sync(all, my_phys, i);
+                const int32_t slot_rows = __shfl_sync(all, my_slot_rows, i);
+                if (lane != 0 || stop) continue;
+                const int32_t rows = slot_rows & 63, off = slot_rows >> 6;
+                const int s = k % S;
+                if (!mbar_wait(&empty[s], ((k / S) & 1) ^ 1, a.err)) {
+                    stop = true;
+                    continue;
+                }
+                ++k;
+                if (phys < 0 || phys >= a.num_blocks) {
+                    flag_error(a.err, PKV_FLAG_BAD_BLOCK);
+                    stage_ok[s] = 0;
+                    mbar_arrive(&full[s]);
+                    continue;
+                }
+                stage_ok[s] = 1;
+                const int64_t row0 = (int64_t)phys * a.block_size + off;
+                unsigned char* kd = stage_base + (size_t)s * 2 * half_bytes;
+                unsigned char* vd = kd + half_bytes;
+                const uint32_t bytes = (uint32_t)(rows * row_bytes);
+                mbar_arrive_expect_tx(&full[s], 2 * bytes);
+                if (HC == a.hkv) {
+                    const size_t o = (size_t)row0 * row_bytes;
+                    bulk_g2s(kd, a.k_cache + o, bytes, &full[s], pol);
+                    bulk_g2s(vd, a.v_cache + o, bytes, &full[s], pol);
+                } else {
+                    const size_t pool_row = (size_t)a.hkv * D * ELT;
+                    for (int r = 0; r < rows; ++r) {
+                        const size_t o = (size_t)(row0 + r) * pool_row + (size_t)head0 * D * ELT;
+                        bulk_g2s(kd + r * row_bytes, a.k_cache + o, (uint32_t)row_bytes, &full[s], pol);
+                        bulk_g2s(vd + r * row_bytes, a.v_cache + o, (uint32_t)row_bytes, &full[s], pol);
+                    }
                 }
             }
+            if (__shfl_sync(all, stop ? 1 : 0, 0)) break;
         }
+        if (lane != 0) return;
         // The CTA must not exit while a copy into its shared memory is in
         // flight: wait (time-limited) for the last fill of every stage.  In a
         // normal run the consumers wait for the same phases, so this costs
         // nothing; after a timeout the consumers may have stopped waiting.
         for (int32_t j = k > S ? k - S : 0; j < k; ++j)
             if (!mbar_wait(&full[j % S], (j / S) & 1, a.err)) break;
+        if (holder) asm volatile("griddepcontrol.wait;" ::: "memory");
         return;
     }
 
@@ -378,7 +403,6 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
     float2 q2[G][8], o2[G][8];
     float m[G], l[G];
     int b = seq_of_tile(tstart, a.batch, t0);
-    int gcur = a.group_cu ? group_of(a, b) : 0;
     int loaded = -1;
     int32_t L = 0, st = 0;
 
@@ -397,8 +421,8 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
                 load8_global<BF16>(a.q, qb + dim0, &q2[g][0]);
                 load8_global<BF16>(a.q, qb + dim1, &q2[g][4]);
             }
-            L = clamp_len(a.seqlens[b], cap);
-            st = seq_start(a, b, L, gcur);
+            L = slen[b];
+            st = sfirst[b];
             const float2 sc2 = make_float2(a.qscale, a.qscale);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
@@ -599,155 +623,147 @@ struct CombineArgs {
     unsigned int* err;
 };
 
+constexpr int kCombineWarps = 4;  // (sequence, head) pairs per CTA of the combine
+
 // DPL consecutive elements of a bf16 or fp32 row as fp32
 template <bool BF16, int DPL>
 __device__ __forceinline__ void load_row(const void* base, int64_t elem, float* x) {
+    if constexpr (BF16) {
+        const uint16_t* p = static_cast<const uint16_t*>(base) + elem;
+        if constexpr (DPL == 4) {
+            const uint2 w = *reinterpret_cast<const uint2*>(p);
+            x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
+        } else {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+            x[0] = bf16lo(w); x[1] = bf16hi(w);
+        }
+    } else {
+        const float* p = static_cast<const float*>(base) + elem;
+        if constexpr (DPL == 4) {
+            const float4 w = *reinterpret_cast<const float4*>(p);
+            x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
+        } else {
+            const float2 w = *reinterpret_cast<const float2*>(p);
+            x[0] = w.x; x[1] = w.y;
+        }
+    }
+}
+
+// The boxed merge rule applied to a running state (M, L, acc) and one more
+// state (m, l, o): M' = max(M, m), both sides rescaled by 2^(. - M').  A state
+// with m = -inf holds nothing and is skipped.
+template <int DPL>
+__device__ __forceinline__ void merge_state(float& M, float& L, float* acc, float m, float l,
+                                            const float* o) {
+    if (m == -INFINITY) return;
+    const float Mn = fmaxf(M, m);
+    const float a = (M == -INFINITY) ? 0.f : ex2(M - Mn);
+    const float w = ex2(m - Mn);
+    L = L * a + l * w;
 #pragma unroll
-    for (int e = 0; e < DPL; ++e)
-        x[e] = BF16 ? __uint_as_float((uint32_t) static_cast<const uint16_t*>(base)[elem + e] << 16)
-                    : static_cast<const float*>(base)[elem + e];
+    for (int e = 0; e < DPL; ++e) acc[e] = acc[e] * a + o[e] * w;
+    M = Mn;
 }
 
 // Merge the partial states of every (sequence, head) and normalise.  One warp
-// per (sequence, head); lane i owns dims [i*D/32, (i+1)*D/32).  Shared-prefix
+// per (sequence, head); lane i owns dims [i*D/32, (i+1)*D/32).  Each state
+// joins a running (M, L, acc) by the boxed rule as it arrives, so the loads of
+// U split pieces (and, first, of the prefix chunks and the new key) are in
+// flight together: a sequence with up to U pieces costs two dependent memory
+// round trips after the split (the tile starts, then everything else).  U is
+// 16 for batches of few sequences (long contexts, many pieces each) and 4 for
+// large batches, whose warps must all fit on the GPU at once.  Shared-prefix
 // mode adds the prefix chunks, each as the state (m = lse, l = 1, o = out);
-// append mode adds the new key (m = its score, l = 1, o = its V row) and
-// writes the new K/V row into the cache (the split kernel, which read only
-// the keys before it, has completed).
-template <int D, bool BF16>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const CombineArgs c) {
+// append mode adds the new key (m = its score, l = 1, o = its V row) and the
+// first warp of each KV head writes the new K/V row into the cache (the split
+// kernel, which read only the keys before it, has completed).
+template <int D, bool BF16, int U>
+__global__ void __launch_bounds__(kCombineWarps * 32, U > 4 ? 4 : 8)
+decode_combine_kernel(const CombineArgs c) {
     constexpr int DPL = D / 32;
     // wait until the split kernel's partials are complete and visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
-    const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int64_t w = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
     const int hq = c.hq, batch = c.batch;
     if (w >= (int64_t)batch * hq) return;
     const int b = (int)(w / hq), h = (int)(w % hq);
     const int32_t total = c.tstart[batch];
     const int32_t tb0 = c.tstart[b], tb1 = c.tstart[b + 1];
-    float acc[DPL];
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-    float lt = 0.f;
     const int32_t chunk = total > 0 ? (total + c.ctas - 1) / c.ctas : 1;
     const int c0 = tb0 / chunk, c1 = tb1 > tb0 ? (tb1 - 1) / chunk : c0 - 1;
     const int64_t xstride = (int64_t)batch * hq;  // one prefix chunk's (sequence, head) count
-    float M = -INFINITY;
-    for (int x = lane; x < c.x_chunks; x += 32)
-        M = fmaxf(M, c.x_lse[x * xstride + (int64_t)b * hq + h]);
-    for (int cc = c0 + lane; cc <= c1; cc += 32)
-        M = fmaxf(M, c.part_ml[(((int64_t)cc + b) * hq + h) * 2]);
+    const int64_t bh = (int64_t)b * hq + h;
+    const int G = hq / (c.hkv > 0 ? c.hkv : 1);
+    const int kvh = h / G;
+    float M = -INFINITY, L = 0.f, acc[DPL];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    // the appended key: score q . k_new in log2 units
-    const int kvh = h / (hq / (c.hkv > 0 ? c.hkv : 1));
-    float s_new = -INFINITY, v_new[DPL];
-    if (c.k_new) {
+    for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+    if (c.k_new) {  // the appended key: score q . k_new in log2 units
         const int64_t row = ((int64_t)b * c.hkv + kvh) * D + lane * DPL;
-        float qv[DPL], kv[DPL];
-        load_row<BF16, DPL>(c.q, ((int64_t)b * hq + h) * D + lane * DPL, qv);
+        float qv[DPL], kv[DPL], vv[DPL];
+        load_row<BF16, DPL>(c.q, bh * D + lane * DPL, qv);
         load_row<BF16, DPL>(c.k_new, row, kv);
-        load_row<BF16, DPL>(c.v_new, row, v_new);
+        load_row<BF16, DPL>(c.v_new, row, vv);
         float dot = 0.f;
 #pragma unroll
         for (int e = 0; e < DPL; ++e) dot = fmaf(qv[e], kv[e], dot);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-        s_new = dot * c.qscale;
-        M = fmaxf(M, s_new);
+        merge_state<DPL>(M, L, acc, dot * c.qscale, 1.f, vv);
     }
-    if (M != -INFINITY) {
-        // pieces in rounds of 32: lane i reads piece i's (m, l), so a round
-        // costs one dependent load; each piece's weight then reaches every
-        // lane by shuffle and the o rows stream in independent loads
-        float lp = 0.f;  // this lane's share of the pieces' l
-        for (int base = c0; base <= c1; base += 32) {
-            const int n = min(32, c1 - base + 1);
-            float wl = 0.f;
-            if (lane < n) {
-                const float2 ml = *reinterpret_cast<const float2*>(
-                    c.part_ml + ((int64_t)(base + lane + b) * hq + h) * 2);
-                wl = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
-                lp += ml.y * wl;
-            }
-            // the round's o rows all in flight at once (predicated loads; rows
-            // past n are zero and their weight is 0: wl is 0 on lanes >= n)
-            float v[32][DPL];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) v[i][e] = 0.f;
-                if (i < n) {
-                    const float* src =
-                        c.part_o + ((int64_t)(base + i + b) * hq + h) * D + lane * DPL;
-                    if constexpr (DPL == 4) {
-                        const float4 t = *reinterpret_cast<const float4*>(src);
-                        v[i][0] = t.x; v[i][1] = t.y; v[i][2] = t.z; v[i][3] = t.w;
-                    } else {
-                        const float2 t = *reinterpret_cast<const float2*>(src);
-                        v[i][0] = t.x; v[i][1] = t.y;
-                    }
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float wgt = __shfl_sync(0xffffffffu, wl, i);
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) acc[e] = fmaf(v[i][e], wgt, acc[e]);
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) lp += __shfl_xor_sync(0xffffffffu, lp, off);
-        lt += lp;
-        for (int x = 0; x < c.x_chunks; ++x) {
-            const float mx = c.x_lse[x * xstride + (int64_t)b * hq + h];
-            if (mx == -INFINITY) continue;
-            const float wgt = ex2(mx - M);
-            lt += wgt;
-            const uint16_t* src = c.x_out + (x * xstride + (int64_t)b * hq + h) * D + lane * DPL;
-#pragma unroll
-            for (int e = 0; e < DPL; e += 2) {
-                const uint32_t pr = *reinterpret_cast<const uint32_t*>(src + e);
-                acc[e] += bf16lo(pr) * wgt;
-                acc[e + 1] += bf16hi(pr) * wgt;
-            }
-        }
-        if (c.k_new) {
-            const float wgt = ex2(s_new - M);
-            lt += wgt;
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) acc[e] = fmaf(v_new[e], wgt, acc[e]);
-        }
+    for (int x = 0; x < c.x_chunks; ++x) {
+        float xo[DPL];
+        const float mx = c.x_lse[x * xstride + bh];
+        load_row<true, DPL>(c.x_out, (x * xstride + bh) * D + lane * DPL, xo);
+        merge_state<DPL>(M, L, acc, mx, 1.f, xo);
     }
-    const float inv = lt > 0.f ? 1.f / lt : 0.f;
-    const int64_t oi = ((int64_t)b * hq + h) * D + lane * DPL;
+    for (int base = c0; base <= c1; base += U) {
+        float2 ml[U];
+        float o[U][DPL];
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            ml[i] = make_float2(-INFINITY, 0.f);
+            if (base + i <= c1) {
+                const int64_t slot = (int64_t)(base + i) + b;
+                ml[i] = *reinterpret_cast<const float2*>(c.part_ml + (slot * hq + h) * 2);
+                load_row<false, DPL>(c.part_o, (slot * hq + h) * D + lane * DPL, o[i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < U; ++i) merge_state<DPL>(M, L, acc, ml[i].x, ml[i].y, o[i]);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int64_t oi = bh * D + lane * DPL;
     if constexpr (BF16) {
         uint16_t* o = static_cast<uint16_t*>(c.out) + oi;
-#pragma unroll
-        for (int e = 0; e < DPL; e += 2)
-            *reinterpret_cast<uint32_t*>(o + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+        if constexpr (DPL == 4) {
+            *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                                      pack_bf16x2(acc[2] * inv, acc[3] * inv));
+        } else {
+            *reinterpret_cast<uint32_t*>(o) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        }
     } else {
         float* o = static_cast<float*>(c.out) + oi;
 #pragma unroll
         for (int e = 0; e < DPL; ++e) o[e] = acc[e] * inv;
     }
-    // one warp per KV head writes the new K/V row into the cache
-    if (c.k_new && h % (hq / c.hkv) == 0) {
-        const int32_t L = c.seqlens[b];
+    // the first warp of each KV head writes the new K/V row into the cache
+    if (c.k_new && h % G == 0) {
+        const int32_t Lb = c.seqlens[b];
         const int32_t B = c.block_size;
-        if (L < 0 || L >= c.max_blocks * B) {
+        if (Lb < 0 || Lb >= c.max_blocks * B) {
             if (lane == 0) flag_error(c.err, PKV_FLAG_BAD_LENGTH);
             return;
         }
-        const int32_t phys = c.table[(int64_t)b * c.max_blocks + L / B];
+        const int32_t phys = c.table[(int64_t)b * c.max_blocks + Lb / B];
         if (phys < 0 || phys >= c.num_blocks) {
             if (lane == 0) flag_error(c.err, PKV_FLAG_BAD_BLOCK);
             return;
         }
         constexpr int ELT = BF16 ? 2 : 4;
         const int64_t src = ((int64_t)b * c.hkv + kvh) * D + lane * DPL;
-        const int64_t dst = (((int64_t)phys * B + L % B) * c.hkv + kvh) * D + lane * DPL;
+        const int64_t dst = (((int64_t)phys * B + Lb % B) * c.hkv + kvh) * D + lane * DPL;
 #pragma unroll
         for (int e = 0; e < DPL * ELT; e += 4) {
             *reinterpret_cast<uint32_t*>(c.k_cache + dst * ELT + e) =
@@ -776,6 +792,7 @@ bool plan_decode(const DeviceInfo& dev, int32_t batch, int hq, int hkv, int d, i
     const int G = hq / hkv;
     if (G != 1 && G != 2 && G != 4) return false;
     if (batch < 0 || batch > kDecodeMaxBatch) return false;
+    if (block_size > (1 << 24)) return false;  // the producer packs slot * 64 + rows
     int HC;
     if (hkv <= kConsumerWarps) {
         if (kConsumerWarps % hkv) return false;
@@ -791,7 +808,7 @@ bool plan_decode(const DeviceInfo& dev, int32_t batch, int hq, int hkv, int d, i
     if (cap_rows > 32) cap_rows = 32;
     const int R = largest_pow2_divisor(block_size, cap_rows);
     const size_t stage = 2 * (size_t)R * row_bytes;
-    const size_t fixed = decode_fixed_smem(G, d);
+    const size_t fixed = decode_fixed_smem(G, d, batch);
     if (dev.max_smem_optin < fixed + 2 * stage) return false;
     int stages = (int)((dev.max_smem_optin - fixed) / stage);
     if (stages > kMaxStages) stages = kMaxStages;
@@ -817,11 +834,14 @@ static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a,
     e = launch_dependent(kern, dim3(plan.ctas, plan.head_groups), dim3(decode_threads<G>()),
                          plan.smem_bytes, stream, a);
     if (e != cudaSuccess) return e;
-    // combine: programmatic dependent of the split kernel
+    // combine: programmatic dependent of the split kernel, one warp per
+    // (sequence, head); 16 pieces in flight per round while every warp of
+    // the batch still fits on the GPU at once (4 warps a CTA, 4 CTAs an SM),
+    // else 4
     cudaLaunchConfig_t cfg = {};
     const int64_t warps = (int64_t)a.batch * a.hq;
-    cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
-    cfg.blockDim = dim3(128);
+    cfg.gridDim = dim3((unsigned)((warps + kCombineWarps - 1) / kCombineWarps));
+    cfg.blockDim = dim3(kCombineWarps * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -829,7 +849,9 @@ static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, BF16>, c);
+    if (warps <= (int64_t)plan.ctas * plan.head_groups * 4 * kCombineWarps)
+        return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, BF16, 16>, c);
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, BF16, 4>, c);
 }
 
 cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_cache,

@@ -67,6 +67,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tcgen05.cuh"
 
 namespace pkv {
 
@@ -85,18 +86,12 @@ constexpr int kRegsLow = 88;
 constexpr int kRegsHigh = 208;
 static_assert(8 * kRegsHigh + 4 * kRegsLow <= 12 * 168, "register split exceeds the launch");
 constexpr int kTmemCols = 512;
-constexpr uint32_t kRegionBytes = BN * 128;   // 16 KiB: 64 dims (128 B) x 128 rows
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // rescale when the row max grows by > 2^8
 
 
 constexpr uint32_t BAR_BYTES = 256;
 
-// instruction descriptors: D fp32, A/B bf16, M = 128, N = n
-constexpr uint32_t idesc(uint32_t b_mn_major, int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (b_mn_major << 16) |
-           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-}
 constexpr uint32_t IDESC_QK = idesc(0, BN);  // S = Q K^T: N = 128 keys
 
 // Per head_dim: a Q, K or V tile is 128 rows of HD bf16 in HD / 64 swizzled
@@ -113,116 +108,6 @@ struct Shape {
     static constexpr size_t kSmemBytes = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
     static constexpr uint32_t IDESC_PV = idesc(1, HD);
 };
-
-__device__ __forceinline__ void fence_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory descriptors split into 32-bit halves: the high word (stride
-// byte offset, version, 128-byte swizzle) is fixed per operand layout, the low
-// word holds (leading byte offset >> 4) << 16 | (address >> 4), so stepping an
-// operand is one 32-bit add (addresses stay below 256 KiB: no carry).
-constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
-__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
-    return ((lbo >> 4) << 16) | ((saddr & 0x3FFFFu) >> 4);
-}
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
-                                       uint32_t id, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "mov.b64 da, {%1, %5};\n\t"
-        "mov.b64 db, {%2, %5};\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_lo), "r"(b_lo), "r"(id), "r"(accumulate), "n"(kDescHi)
-        : "memory");
-}
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
-                                       uint32_t id, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "mov.b64 db, {%2, %5};\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "r"(b_lo), "r"(id), "r"(accumulate), "n"(kDescHi)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
-#define PKV_R32(p) \
-    "=r"(p[0]), "=r"(p[1]), "=r"(p[2]), "=r"(p[3]), "=r"(p[4]), "=r"(p[5]), "=r"(p[6]), \
-    "=r"(p[7]), "=r"(p[8]), "=r"(p[9]), "=r"(p[10]), "=r"(p[11]), "=r"(p[12]), "=r"(p[13]), \
-    "=r"(p[14]), "=r"(p[15]), "=r"(p[16]), "=r"(p[17]), "=r"(p[18]), "=r"(p[19]), "=r"(p[20]), \
-    "=r"(p[21]), "=r"(p[22]), "=r"(p[23]), "=r"(p[24]), "=r"(p[25]), "=r"(p[26]), "=r"(p[27]), \
-    "=r"(p[28]), "=r"(p[29]), "=r"(p[30]), "=r"(p[31])
-#define PKV_W32(p) \
-    "r"(p[0]), "r"(p[1]), "r"(p[2]), "r"(p[3]), "r"(p[4]), "r"(p[5]), "r"(p[6]), "r"(p[7]), \
-    "r"(p[8]), "r"(p[9]), "r"(p[10]), "r"(p[11]), "r"(p[12]), "r"(p[13]), "r"(p[14]), \
-    "r"(p[15]), "r"(p[16]), "r"(p[17]), "r"(p[18]), "r"(p[19]), "r"(p[20]), "r"(p[21]), \
-    "r"(p[22]), "r"(p[23]), "r"(p[24]), "r"(p[25]), "r"(p[26]), "r"(p[27]), "r"(p[28]), \
-    "r"(p[29]), "r"(p[30]), "r"(p[31])
-
-// 32 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-        "%28, %29, %30, %31}, [%32];"
-        : PKV_R32(r)
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-        "%28, %29, %30, %31, %32};" ::"r"(taddr),
-        PKV_W32(r)
-        : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() {
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y,
-                                            int z, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// shared -> global TMA store of one box (completion tracked by bulk groups)
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x,
-                                             int y, int z) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
-        : "memory");
-}
-
-// byte offset of 16-byte chunk `c` (0..15) of row `r` in a 128-row x 256-byte
-// tile stored as two 128-byte-swizzled regions (the layout TMA writes with
-// CU_TENSOR_MAP_SWIZZLE_128B and the MMA reads as a K-major operand)
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-    return (uint32_t)((c >> 3) * kRegionBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
 
 struct PrefillArgs {
     uint16_t* out;
@@ -256,17 +141,6 @@ struct PrefillArgs {
     int32_t causal;
     int32_t pair_tiles;  // 1: a CTA takes query tiles qt and qt - 1 of one head
 };
-
-// v[x] for a runtime x in {0, 1} without indexing the array (which would
-// put it in local memory)
-template <typename T>
-__device__ __forceinline__ T pick(const T (&v)[2], int x) {
-    return x ? v[1] : v[0];
-}
-
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* err) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
-}
 
 // kExt: the per-request key counts / table rows, key chunks and log2-sum-exp
 // output of PrefillArgs are in use (a separate instantiation, so the plain
@@ -830,43 +704,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static std::once_flag once;
-    static EncodeTiledFn fn = nullptr;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-// [rows, heads, hd] bf16 viewed as 3-D (dim, head, row); box (64 dims, 1
-// head, piece rows), 128-byte swizzle.  Serves the K/V pools (rows = slots)
-// and q (rows = query tokens, piece = 128).
-bool make_rows_map(CUtensorMap* map, const void* base, int hkv, int64_t rows, int piece,
-                   int hd) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)hkv, (cuuint64_t)rows};
-    cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)hkv * hd * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)piece};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
-                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 size_t prefill_workspace_bytes(int32_t, int32_t, int) { return 0; }

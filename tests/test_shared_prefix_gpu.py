@@ -80,6 +80,7 @@ def build_groups(rng, sizes, prefixes, suffix_max, B, hq=16, hkv=8, d=128):
     ([3, 3], [256, 512], 0, 256),                      # some members have no own keys
     ([7], [128], 700, 64),
     ([2, 2, 2], [0, 0, 0], 200, 32),                   # no sharing at all
+    ([32] * 8, [4096] * 8, 0, 16),                     # prefix only: the split has no tile
 ])
 def test_groups(sizes, prefixes, suffix_max, B):
     rng = np.random.default_rng(sum(sizes) + B)
