@@ -227,6 +227,47 @@ size_t paged_decode_shared_prefix_workspace_size(int32_t batch, const pkv_geom* 
     return dec + shared_prefix_extra_bytes(batch, geom);
 }
 
+// The shared-prefix pass of a grouped decode: one work item per (group, KV
+// head, key chunk, block of 128 / G members); the keys are cut into enough
+// chunks for the items to cover the SMs once.  Fills *kchunks_out.
+static cudaError_t launch_prefix_pass(const DeviceInfo& dev, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* table,
+                                      int32_t max_blocks, int32_t batch, const int32_t* group_cu,
+                                      const int32_t* group_plen, int32_t n_groups,
+                                      int32_t max_group_size, float scale, void* x_out,
+                                      float* x_lse, const pkv_geom* g, bool pdl,
+                                      cudaStream_t stream, int* kchunks_out) {
+    const int G = g->num_heads / g->num_kv_heads;
+    const int per_blk = G <= 128 ? 128 / G : 1;
+    const int units = n_groups * g->num_kv_heads * ((max_group_size + per_blk - 1) / per_blk);
+    int kchunks = units > 0 ? dev.num_sms / units : 1;
+    kchunks = kchunks < 1 ? 1 : (kchunks > kMaxPrefixChunks ? kMaxPrefixChunks : kchunks);
+    pkv::PrefixLaunch p{};
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.table = table;
+    p.group_cu = group_cu;
+    p.group_plen = group_plen;
+    p.x_out = x_out;
+    p.x_lse = x_lse;
+    p.err = dev.err;
+    p.num_blocks = g->num_blocks;
+    p.scale = scale;
+    p.max_blocks = max_blocks;
+    p.batch = batch;
+    p.hq = g->num_heads;
+    p.hkv = g->num_kv_heads;
+    p.hd = g->head_dim;
+    p.block_size = g->block_size;
+    p.n_groups = n_groups;
+    p.max_group_size = max_group_size;
+    p.kchunks = kchunks;
+    p.pdl = pdl;
+    *kchunks_out = kchunks;
+    return pkv::launch_prefix(dev, p, stream);
+}
+
 int paged_decode_shared_prefix(const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* block_table, int32_t max_blocks_per_seq,
                                const int32_t* cache_seqlens, int32_t batch,
@@ -258,21 +299,14 @@ int paged_decode_shared_prefix(const void* q, const void* k_cache, const void* v
     unsigned char* x_out = static_cast<unsigned char*>(workspace) + plan.ws_bytes;
     float* x_lse = reinterpret_cast<float*>(
         x_out + align256((size_t)kMaxPrefixChunks * batch * geom->num_heads * geom->head_dim * 2));
-    // enough (group, chunk, head pair, query tile) items to cover the SMs once
-    const int units = n_groups * (geom->num_heads / geom->num_kv_heads % 2 == 0
-                                      ? geom->num_heads / 2 : geom->num_heads) *
-                      ((max_group_size + 127) / 128);
-    int kchunks = units > 0 ? dev.num_sms / units : 1;
-    kchunks = kchunks < 1 ? 1 : (kchunks > kMaxPrefixChunks ? kMaxPrefixChunks : kchunks);
-    // 1. the prefix of every group, once: non-causal attention of the group's
-    //    queries over its first group_prefix_len[g] keys, read through the
-    //    block-table row of the group's first sequence (tensor cores)
-    pkv::PrefillExtra ex{group_prefix_len, group_cu, x_lse, kchunks, batch};
-    cudaError_t e = pkv::launch_prefill(dev, q, k_cache, v_cache, group_cu, group_cu, n_groups,
-                                        max_group_size, 0, block_table, max_blocks_per_seq, 0,
-                                        scale, x_out, nullptr, geom->num_heads,
-                                        geom->num_kv_heads, geom->head_dim, geom->block_size,
-                                        geom->num_blocks, dev.err, stream, &ex);
+    // 1. the prefix of every group, once: attention of the group's queries
+    //    over its first group_prefix_len[g] keys, read through the block-table
+    //    row of the group's first sequence (tensor cores)
+    int kchunks = 1;
+    cudaError_t e = launch_prefix_pass(dev, q, k_cache, v_cache, block_table, max_blocks_per_seq,
+                                       batch, group_cu, group_prefix_len, n_groups,
+                                       max_group_size, scale, x_out, x_lse, geom, false, stream,
+                                       &kchunks);
     if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return PKV_ERR_CUDA;
     // 2. each sequence's own keys after the prefix, merged with the prefix state.
@@ -365,18 +399,12 @@ int paged_mixed_step(const pkv_mixed_step* s, void* k_cache, void* v_cache, void
         float* x_lse = reinterpret_cast<float*>(
             x_out + align256((size_t)kMaxPrefixChunks * s->decode_batch * geom->num_heads *
                              geom->head_dim * 2));
-        const int units = s->n_groups * (geom->num_heads / geom->num_kv_heads % 2 == 0
-                                             ? geom->num_heads / 2 : geom->num_heads) *
-                          ((s->max_group_size + 127) / 128);
-        int kchunks = units > 0 ? dev.num_sms / units : 1;
-        kchunks = kchunks < 1 ? 1 : (kchunks > kMaxPrefixChunks ? kMaxPrefixChunks : kchunks);
-        pkv::PrefillExtra ex{s->group_prefix_len, s->group_cu, x_lse, kchunks, s->decode_batch,
-                             chained};
-        cudaError_t e = pkv::launch_prefill(
-            dev, s->decode_q, k_cache, v_cache, s->group_cu, s->group_cu, s->n_groups,
-            s->max_group_size, 0, s->decode_table, s->decode_max_blocks, 0, s->scale, x_out,
-            nullptr, geom->num_heads, geom->num_kv_heads, geom->head_dim, geom->block_size,
-            geom->num_blocks, dev.err, stream, &ex);
+        int kchunks = 1;
+        cudaError_t e = launch_prefix_pass(dev, s->decode_q, k_cache, v_cache, s->decode_table,
+                                           s->decode_max_blocks, s->decode_batch, s->group_cu,
+                                           s->group_prefix_len, s->n_groups, s->max_group_size,
+                                           s->scale, x_out, x_lse, geom, chained, stream,
+                                           &kchunks);
         if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
         if (e != cudaSuccess) return PKV_ERR_CUDA;
         sp = pkv::SharedPrefix{s->group_cu, s->group_prefix_len, s->n_groups, x_out, x_lse,

@@ -131,18 +131,31 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
                           const DecodeAppend* append = nullptr,
                           const DecodeChain* chain = nullptr);
 
+// ---- shared-prefix pass (prefix.cu) --------------------------------------------
+// For every group of consecutive sequences sharing their first group_plen[g]
+// keys: attention of all the group's queries over those keys (in kchunks key
+// chunks), written as normalised bf16 rows x_out [kchunks, batch, hq, hd] and
+// log2-sum-exp x_lse [kchunks, batch, hq] for the decode's merge.
+struct PrefixLaunch {
+    const void* q;              // [batch, hq, hd] bf16
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* table;       // [batch, max_blocks]; a group reads its first member's row
+    const int32_t* group_cu;    // [n_groups + 1]
+    const int32_t* group_plen;  // [n_groups]
+    void* x_out;
+    float* x_lse;
+    unsigned int* err;
+    int64_t num_blocks;
+    float scale;
+    int32_t max_blocks, batch, hq, hkv, hd, block_size, n_groups, max_group_size, kchunks;
+    bool pdl;                   // launch as a programmatic dependent of the previous kernel
+};
+
+cudaError_t launch_prefix(const DeviceInfo& dev, const PrefixLaunch& p, cudaStream_t stream);
+
 // ---- prefill ----------------------------------------------------------------
 size_t prefill_workspace_bytes(int32_t batch, int32_t max_seqlen_q, int hq);
-
-// optional per-request inputs and outputs of the prefill kernel (see prefill.cu)
-struct PrefillExtra {
-    const int32_t* req_klen;
-    const int32_t* req_table_row;
-    float* lse;
-    int32_t kchunks;     // key chunks per request (non-causal), 1 = none
-    int32_t chunk_rows;  // output rows of one chunk (kchunks > 1)
-    bool pdl;            // launch as a programmatic dependent of the previous kernel
-};
 
 cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_cache,
                            const void* v_cache, const int32_t* cu_q, const int32_t* cu_k,
@@ -150,6 +163,6 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
                            const int32_t* block_table, int32_t max_blocks, int causal,
                            float scale, void* out, void* workspace, int hq, int hkv, int d,
                            int block_size, int64_t num_blocks, unsigned int* err,
-                           cudaStream_t stream, const PrefillExtra* extra = nullptr);
+                           cudaStream_t stream);
 
 }  // namespace pkv

@@ -44,19 +44,14 @@
 //   The epilogue divides O by l and stages the bf16 rows in the (now dead)
 //   Q tile; a full tile leaves by two TMA boxes, a ragged one with coalesced
 //   16-byte writes of its valid rows.
-// Also served by the same kernel:
-//   - packed K/V (no block table; flash-attn's varlen call without a prefix
-//     cache): request r's keys are rows cu_k[r] .. of [rows, Hkv, d] arrays,
-//     one 128-row box per K/V tile;
-//   - prefill_tc_kernel<true>, the shared-prefix pass of grouped decode: the
-//     key count and block-table row of each request come from per-request
-//     arrays, the keys may be cut into chunks (each a separate work item with
-//     its own output block), and each row's log2-sum-exp m + log2(l) is
-//     written for the merge with the rest of the keys.
-// The plain prefill starts as a programmatic dependent of the kernel before
-// it and waits for it; after that it lets its own dependents start (it
-// writes nothing they read).  The shared-prefix instantiation lets them start
-// at once.
+// Also served by the same kernel: packed K/V (no block table; flash-attn's
+// varlen call without a prefix cache): request r's keys are rows cu_k[r] ..
+// of [rows, Hkv, d] arrays, one 128-row box per K/V tile.  (The shared-prefix
+// pass of grouped decode, a non-causal attention of many short query sets,
+// has a kernel of its own: prefix.cu.)
+// The prefill starts as a programmatic dependent of the kernel before it and
+// waits for it; after that it lets its own dependents start (it writes
+// nothing they read).
 // Every mbarrier wait is time-limited; a timeout sets PKV_FLAG_TIMEOUT and the
 // CTA drains its copies, waits for its issued MMAs and frees TMEM before
 // returning.
@@ -111,19 +106,6 @@ struct Shape {
 
 struct PrefillArgs {
     uint16_t* out;
-    // optional (else null): keys of request r = req_klen[r] instead of the
-    // cu_k difference, block-table row of request r = req_table_row[r]
-    // instead of r, and the row's log2-sum-exp m + log2(l) in
-    // lse[(row) * hq + head]
-    const int32_t* req_klen;
-    const int32_t* req_table_row;
-    float* lse;
-    // key chunks (non-causal only): grid.z enumerates (request, chunk); chunk
-    // c of a request covers keys [c*per, (c+1)*per), per = its keys / kchunks
-    // rounded up to whole tiles, and writes output rows shifted by
-    // c * chunk_rows (out and lse hold kchunks stacked outputs)
-    int32_t kchunks;
-    int32_t chunk_rows;
     const int32_t* cu_q;
     const int32_t* cu_k;
     const int32_t* table;
@@ -142,10 +124,7 @@ struct PrefillArgs {
     int32_t pair_tiles;  // 1: a CTA takes query tiles qt and qt - 1 of one head
 };
 
-// kExt: the per-request key counts / table rows, key chunks and log2-sum-exp
-// output of PrefillArgs are in use (a separate instantiation, so the plain
-// prefill compiles without them)
-template <bool kExt, int HD>
+template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_o,
@@ -169,22 +148,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     uint64_t* mma_done = q_ready + 1;    // every MMA of the CTA complete
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
-    // The plain prefill is launched as a programmatic dependent of the kernel
-    // before it (typically the write of the new rows), so it waits for that
-    // kernel before reading anything.  Only then may a kernel launched after
-    // this one start; one that does not wait (the shared-prefix pass) thus
-    // still runs after the write.  The shared-prefix instantiation is
-    // launched after its inputs are complete and needs no wait.
-    if constexpr (!kExt) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Launched as a programmatic dependent of the kernel before it (typically
+    // the write of the new rows), the prefill waits for that kernel before
+    // reading anything.  Only then may a kernel launched after this one
+    // start; one that does not wait (the shared-prefix pass of the mixed
+    // step) thus still runs after the write.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = kExt ? (int)blockIdx.z / a.kchunks : (int)blockIdx.z;
-    const int kchunk = kExt ? (int)blockIdx.z % a.kchunks : 0;
+    const int r = (int)blockIdx.z;
     const int h_a = a.pair_heads ? 2 * (int)blockIdx.y : (int)blockIdx.y;
     const int32_t cq0 = a.cu_q[r], cq1 = a.cu_q[r + 1];
     const int32_t ck0 = a.cu_k[r], ck1 = a.cu_k[r + 1];
-    int32_t q_len = cq1 - cq0, k_len = (kExt && a.req_klen) ? a.req_klen[r] : ck1 - ck0;
-    const int64_t trow = (kExt && a.req_table_row) ? a.req_table_row[r] : r;
+    int32_t q_len = cq1 - cq0, k_len = ck1 - ck0;
+    const int64_t trow = r;
     // keys a request may have: its block-table row, or (packed K/V) the rows
     // from its first key to the end of the arrays
     const int32_t cap = a.table ? a.max_blocks * a.block_size : max(0, a.oob_row - ck0);
@@ -194,12 +171,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
             flag_error(a.err, PKV_FLAG_BAD_LENGTH);
         if (q_len < 0) q_len = 0;
         k_len = k_len < 0 ? 0 : (k_len > cap ? cap : k_len);
-    }
-    int32_t kbase = 0;  // first key of this chunk
-    if (kExt && a.kchunks > 1) {
-        const int32_t per = ((k_len + a.kchunks - 1) / a.kchunks + BN - 1) / BN * BN;
-        kbase = kchunk * per;
-        k_len = max(0, min(per, k_len - kbase));
     }
     // The CTA's two Q tiles, A (x = 0) and B (x = 1), share every K/V tile:
     //   - pair_heads: one 128-row query tile for query heads h_a and h_a + 1
@@ -234,7 +205,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         tshift[x] = BM - trows[x];
         tbox[x] = cq0 + tq0[x] + trows[x] - BM;  // negative rows arrive zero-filled
         thead[x] = a.pair_tiles ? h_a : h_a + x;
-        tout[x] = (int64_t)cq0 + tq0[x] + (kExt ? (int64_t)kchunk * a.chunk_rows : 0);
+        tout[x] = (int64_t)cq0 + tq0[x];
     }
     const int32_t diag = k_len - q_len;  // query i sees key j <= i + diag
     int32_t last_key = k_len - 1;
@@ -244,9 +215,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     if (n_tiles == 0) {  // no query row of these tiles sees a key: output 0
         const int nh = has_b ? 2 : 1;
         for (int x = 0; x < nh; ++x) {
-            if (kExt && a.lse)
-                for (int i = threadIdx.x; i < pick(trows, x); i += blockDim.x)
-                    a.lse[(pick(tout, x) + i) * a.hq + pick(thead, x)] = -INFINITY;
             for (int i = threadIdx.x; i < pick(trows, x) * (HD / 8); i += blockDim.x) {
                 const int rr = i / (HD / 8), c = i % (HD / 8);
                 const int64_t row = pick(tout, x) + rr;
@@ -309,22 +277,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
             const int32_t* trow_ptr = a.table ? a.table + trow * a.max_blocks : nullptr;
             const int32_t lane_key = piece_of_lane < pieces ? piece_of_lane * a.piece
                                                             : INT32_MAX - BN * n_tiles;
-            const int32_t kadd = kExt ? kbase : 0;
             // the table entry behind this lane's piece of tile j (0 if none is read)
             auto entry = [&](int j) -> int32_t {
                 const int32_t key = j * BN + lane_key;
                 if (key >= k_len || !trow_ptr) return 0;
-                return trow_ptr[(key + kadd) / a.block_size];
+                return trow_ptr[key / a.block_size];
             };
             auto row_of = [&](int j, int32_t phys) -> int32_t {
                 const int32_t key = j * BN + lane_key;
                 if (key >= k_len) return a.oob_row;  // zero-filled by TMA (and idle lanes)
-                if (!trow_ptr) return ck0 + key + kadd;  // packed K/V
+                if (!trow_ptr) return ck0 + key;  // packed K/V
                 if (phys < 0 || phys >= a.num_blocks) {
                     flag_error(a.err, PKV_FLAG_BAD_BLOCK);
                     return a.oob_row;
                 }
-                return phys * a.block_size + (key + kadd) % a.block_size;
+                return phys * a.block_size + key % a.block_size;
             };
             if (pw == 0 && lane == 0) {
                 const int nq = has_b ? 2 : 1;
@@ -386,7 +353,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
             int issued = 0, issued_v = 0;
             auto page_row = [&](int32_t key) -> int32_t {
                 if (key >= k_len) return a.oob_row;  // zero-filled by TMA
-                if constexpr (kExt) key += kbase;
                 if (!a.table) return ck0 + key;       // packed K/V
                 const int32_t phys = a.table[trow * a.max_blocks + key / a.block_size];
                 if (phys < 0 || phys >= a.num_blocks) {
@@ -646,9 +612,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         // last reader, QK of the final K tile, completed before o_ready),
         // then stored with coalesced 16-byte writes, 16 threads per row.
         unsigned char* stage = sm + OFF_Q + x * kTileBytes;
-        if (kExt && ok && a.lse && t >= shift)
-            a.lse[(out_row0 + t - shift) * a.hq + h] =
-                l > 0.f ? m_ref * sl + __log2f(l) : -INFINITY;
         if (ok) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -714,7 +677,7 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
                            const int32_t* block_table, int32_t max_blocks, int causal,
                            float scale, void* out, void* workspace, int hq, int hkv, int d,
                            int block_size, int64_t num_blocks, unsigned int* err,
-                           cudaStream_t stream, const PrefillExtra* ex) {
+                           cudaStream_t stream) {
     (void)max_seqlen_k;
     (void)workspace;
     if (d != 128 && d != 64) return cudaErrorNotSupported;
@@ -733,22 +696,13 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
     // last row of its own request, so this bound never clips a valid row
     const int64_t q_rows = std::min<int64_t>((int64_t)batch * max_seqlen_q, 0x7fffffffLL);
     CUtensorMap mq, mo, mk, mv;
-    const int kchunks = (ex && ex->kchunks > 1 && !causal) ? ex->kchunks : 1;
-    if ((int64_t)batch * kchunks > 65535) return cudaErrorNotSupported;
-    // output rows: kchunks stacked outputs of chunk_rows rows each
-    const int64_t o_rows =
-        kchunks > 1 ? std::min<int64_t>((int64_t)kchunks * ex->chunk_rows, 0x7fffffffLL) : q_rows;
+    const int64_t o_rows = q_rows;
     if (!make_rows_map(&mq, q, hq, q_rows, BM, d) || !make_rows_map(&mo, out, hq, o_rows, BM, d) ||
         !make_rows_map(&mk, k_cache, hkv, rows, piece, d) ||
         !make_rows_map(&mv, v_cache, hkv, rows, piece, d))
         return cudaErrorInvalidValue;
     PrefillArgs a;
     a.out = static_cast<uint16_t*>(out);
-    a.req_klen = ex ? ex->req_klen : nullptr;
-    a.req_table_row = ex ? ex->req_table_row : nullptr;
-    a.lse = ex ? ex->lse : nullptr;
-    a.kchunks = (ex && ex->kchunks > 1 && !causal) ? ex->kchunks : 1;
-    a.chunk_rows = ex ? ex->chunk_rows : 0;
     a.cu_q = cu_q;
     a.cu_k = cu_k;
     a.table = block_table;
@@ -761,37 +715,21 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const void* q, const void* k_c
     a.pair_heads = (a.group % 2 == 0) ? 1 : 0;
     // one query head per KV head: the CTA's second Q tile is the query tile
     // before the first (same head, same keys) instead of a second head
-    a.pair_tiles = (!ex && !a.pair_heads) ? 1 : 0;
+    a.pair_tiles = a.pair_heads ? 0 : 1;
     a.block_size = block_size;
     a.piece = piece;
     a.oob_row = (int32_t)rows;
     a.tiles_q = (max_seqlen_q + BM - 1) / BM;
     a.causal = causal ? 1 : 0;
-    auto kern = ex ? (d == 128 ? prefill_tc_kernel<true, 128> : prefill_tc_kernel<true, 64>)
-                   : (d == 128 ? prefill_tc_kernel<false, 128> : prefill_tc_kernel<false, 64>);
+    auto kern = d == 128 ? prefill_tc_kernel<128> : prefill_tc_kernel<64>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.pair_tiles ? (a.tiles_q + 1) / 2 : a.tiles_q, a.pair_heads ? (hq + 1) / 2 : hq,
-              batch * a.kchunks);
-    if (!ex || ex->pdl) {
-        // start as a programmatic dependent of the previous kernel: the plain
-        // prefill waits for it in the kernel; the shared-prefix pass of the
-        // mixed step needs none of its results
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = grid;
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kern, mq, mo, mk, mv, a);
-    }
-    kern<<<grid, kThreads, smem, stream>>>(mq, mo, mk, mv, a);
-    return cudaGetLastError();
+              batch);
+    // a programmatic dependent of the previous kernel: the prefill waits for
+    // it in the kernel
+    return launch_dependent(kern, grid, dim3(kThreads), smem, stream, mq, mo, mk, mv, a);
 }
 
 }  // namespace pkv
