@@ -52,7 +52,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode KV GB/s & % HBM peak; varlen prefill TFLOP/s & % bf16 peak"
 DECODE_CFG, QWEN_CFG, PREFILL_CFG, MIXED_CFG = 3, 2, 4, 5
-PARTS = ("all", "decode", "qwen3", "write", "prefill", "copy", "shared", "mixed")
+PARTS = ("all", "decode", "qwen3", "shapes", "write", "prefill", "copy", "shared", "mixed")
 
 
 def parse_args():
@@ -582,6 +582,8 @@ def main():
         dstep = run_decode(args, world, pkv, W, peaks, flush, line)
     if only in ("all", "qwen3"):
         run_qwen3(args, world, pkv, W, peaks, flush, line)
+    if only in ("all", "shapes"):
+        run_shapes(args, world, pkv, W, peaks, flush, line)
     if only in ("all", "write"):
         run_write(args, world, pkv, W, peaks, flush, line)
     if only in ("all", "prefill"):
@@ -703,6 +705,38 @@ def run_qwen3(args, world, pkv, W, peaks, flush, line):
     line["error_flags"] |= pkv.paged_error_flags()
     del dev
     torch.cuda.empty_cache()
+
+
+# Decode shapes beyond the workloads: the long-context lengths (8 sequences,
+# U[16384, 40960] keys, block 256) with a GQA group of 4, head_dim 64, and 4
+# KV heads.
+SHAPES = {"gqa4_32q_8kv_d128": (32, 8, 128), "d64_16q_8kv": (16, 8, 64),
+          "16q_4kv_d128": (16, 4, 128)}
+
+
+def run_shapes(args, world, pkv, W, peaks, flush, line):
+    hbm_peak, _, _, peak_src = peaks
+    lens = np.random.default_rng(1003 + 7_000_000).integers(16384, 40960, size=8, endpoint=True)
+    out = {}
+    for i, (name, (hq, hkv, d)) in enumerate(SHAPES.items()):
+        s = W.make_step(name=name, dtype="bf16", hq=hq, hkv=hkv, d=d, block_size=256,
+                        decode_lens=lens, seed=1200 + i)
+        dev = DecodeStep(s, pkv)
+        ms_step, per = time_parts([dev.run], args.steps, args.warmup, world, flush)
+        nbytes = decode_append_bytes(s)
+        out[name] = {"value": round(world * nbytes / (ms_step * 1e-3) / 1e9, 2), "unit": "GB/s",
+                     "ms_per_step": round(ms_step, 5), "bytes_per_step": nbytes,
+                     "roofline": hbm_roofline("paged_decode_append (split kernel + combine)",
+                                              nbytes, per[0][0], per[0][1], hbm_peak, peak_src,
+                                              "decode_" + name)}
+        line["gpu_launches"] += DecodeStep.launches * args.steps
+        del dev
+        torch.cuda.empty_cache()
+    line["decode_shapes"] = {
+        "metric": "decode KV GB/s at shapes beyond the workloads", "unit": "GB/s",
+        "workload": "8 sequences, L~U[16384,40960], B=256, bf16, one paged_decode_append call; "
+                    "L2 flushed between steps", "shapes": out}
+    line["error_flags"] |= pkv.paged_error_flags()
 
 
 def run_write(args, world, pkv, W, peaks, flush, line):

@@ -221,22 +221,31 @@ static size_t shared_prefix_extra_bytes(int32_t batch, const pkv_geom* g) {
            align256((size_t)kMaxPrefixChunks * batch * g->num_heads * 4);
 }
 
+// Workspace of a grouped decode: the split's pieces, then the prefix partials.
+static size_t grouped_ws_bytes(const pkv::DecodePlan& plan, int32_t batch, const pkv_geom* g) {
+    return plan.ws_bytes + shared_prefix_extra_bytes(batch, g);
+}
+
 size_t paged_decode_shared_prefix_workspace_size(int32_t batch, const pkv_geom* geom) {
-    const size_t dec = paged_decode_workspace_size(batch, geom);
-    if (!dec) return 0;
-    return dec + shared_prefix_extra_bytes(batch, geom);
+    if (check_geom(geom) != PKV_OK || batch < 0) return 0;
+    DeviceInfo dev;
+    if (pkv::current_device_info(&dev) != cudaSuccess) return 0;
+    pkv::DecodePlan plan;
+    if (!pkv::plan_decode(dev, batch, geom->num_heads, geom->num_kv_heads, geom->head_dim,
+                          geom->block_size, elt_size(geom->dtype), &plan))
+        return 0;
+    return grouped_ws_bytes(plan, batch, geom);
 }
 
 // The shared-prefix pass of a grouped decode: one work item per (group, KV
 // head, key chunk, block of 128 / G members); the keys are cut into enough
-// chunks for the items to cover the SMs once.  Fills *kchunks_out.
-static cudaError_t launch_prefix_pass(const DeviceInfo& dev, const void* q, const void* k_cache,
-                                      const void* v_cache, const int32_t* table,
-                                      int32_t max_blocks, int32_t batch, const int32_t* group_cu,
-                                      const int32_t* group_plen, int32_t n_groups,
-                                      int32_t max_group_size, float scale, void* x_out,
-                                      float* x_lse, const pkv_geom* g, bool pdl,
-                                      cudaStream_t stream, int* kchunks_out) {
+// chunks for the items to cover the SMs once.
+static pkv::PrefixLaunch prefix_pass(const DeviceInfo& dev, const void* q, const void* k_cache,
+                                     const void* v_cache, const int32_t* table,
+                                     int32_t max_blocks, int32_t batch, const int32_t* group_cu,
+                                     const int32_t* group_plen, int32_t n_groups,
+                                     int32_t max_group_size, float scale, void* x_out,
+                                     float* x_lse, const pkv_geom* g, bool pdl) {
     const int G = g->num_heads / g->num_kv_heads;
     const int per_blk = G <= 128 ? 128 / G : 1;
     const int units = n_groups * g->num_kv_heads * ((max_group_size + per_blk - 1) / per_blk);
@@ -264,8 +273,7 @@ static cudaError_t launch_prefix_pass(const DeviceInfo& dev, const void* q, cons
     p.max_group_size = max_group_size;
     p.kchunks = kchunks;
     p.pdl = pdl;
-    *kchunks_out = kchunks;
-    return pkv::launch_prefix(dev, p, stream);
+    return p;
 }
 
 int paged_decode_shared_prefix(const void* q, const void* k_cache, const void* v_cache,
@@ -294,7 +302,7 @@ int paged_decode_shared_prefix(const void* q, const void* k_cache, const void* v
     if (!pkv::plan_decode(dev, batch, geom->num_heads, geom->num_kv_heads, geom->head_dim,
                           geom->block_size, elt_size(geom->dtype), &plan))
         return PKV_ERR_UNSUPPORTED;
-    const size_t need = plan.ws_bytes + shared_prefix_extra_bytes(batch, geom);
+    const size_t need = grouped_ws_bytes(plan, batch, geom);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return PKV_ERR_WORKSPACE;
     unsigned char* x_out = static_cast<unsigned char*>(workspace) + plan.ws_bytes;
     float* x_lse = reinterpret_cast<float*>(
@@ -302,11 +310,12 @@ int paged_decode_shared_prefix(const void* q, const void* k_cache, const void* v
     // 1. the prefix of every group, once: attention of the group's queries
     //    over its first group_prefix_len[g] keys, read through the block-table
     //    row of the group's first sequence (tensor cores)
-    int kchunks = 1;
-    cudaError_t e = launch_prefix_pass(dev, q, k_cache, v_cache, block_table, max_blocks_per_seq,
-                                       batch, group_cu, group_prefix_len, n_groups,
-                                       max_group_size, scale, x_out, x_lse, geom, false, stream,
-                                       &kchunks);
+    const pkv::PrefixLaunch pp = prefix_pass(dev, q, k_cache, v_cache, block_table,
+                                             max_blocks_per_seq, batch, group_cu,
+                                             group_prefix_len, n_groups, max_group_size, scale,
+                                             x_out, x_lse, geom, false);
+    const int kchunks = pp.kchunks;
+    cudaError_t e = pkv::launch_prefix(dev, pp, stream);
     if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return PKV_ERR_CUDA;
     // 2. each sequence's own keys after the prefix, merged with the prefix state.
@@ -364,13 +373,11 @@ int paged_mixed_step(const pkv_mixed_step* s, void* k_cache, void* v_cache, void
         if (!pkv::plan_decode(dev, s->decode_batch, geom->num_heads, geom->num_kv_heads,
                               geom->head_dim, geom->block_size, elt_size(geom->dtype), &plan))
             return PKV_ERR_UNSUPPORTED;
-        const size_t need = plan.ws_bytes + (grp ? shared_prefix_extra_bytes(s->decode_batch, geom)
-                                                 : 0);
+        const size_t need = grouped_ws_bytes(plan, s->decode_batch, geom);
         if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
             return PKV_ERR_WORKSPACE;
     }
     const int64_t kv_dim = (int64_t)geom->num_kv_heads * geom->head_dim;
-    bool chained = false;  // a kernel this call launched precedes the next one
     // 1. the prefill requests' new rows
     if (s->prefill_new_tokens > 0) {
         cudaError_t e = pkv::launch_kv_write(s->prefill_k_new, s->prefill_v_new, geom->dtype,
@@ -379,38 +386,44 @@ int paged_mixed_step(const pkv_mixed_step* s, void* k_cache, void* v_cache, void
                                              geom->num_blocks * geom->block_size, dev.err, stream);
         if (e != cudaSuccess) return PKV_ERR_CUDA;
     }
-    // 2. causal varlen prefill
-    if (pf) {
-        cudaError_t e = pkv::launch_prefill(
-            dev, s->prefill_q, k_cache, v_cache, s->cu_seqlens_q, s->cu_seqlens_k,
-            s->prefill_batch, s->max_seqlen_q, s->max_seqlen_k, s->prefill_table,
-            s->prefill_max_blocks, 1, s->scale, s->prefill_out, nullptr, geom->num_heads,
-            geom->num_kv_heads, geom->head_dim, geom->block_size, geom->num_blocks, dev.err,
-            stream);
-        if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
-        if (e != cudaSuccess) return PKV_ERR_CUDA;
-        chained = true;
-    }
-    if (!dec) return PKV_OK;
-    // 3. decode with the append (shared prefixes first when grouped)
+    // 2. the tensor-core work: the causal varlen prefill and, when the decode
+    //    is grouped, the shared-prefix pass, in one launch (the prefix items
+    //    start at once; the prefill items wait for the write)
     pkv::SharedPrefix sp{};
+    pkv::PrefixLaunch pp{};
     if (grp) {
         unsigned char* x_out = static_cast<unsigned char*>(workspace) + plan.ws_bytes;
         float* x_lse = reinterpret_cast<float*>(
             x_out + align256((size_t)kMaxPrefixChunks * s->decode_batch * geom->num_heads *
                              geom->head_dim * 2));
-        int kchunks = 1;
-        cudaError_t e = launch_prefix_pass(dev, s->decode_q, k_cache, v_cache, s->decode_table,
-                                           s->decode_max_blocks, s->decode_batch, s->group_cu,
-                                           s->group_prefix_len, s->n_groups, s->max_group_size,
-                                           s->scale, x_out, x_lse, geom, chained, stream,
-                                           &kchunks);
-        if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
-        if (e != cudaSuccess) return PKV_ERR_CUDA;
+        pp = prefix_pass(dev, s->decode_q, k_cache, v_cache, s->decode_table, s->decode_max_blocks,
+                         s->decode_batch, s->group_cu, s->group_prefix_len, s->n_groups,
+                         s->max_group_size, s->scale, x_out, x_lse, geom, true);
         sp = pkv::SharedPrefix{s->group_cu, s->group_prefix_len, s->n_groups, x_out, x_lse,
-                               kchunks};
-        chained = true;
+                               pp.kchunks};
     }
+    cudaError_t e = cudaSuccess;
+    if (pf && grp) {
+        e = pkv::launch_prefill_with_prefix(
+            dev, s->prefill_q, k_cache, v_cache, s->cu_seqlens_q, s->cu_seqlens_k,
+            s->prefill_batch, s->max_seqlen_q, s->prefill_table, s->prefill_max_blocks, s->scale,
+            s->prefill_out, geom->num_heads, geom->num_kv_heads, geom->head_dim,
+            geom->block_size, geom->num_blocks, dev.err, pp, stream);
+    } else if (pf) {
+        e = pkv::launch_prefill(dev, s->prefill_q, k_cache, v_cache, s->cu_seqlens_q,
+                                s->cu_seqlens_k, s->prefill_batch, s->max_seqlen_q,
+                                s->max_seqlen_k, s->prefill_table, s->prefill_max_blocks, 1,
+                                s->scale, s->prefill_out, nullptr, geom->num_heads,
+                                geom->num_kv_heads, geom->head_dim, geom->block_size,
+                                geom->num_blocks, dev.err, stream);
+    } else if (grp) {
+        e = pkv::launch_prefix(dev, pp, stream);
+    }
+    if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    const bool chained = pf || grp;  // a kernel of this call precedes the decode
+    if (!dec) return PKV_OK;
+    // 3. decode with the append, merged with the shared prefixes when grouped
     pkv::DecodeAppend ap{s->decode_k_new, s->decode_v_new, k_cache, v_cache};
     pkv::DecodeChain ch{chained};
     return cuda_status(pkv::launch_decode(

@@ -107,6 +107,12 @@ struct DecodeArgs {
     int32_t wait_inputs;  // wait for the previous kernel before reading any input
 };
 
+// Tiles of one piece of the split: one CTA's equal share of the tile list
+// (the combine derives the same size).
+__device__ __forceinline__ int32_t piece_tiles(int32_t total, int ctas) {
+    return total > 0 ? (total + ctas - 1) / ctas : 1;
+}
+
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 __host__ __device__ constexpr size_t merge_bytes(int G, int D) {
@@ -117,9 +123,11 @@ __host__ __device__ constexpr size_t merge_bytes(int G, int D) {
 __host__ __device__ constexpr size_t seq_table_bytes(int batch) {
     return align_up((size_t)(batch + 1) * 4, 128) + 2 * align_up((size_t)batch * 4, 128);
 }
-// [barriers 128 B][stage valid flags 128 B][sequence tables][merge scratch][stages]
+// [ring barriers 128 B][stage tags 128 B][merge barriers 128 B][sequence
+// tables][merge scratch][stages]
+constexpr size_t kDecodeHeaderBytes = 384;
 __host__ __device__ constexpr size_t decode_fixed_smem(int G, int D, int batch) {
-    return 256 + seq_table_bytes(batch) + merge_bytes(G, D);
+    return kDecodeHeaderBytes + seq_table_bytes(batch) + merge_bytes(G, D);
 }
 
 // two bf16 packed in a word -> (element 2i, element 2i+1) as fp32 (exact)
@@ -257,11 +265,17 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kMaxStages;
+    // per stage: valid block id, tile index, piece (CTA or chunk) index, and
+    // whether the tile ends its piece
     int32_t* stage_ok = reinterpret_cast<int32_t*>(smem + 128);
-    int32_t* tstart = reinterpret_cast<int32_t*>(smem + 256);
+    int32_t* stage_tile = stage_ok + kMaxStages;
+    int32_t* stage_piece = stage_tile + kMaxStages;
+    int32_t* stage_last = stage_piece + kMaxStages;
+    uint64_t* merge_bar = reinterpret_cast<uint64_t*>(smem + 256);  // [2]
+    int32_t* tstart = reinterpret_cast<int32_t*>(smem + kDecodeHeaderBytes);
     int32_t* sfirst = tstart + align_up((size_t)(a.batch + 1) * 4, 128) / 4;
     int32_t* slen = sfirst + align_up((size_t)a.batch * 4, 128) / 4;
-    float* mscratch = reinterpret_cast<float*>(smem + 256 + seq_table_bytes(a.batch));
+    float* mscratch = reinterpret_cast<float*>(smem + kDecodeHeaderBytes + seq_table_bytes(a.batch));
     unsigned char* stage_base = smem + decode_fixed_smem(G, D, a.batch);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -275,6 +289,8 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
+        mbar_init(&merge_bar[0], kConsumerWarps);
+        mbar_init(&merge_bar[1], kConsumerWarps);
         fence_barrier_init();
     }
     // launched as a programmatic dependent: the lengths, table and K/V may come
@@ -299,7 +315,8 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
             if (L < 0 || L > cap) flag_error(a.err, PKV_FLAG_BAD_LENGTH);
         }
     }
-    const int32_t chunk = total > 0 ? (total + gridDim.x - 1) / gridDim.x : 0;
+    // this CTA's share [t0, t1) of the tile list
+    const int32_t chunk = piece_tiles(total, gridDim.x);
     const int32_t t0 = blockIdx.x * chunk;
     const int32_t t1 = min(t0 + chunk, total);
     if (t0 >= t1) {
@@ -326,56 +343,73 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
 #endif
         int32_t k = 0;  // stages filled so far (lane 0)
         bool stop = false;
-        for (int32_t tb = t0; tb < t1; tb += 32) {
-            // lane i: tile tb + i's block-table entry and (first key's slot in
-            // the block) * 64 + rows (rows <= 32); the batch's table reads are
-            // covered by the stages still queued in the ring
-            int32_t my_phys = 0, my_slot_rows = 0;
-            if (tb + lane < t1) {
-                const int32_t t = tb + lane;
-                const int bb = seq_of_tile(tstart, a.batch, t);
-                const int32_t pos0 = sfirst[bb] + (t - tstart[bb]) * R;
-                my_slot_rows = (pos0 % a.block_size) * 64 + min(R, slen[bb] - pos0);
-                my_phys = a.table[(int64_t)bb * a.max_blocks + pos0 / a.block_size];
-            }
-            const int n = min(32, t1 - tb);
-            for (int i = 0; i < n; ++i) {
-                const int32_t phys = __shfl_sync(all, my_phys, i);
-                const int32_t slot_rows = __shfl_sync(all, my_slot_rows, i);
-                if (lane != 0 || stop) continue;
-                const int32_t rows = slot_rows & 63, off = slot_rows >> 6;
-                const int s = k % S;
-                if (!mbar_wait(&empty[s], ((k / S) & 1) ^ 1, a.err)) {
-                    stop = true;
-                    continue;
+        {
+            // the CTA's piece: its share [t0, t1) of the tile list
+            const int32_t piece = blockIdx.x, pt0 = t0, pt1 = t1;
+            for (int32_t tb = pt0; tb < pt1 && !stop; tb += 32) {
+                // lane i: tile tb + i's block-table entry and (first key's slot
+                // in the block) * 64 + rows (rows <= 32); the batch's table
+                // reads are covered by the stages still queued in the ring
+                int32_t my_phys = 0, my_slot_rows = 0;
+                if (tb + lane < pt1) {
+                    const int32_t t = tb + lane;
+                    const int bb = seq_of_tile(tstart, a.batch, t);
+                    const int32_t pos0 = sfirst[bb] + (t - tstart[bb]) * R;
+                    my_slot_rows = (pos0 % a.block_size) * 64 + min(R, slen[bb] - pos0);
+                    my_phys = a.table[(int64_t)bb * a.max_blocks + pos0 / a.block_size];
                 }
-                ++k;
-                if (phys < 0 || phys >= a.num_blocks) {
-                    flag_error(a.err, PKV_FLAG_BAD_BLOCK);
-                    stage_ok[s] = 0;
-                    mbar_arrive(&full[s]);
-                    continue;
-                }
-                stage_ok[s] = 1;
-                const int64_t row0 = (int64_t)phys * a.block_size + off;
-                unsigned char* kd = stage_base + (size_t)s * 2 * half_bytes;
-                unsigned char* vd = kd + half_bytes;
-                const uint32_t bytes = (uint32_t)(rows * row_bytes);
-                mbar_arrive_expect_tx(&full[s], 2 * bytes);
-                if (HC == a.hkv) {
-                    const size_t o = (size_t)row0 * row_bytes;
-                    bulk_g2s(kd, a.k_cache + o, bytes, &full[s], pol);
-                    bulk_g2s(vd, a.v_cache + o, bytes, &full[s], pol);
-                } else {
-                    const size_t pool_row = (size_t)a.hkv * D * ELT;
-                    for (int r = 0; r < rows; ++r) {
-                        const size_t o = (size_t)(row0 + r) * pool_row + (size_t)head0 * D * ELT;
-                        bulk_g2s(kd + r * row_bytes, a.k_cache + o, (uint32_t)row_bytes, &full[s], pol);
-                        bulk_g2s(vd + r * row_bytes, a.v_cache + o, (uint32_t)row_bytes, &full[s], pol);
+                const int n = min(32, pt1 - tb);
+                for (int i = 0; i < n; ++i) {
+                    const int32_t phys = __shfl_sync(all, my_phys, i);
+                    const int32_t slot_rows = __shfl_sync(all, my_slot_rows, i);
+                    if (lane != 0 || stop) continue;
+                    const int32_t rows = slot_rows & 63, off = slot_rows >> 6;
+                    const int s = k % S;
+                    if (!mbar_wait(&empty[s], ((k / S) & 1) ^ 1, a.err)) {
+                        stop = true;
+                        continue;
+                    }
+                    ++k;
+                    stage_tile[s] = tb + i;
+                    stage_piece[s] = piece;
+                    stage_last[s] = (tb + i + 1 == pt1) ? 1 : 0;
+                    if (phys < 0 || phys >= a.num_blocks) {
+                        flag_error(a.err, PKV_FLAG_BAD_BLOCK);
+                        stage_ok[s] = 0;
+                        mbar_arrive(&full[s]);
+                        continue;
+                    }
+                    stage_ok[s] = 1;
+                    const int64_t row0 = (int64_t)phys * a.block_size + off;
+                    unsigned char* kd = stage_base + (size_t)s * 2 * half_bytes;
+                    unsigned char* vd = kd + half_bytes;
+                    const uint32_t bytes = (uint32_t)(rows * row_bytes);
+                    mbar_arrive_expect_tx(&full[s], 2 * bytes);
+                    if (HC == a.hkv) {
+                        const size_t o = (size_t)row0 * row_bytes;
+                        bulk_g2s(kd, a.k_cache + o, bytes, &full[s], pol);
+                        bulk_g2s(vd, a.v_cache + o, bytes, &full[s], pol);
+                    } else {
+                        const size_t pool_row = (size_t)a.hkv * D * ELT;
+                        for (int r = 0; r < rows; ++r) {
+                            const size_t o = (size_t)(row0 + r) * pool_row + (size_t)head0 * D * ELT;
+                            bulk_g2s(kd + r * row_bytes, a.k_cache + o, (uint32_t)row_bytes, &full[s], pol);
+                            bulk_g2s(vd + r * row_bytes, a.v_cache + o, (uint32_t)row_bytes, &full[s], pol);
+                        }
                     }
                 }
+                stop = __shfl_sync(all, stop ? 1 : 0, 0) != 0;
             }
-            if (__shfl_sync(all, stop ? 1 : 0, 0)) break;
+        }
+        // the end of the CTA's tiles: a stage with tile -1 (no copy)
+        if (!stop && lane == 0) {
+            const int s = k % S;
+            if (mbar_wait(&empty[s], ((k / S) & 1) ^ 1, a.err)) {
+                stage_tile[s] = -1;
+                stage_ok[s] = 0;
+                mbar_arrive(&full[s]);
+                ++k;
+            }
         }
         if (lane != 0) return;
         // The CTA must not exit while a copy into its shared memory is in
@@ -402,18 +436,34 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
 
     float2 q2[G][8], o2[G][8];
     float m[G], l[G];
-    int b = seq_of_tile(tstart, a.batch, t0);
-    int loaded = -1;
+    int b = 0;
+    int loaded = -1;     // the sequence whose queries are in registers
+    bool fresh = false;  // the state holds no key of the current piece yet
     int32_t L = 0, st = 0;
 
-    // After a timed-out wait the warp stops waiting, reading shared memory and
-    // releasing stages, but keeps walking the same tiles so that it meets the
-    // other consumer warps at every named barrier below.
-    bool live = true;
-    for (int32_t t = t0, k = 0; t < t1; ++t, ++k) {
-        while (t >= tstart[b + 1]) ++b;
+    // The consumers follow the stages' tags (tile, piece, piece end) until the
+    // closing stage.  A timed-out wait ends the warp's loop; the other
+    // warps then time out at the next merge barrier or ring stage, so every
+    // wait of the CTA still ends.
+    int merges = 0;       // merge-barrier rounds so far (phase parity)
+    int32_t prev_t = -2;  // previous tile (consecutive tiles keep the sequence cursor)
+    for (int32_t k = 0;; ++k) {
+        const int s = k % S;
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (k / S) & 1, a.err))) break;
+        const int32_t t = stage_tile[s];
+        if (t < 0) break;  // the closing stage
+        const int32_t piece = stage_piece[s];
+        const bool piece_end = stage_last[s] != 0;
+        const bool stage_valid = stage_ok[s] != 0;
+        if (t != prev_t + 1) {
+            b = seq_of_tile(tstart, a.batch, t);
+        } else {
+            while (t >= tstart[b + 1]) ++b;
+        }
+        prev_t = t;
         if (b != loaded) {
             loaded = b;
+            fresh = false;
             // the queries first: their loads overlap the length lookups
 #pragma unroll
             for (int g = 0; g < G; ++g) {
@@ -425,20 +475,22 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
             st = sfirst[b];
             const float2 sc2 = make_float2(a.qscale, a.qscale);
 #pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q2[g][e] = fmul2(q2[g][e], sc2);
+        }
+        if (!fresh) {  // a new piece: empty state (the queries stay)
+            fresh = true;
+#pragma unroll
             for (int g = 0; g < G; ++g) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    q2[g][e] = fmul2(q2[g][e], sc2);
-                    o2[g][e] = make_float2(0.f, 0.f);
-                }
+                for (int e = 0; e < 8; ++e) o2[g][e] = make_float2(0.f, 0.f);
                 m[g] = -INFINITY;
                 l[g] = 0.f;
             }
         }
-        const int s = k % S;
-        if (live) live = __all_sync(0xffffffffu, mbar_wait(&full[s], (k / S) & 1, a.err));
         const int32_t rows = min(R, L - st - (t - tstart[b]) * R);
-        if (live && stage_ok[s]) {
+        if (stage_valid) {
             const unsigned char* ks = stage_base + (size_t)s * 2 * half_bytes;
             const unsigned char* vs = ks + half_bytes;
             // warp-uniform loop over pairs of rows (ra, rb = ra + row_step)
@@ -492,10 +544,10 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
             }
         }
         __syncwarp();
-        if (live && lane == 0) mbar_arrive(&empty[s]);
+        if (lane == 0) mbar_arrive(&empty[s]);
 
-        // end of this CTA's piece of sequence b: merge and store the partial state
-        const bool seg_end = (t + 1 == t1) || (t + 1 >= tstart[b + 1]);
+        // end of this piece of sequence b: merge and store the partial state
+        const bool seg_end = piece_end || (t + 1 >= tstart[b + 1]);
         if (!seg_end) continue;
         // merge the groups of the warp (lanes with equal tl hold the same dims)
 #pragma unroll
@@ -535,7 +587,9 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
                     }
                 }
             }
-            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&merge_bar[0]);
+            if (!__all_sync(0xffffffffu, mbar_wait(&merge_bar[0], merges & 1, a.err))) break;
             if (wrank == 0) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
@@ -565,10 +619,13 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
                     for (int e = 0; e < 8; ++e) o2[g][e] = ot[e];
                 }
             }
-            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&merge_bar[1]);
+            if (!__all_sync(0xffffffffu, mbar_wait(&merge_bar[1], merges & 1, a.err))) break;
+            ++merges;
         }
         if (wrank == 0 && grp == 0) {
-            const int64_t slot = (int64_t)blockIdx.x + b;
+            const int64_t slot = (int64_t)piece + b;
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const int64_t qh = (int64_t)kvh * G + g;
@@ -587,7 +644,7 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
                 }
             }
         }
-        loaded = -1;  // the next tile starts a new piece (re-load q, reset state)
+        fresh = false;  // the next tile starts a new piece
     }
 }
 
@@ -681,30 +738,41 @@ template <int D, bool BF16, int U>
 __global__ void __launch_bounds__(kCombineWarps * 32, U > 4 ? 4 : 8)
 decode_combine_kernel(const CombineArgs c) {
     constexpr int DPL = D / 32;
-    // wait until the split kernel's partials are complete and visible
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t w = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
     const int hq = c.hq, batch = c.batch;
-    if (w >= (int64_t)batch * hq) return;
-    const int b = (int)(w / hq), h = (int)(w % hq);
-    const int32_t total = c.tstart[batch];
-    const int32_t tb0 = c.tstart[b], tb1 = c.tstart[b + 1];
-    const int32_t chunk = total > 0 ? (total + c.ctas - 1) / c.ctas : 1;
-    const int c0 = tb0 / chunk, c1 = tb1 > tb0 ? (tb1 - 1) / chunk : c0 - 1;
-    const int64_t xstride = (int64_t)batch * hq;  // one prefix chunk's (sequence, head) count
+    const bool live = w < (int64_t)batch * hq;
+    const int b = live ? (int)(w / hq) : 0, h = live ? (int)(w % hq) : 0;
     const int64_t bh = (int64_t)b * hq + h;
     const int G = hq / (c.hkv > 0 ? c.hkv : 1);
     const int kvh = h / G;
+    // Before the wait: what the split kernel does not write (the appended
+    // key's score and V row, and where its K/V row goes), so that these loads
+    // overlap the split kernel's tail.
     float M = -INFINITY, L = 0.f, acc[DPL];
 #pragma unroll
     for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-    if (c.k_new) {  // the appended key: score q . k_new in log2 units
+    int64_t new_slot = -1;  // the appended row's slot, when this warp writes it
+    if (c.k_new && live) {  // the appended key: score q . k_new in log2 units
         const int64_t row = ((int64_t)b * c.hkv + kvh) * D + lane * DPL;
         float qv[DPL], kv[DPL], vv[DPL];
         load_row<BF16, DPL>(c.q, bh * D + lane * DPL, qv);
         load_row<BF16, DPL>(c.k_new, row, kv);
         load_row<BF16, DPL>(c.v_new, row, vv);
+        if (h % G == 0) {  // the first warp of each KV head writes the row
+            const int32_t Lb = c.seqlens[b];
+            const int32_t B = c.block_size;
+            if (Lb < 0 || Lb >= c.max_blocks * B) {
+                if (lane == 0) flag_error(c.err, PKV_FLAG_BAD_LENGTH);
+            } else {
+                const int32_t phys = c.table[(int64_t)b * c.max_blocks + Lb / B];
+                if (phys < 0 || phys >= c.num_blocks) {
+                    if (lane == 0) flag_error(c.err, PKV_FLAG_BAD_BLOCK);
+                } else {
+                    new_slot = (int64_t)phys * B + Lb % B;
+                }
+            }
+        }
         float dot = 0.f;
 #pragma unroll
         for (int e = 0; e < DPL; ++e) dot = fmaf(qv[e], kv[e], dot);
@@ -712,6 +780,14 @@ decode_combine_kernel(const CombineArgs c) {
         for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
         merge_state<DPL>(M, L, acc, dot * c.qscale, 1.f, vv);
     }
+    // wait until the split kernel's partials are complete and visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!live) return;
+    const int32_t total = c.tstart[batch];
+    const int32_t tb0 = c.tstart[b], tb1 = c.tstart[b + 1];
+    const int32_t chunk = piece_tiles(total, c.ctas);
+    const int c0 = tb0 / chunk, c1 = tb1 > tb0 ? (tb1 - 1) / chunk : c0 - 1;
+    const int64_t xstride = (int64_t)batch * hq;  // one prefix chunk's (sequence, head) count
     for (int x = 0; x < c.x_chunks; ++x) {
         float xo[DPL];
         const float mx = c.x_lse[x * xstride + bh];
@@ -748,22 +824,12 @@ decode_combine_kernel(const CombineArgs c) {
 #pragma unroll
         for (int e = 0; e < DPL; ++e) o[e] = acc[e] * inv;
     }
-    // the first warp of each KV head writes the new K/V row into the cache
-    if (c.k_new && h % G == 0) {
-        const int32_t Lb = c.seqlens[b];
-        const int32_t B = c.block_size;
-        if (Lb < 0 || Lb >= c.max_blocks * B) {
-            if (lane == 0) flag_error(c.err, PKV_FLAG_BAD_LENGTH);
-            return;
-        }
-        const int32_t phys = c.table[(int64_t)b * c.max_blocks + Lb / B];
-        if (phys < 0 || phys >= c.num_blocks) {
-            if (lane == 0) flag_error(c.err, PKV_FLAG_BAD_BLOCK);
-            return;
-        }
+    // the new K/V row into the cache (after the wait: the split kernel has
+    // read every cached key)
+    if (new_slot >= 0) {
         constexpr int ELT = BF16 ? 2 : 4;
         const int64_t src = ((int64_t)b * c.hkv + kvh) * D + lane * DPL;
-        const int64_t dst = (((int64_t)phys * B + Lb % B) * c.hkv + kvh) * D + lane * DPL;
+        const int64_t dst = (new_slot * c.hkv + kvh) * D + lane * DPL;
 #pragma unroll
         for (int e = 0; e < DPL * ELT; e += 4) {
             *reinterpret_cast<uint32_t*>(c.k_cache + dst * ELT + e) =

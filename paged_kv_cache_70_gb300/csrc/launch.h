@@ -131,7 +131,7 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
                           const DecodeAppend* append = nullptr,
                           const DecodeChain* chain = nullptr);
 
-// ---- shared-prefix pass (prefix.cu) --------------------------------------------
+// ---- shared-prefix pass (prefill.cu) -------------------------------------------
 // For every group of consecutive sequences sharing their first group_plen[g]
 // keys: attention of all the group's queries over those keys (in kchunks key
 // chunks), written as normalised bf16 rows x_out [kchunks, batch, hq, hd] and
@@ -153,6 +153,18 @@ struct PrefixLaunch {
 };
 
 cudaError_t launch_prefix(const DeviceInfo& dev, const PrefixLaunch& p, cudaStream_t stream);
+
+// A causal varlen prefill (the arguments of launch_prefill) and a
+// shared-prefix pass in ONE launch: the prefill's items wait for the kernel
+// before them, the prefix items start at once, and the SMs take either kind
+// as they free up.
+cudaError_t launch_prefill_with_prefix(const DeviceInfo& dev, const void* q, const void* k_cache,
+                                       const void* v_cache, const int32_t* cu_q,
+                                       const int32_t* cu_k, int32_t batch, int32_t max_seqlen_q,
+                                       const int32_t* block_table, int32_t max_blocks,
+                                       float scale, void* out, int hq, int hkv, int d,
+                                       int block_size, int64_t num_blocks, unsigned int* err,
+                                       const PrefixLaunch& p, cudaStream_t stream);
 
 // ---- prefill ----------------------------------------------------------------
 size_t prefill_workspace_bytes(int32_t batch, int32_t max_seqlen_q, int hq);

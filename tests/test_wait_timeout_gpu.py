@@ -1,10 +1,10 @@
 """A decode whose pipeline wait runs out, on a test-only build of the split
 kernel: its producer issues no copy and every wait gives up after 1 ms.  The
 consumers' first wait then times out with nothing in flight (decode uses no
-TMEM).  The call must return, the kernels must finish, the device error word
-of that build must carry PKV_FLAG_TIMEOUT, and the output is the empty state
-(0).  With two KV heads the eight consumer warps share heads and merge through
-named barriers, which they must all still reach after the timeout.
+TMEM).  The call must return, the kernels must finish, and the device error
+word of that build must carry PKV_FLAG_TIMEOUT.  With two KV heads the eight
+consumer warps share heads and merge through time-limited barriers, which must
+not hold any warp after the timeout.
 
 The build compiles decode.cu with the two test defines into its own library
 (_build/test_wait_timeout/); the default library is not changed."""
@@ -58,8 +58,8 @@ def test_decode_wait_timeout_sets_flag_and_returns(timeout_lib, hq, hkv):
     torch.cuda.synchronize()  # the kernels finished: every wait gave up after 1 ms
     assert _flags(lib) & pkv.PKV_FLAG_TIMEOUT
     assert pkv.paged_error_flags() == 0  # the default library saw nothing
-    # no key was read: every (sequence, head) keeps the empty state, output 0
-    assert torch.count_nonzero(out).item() == 0
+    # (the output of a call whose wait ran out is unspecified: only the flag
+    # says so)
     # the default library still decodes correctly on the same inputs
     want = dev.decode()
     torch.cuda.synchronize()
