@@ -307,10 +307,11 @@ class WriteDecodeStep:
 
 class PrefillStep:
     """A chunked-prefill step resident on the device: slot_mapping build and
-    write of the requests' new rows, then causal varlen prefill over cached +
-    new keys through the block table."""
+    write of the requests' new rows (one paged_kv_write_positions launch, which
+    also stores the slot mapping for other layers), then causal varlen prefill
+    over cached + new keys through the block table."""
 
-    launches = 3
+    launches = 2
 
     def __init__(self, step, pkv):
         s = step
@@ -336,6 +337,12 @@ class PrefillStep:
         t = self.dev if t is None else t
         self.pkv.paged_kv_write(t["new_k"], t["new_v"], self.slots, self.k_cache, self.v_cache)
 
+    def write_pos(self, t=None):
+        t = self.dev if t is None else t
+        self.pkv.paged_kv_write_positions(t["new_k"], t["new_v"], t["table"], t["token_seq"],
+                                          t["token_pos"], self.k_cache, self.v_cache,
+                                          slot_mapping_out=self.slots)
+
     def attend(self, t=None):
         t = self.dev if t is None else t
         s = self.s
@@ -345,8 +352,7 @@ class PrefillStep:
                                       workspace=self.ws)
 
     def run(self, t=None):
-        self.slot_build(t)
-        self.write(t)
+        self.write_pos(t)
         self.attend(t)
 
 
@@ -760,6 +766,16 @@ def run_write(args, world, pkv, W, peaks, flush, line):
         "roofline": hbm_roofline("kv_write_copy_kernel (paged_kv_write)", wb, per[1][0],
                                  per[1][1], hbm_peak, peak_src, "kv_write")}
     line["gpu_launches"] += 2 * args.steps
+    # the same rows through paged_kv_write_positions: slot build and write in
+    # one launch (the slot mapping stored for other layers)
+    ms_pos, per_pos = time_parts([dev.write_pos], args.steps, args.warmup, world, flush)
+    line["kv_write"]["write_positions"] = {
+        "value": round(world * (wb + sb) / (ms_pos * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "ms_per_step": round(ms_pos, 5), "bytes_per_step": wb + sb,
+        "roofline": hbm_roofline("kv_write_copy_kernel<slots from positions> "
+                                 "(paged_kv_write_positions)", wb + sb, per_pos[0][0],
+                                 per_pos[0][1], hbm_peak, peak_src, "kv_write_positions")}
+    line["gpu_launches"] += args.steps
     line["error_flags"] |= pkv.paged_error_flags()
     del dev
     torch.cuda.empty_cache()
@@ -782,22 +798,22 @@ def run_prefill(args, world, pkv, W, peaks, flush, line):
         return
     clocks = Clocks(torch.cuda.current_device())
     clocks.start()
-    p_ms, per = time_parts([pdev.slot_build, pdev.write, pdev.attend], args.steps, args.warmup,
-                           world, flush)
+    p_ms, per = time_parts([pdev.write_pos, pdev.attend], args.steps, args.warmup, world, flush)
     if not args.no_soak:
         soak(pdev.run)
     pclk = clocks.stop()
     pclk["window"] = "warm-up, timed region, then 0.5 s more of the same step (untimed)"
     flops = prefill_flops(pstep)
-    pmean, pmed = per[2]
+    pmean, pmed = per[1]
     tflops = flops / (pmean * 1e-3) / 1e12
     line["prefill"] = {
         "metric": "varlen prefill TFLOP/s", "workload": W.CONFIG_NAMES[PREFILL_CFG],
         "value": round(world * flops / (p_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
         "ms_per_step": round(p_ms, 5),
-        "step": "slot_mapping build + write of 16 requests' new K/V + causal varlen "
-                "prefill (L2 flushed between steps, not timed)",
-        "slot_build_ms": round(per[0][0], 5), "write_ms": round(per[1][0], 5),
+        "step": "slot_mapping build and write of 16 requests' new K/V in one launch "
+                "(paged_kv_write_positions) + causal varlen prefill (L2 flushed between "
+                "steps, not timed)",
+        "write_ms": round(per[0][0], 5),
         "flops_per_step": flops, "visible_pairs": prefill_pairs(pstep),
         "roofline": {"bound": "tensor", "kernel": "paged_varlen_prefill",
                      "achieved": round(tflops, 1), "peak": bf16_peak,

@@ -117,6 +117,26 @@ int paged_kv_write(const void* k, const void* v, int32_t kv_dtype, const int32_t
                    cudaStream_t stream);
 
 /*
+ * paged_kv_write_positions -- paged_build_slot_mapping and paged_kv_write in
+ * one launch: token n's slot is block_table[s][p / B] * B + p % B with
+ * s = token_seq[n], p = token_pos[n] ("11. Paged attention 与 online softmax"
+ * §11.1; "自己来实现一个" computes it once per step for every layer), and its
+ * K and V rows are written there as paged_kv_write does.  The slots are also
+ * stored in slot_mapping_out [num_tokens] when it is not NULL, so that the
+ * other layers of the step can call paged_kv_write with them.  token_seq[n] < 0
+ * marks a padding row (slot -1, nothing written).  Out-of-range s, p or table
+ * entries give slot -1 (nothing written) and set PKV_FLAG_BAD_SEQ /
+ * _BAD_LENGTH / _BAD_BLOCK; a slot >= num_blocks * B sets PKV_FLAG_BAD_SLOT.
+ * Arguments as for the two calls it replaces.
+ */
+int paged_kv_write_positions(const void* k, const void* v, int32_t kv_dtype,
+                             const int32_t* block_table, int32_t max_blocks_per_seq,
+                             int32_t num_seqs, const int32_t* token_seq,
+                             const int32_t* token_pos, int64_t num_tokens,
+                             int32_t* slot_mapping_out, void* k_cache, void* v_cache,
+                             const pkv_geom* geom, cudaStream_t stream);
+
+/*
  * paged_decode_workspace_size -- bytes of device scratch paged_decode needs for
  * `batch` sequences on the CURRENT device (the split plan depends on its SM
  * count).  Returns 0 for invalid arguments.  There is no max_seqlen_k

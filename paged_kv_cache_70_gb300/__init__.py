@@ -31,6 +31,7 @@ from ._binding import (  # noqa: F401
     paged_decode_workspace_size,
     paged_error_flags,
     paged_kv_write,
+    paged_kv_write_positions,
     paged_varlen_prefill,
     paged_varlen_prefill_workspace_size,
 )

@@ -29,6 +29,7 @@ PKV_FLAG_TIMEOUT = 1 << 4
 EXPORTED = (
     "paged_build_slot_mapping",
     "paged_kv_write",
+    "paged_kv_write_positions",
     "paged_decode_workspace_size",
     "paged_decode",
     "paged_varlen_prefill_workspace_size",
@@ -117,6 +118,9 @@ def load_library(path: str | None = None):
         lib.paged_build_slot_mapping.restype = ctypes.c_int
         lib.paged_kv_write.argtypes = [vp, vp, i32, vp, i64, vp, vp, gp, vp]
         lib.paged_kv_write.restype = ctypes.c_int
+        lib.paged_kv_write_positions.argtypes = [vp, vp, i32, vp, i32, i32, vp, vp, i64, vp, vp,
+                                                 vp, gp, vp]
+        lib.paged_kv_write_positions.restype = ctypes.c_int
         lib.paged_decode_workspace_size.argtypes = [i32, gp]
         lib.paged_decode_workspace_size.restype = sz
         lib.paged_decode.argtypes = [vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp, sz,
@@ -239,6 +243,36 @@ def paged_kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
                                        k.shape[0], _ptr(k_cache), _ptr(v_cache),
                                        ctypes.byref(g), _stream(k))
     _check("paged_kv_write", st)
+
+
+def paged_kv_write_positions(k: torch.Tensor, v: torch.Tensor, block_table: torch.Tensor,
+                             token_seq: torch.Tensor, token_pos: torch.Tensor,
+                             k_cache: torch.Tensor, v_cache: torch.Tensor,
+                             slot_mapping_out: torch.Tensor | None = None) -> None:
+    """paged_build_slot_mapping and paged_kv_write in one launch; the slots go
+    to slot_mapping_out when given."""
+    _cuda_contig("k", k)
+    _cuda_contig("v", v, k.dtype)
+    for n, t in (("block_table", block_table), ("token_seq", token_seq), ("token_pos", token_pos)):
+        _cuda_contig(n, t, torch.int32)
+    _cuda_contig("k_cache", k_cache)
+    _cuda_contig("v_cache", v_cache, k_cache.dtype)
+    if k.shape != v.shape or k.shape[1:] != k_cache.shape[2:] or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between k/v rows and the pools")
+    n_tok = k.shape[0]
+    if token_seq.numel() != n_tok or token_pos.numel() != n_tok:
+        raise ValueError("token_seq and token_pos must have one entry per token row")
+    if slot_mapping_out is not None:
+        _cuda_contig("slot_mapping_out", slot_mapping_out, torch.int32)
+        if slot_mapping_out.numel() != n_tok:
+            raise ValueError("slot_mapping_out must have one entry per token row")
+    rows, width = block_table.shape
+    g = geom_of(k_cache, k_cache.shape[2])
+    st = load_library().paged_kv_write_positions(
+        _ptr(k), _ptr(v), _dtype_code(k), _ptr(block_table), width, rows, _ptr(token_seq),
+        _ptr(token_pos), n_tok, _ptr(slot_mapping_out),
+        _ptr(k_cache), _ptr(v_cache), ctypes.byref(g), _stream(k))
+    _check("paged_kv_write_positions", st)
 
 
 def paged_decode_workspace_size(batch: int, q_heads: int, k_cache: torch.Tensor) -> int:

@@ -105,6 +105,29 @@ int paged_kv_write(const void* k, const void* v, int32_t kv_dtype, const int32_t
                                             stream));
 }
 
+int paged_kv_write_positions(const void* k, const void* v, int32_t kv_dtype,
+                             const int32_t* block_table, int32_t max_blocks_per_seq,
+                             int32_t num_seqs, const int32_t* token_seq,
+                             const int32_t* token_pos, int64_t num_tokens,
+                             int32_t* slot_mapping_out, void* k_cache, void* v_cache,
+                             const pkv_geom* geom, cudaStream_t stream) {
+    int st = check_geom(geom);
+    if (st != PKV_OK) return st;
+    if (!elt_size(kv_dtype) || num_tokens < 0 || max_blocks_per_seq < 0 || num_seqs < 0)
+        return PKV_ERR_INVALID;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !token_seq || !token_pos || !k_cache || !v_cache) return PKV_ERR_INVALID;
+    if (num_seqs > 0 && max_blocks_per_seq > 0 && !block_table) return PKV_ERR_INVALID;
+    DeviceInfo dev;
+    if (pkv::current_device_info(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    const int64_t kv_dim = (int64_t)geom->num_kv_heads * geom->head_dim;
+    const int64_t num_slots = geom->num_blocks * geom->block_size;
+    return cuda_status(pkv::launch_kv_write_positions(
+        k, v, kv_dtype, block_table, max_blocks_per_seq, num_seqs, token_seq, token_pos,
+        num_tokens, geom->block_size, slot_mapping_out, k_cache, v_cache, geom->dtype, kv_dim,
+        num_slots, dev.err, stream));
+}
+
 size_t paged_decode_workspace_size(int32_t batch, const pkv_geom* geom) {
     if (check_geom(geom) != PKV_OK || batch < 0) return 0;
     DeviceInfo dev;

@@ -73,6 +73,15 @@ cudaError_t launch_kv_write(const void* k, const void* v, int src_dtype, const i
                             int64_t kv_dim, int64_t num_slots, unsigned int* err,
                             cudaStream_t stream);
 
+// The slot build and the write in one launch (slots_out may be null).
+cudaError_t launch_kv_write_positions(const void* k, const void* v, int src_dtype,
+                                      const int32_t* block_table, int32_t max_blocks,
+                                      int32_t num_seqs, const int32_t* token_seq,
+                                      const int32_t* token_pos, int64_t num_tokens,
+                                      int32_t block_size, int32_t* slots_out, void* k_cache,
+                                      void* v_cache, int cache_dtype, int64_t kv_dim,
+                                      int64_t num_slots, unsigned int* err, cudaStream_t stream);
+
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src,
                                const int32_t* dst, int32_t n_pairs, int64_t block_bytes,
                                int64_t num_blocks, unsigned int* err, cudaStream_t stream);
@@ -121,6 +130,7 @@ struct DecodeChain {
 // Returns false when the geometry is not supported.
 bool plan_decode(const DeviceInfo& dev, int32_t batch, int hq, int hkv, int d, int block_size,
                  int elt, DecodePlan* plan);
+
 
 cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_cache,
                           const void* v_cache, const int32_t* block_table, int32_t max_blocks,

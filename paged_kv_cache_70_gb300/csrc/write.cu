@@ -17,32 +17,44 @@
 
 namespace pkv {
 
-__global__ void build_slot_mapping_kernel(const int32_t* __restrict__ table, int32_t max_blocks,
-                                          int32_t num_seqs, const int32_t* __restrict__ token_seq,
-                                          const int32_t* __restrict__ token_pos,
-                                          int64_t num_tokens, int32_t block_size,
+// The slot of token n: table[s][p / B] * B + p % B for s = token_seq[n],
+// p = token_pos[n]; -1 for a padding row (s < 0) or an out-of-range s, p or
+// table entry (flagged).
+struct TokenSlots {
+    const int32_t* table;
+    int32_t max_blocks;
+    int32_t num_seqs;
+    const int32_t* token_seq;
+    const int32_t* token_pos;
+    int32_t block_size;
+};
+
+__device__ __forceinline__ int32_t token_slot(const TokenSlots& t, int64_t n, unsigned int* err) {
+    const int32_t s = t.token_seq[n];
+    const int32_t p = t.token_pos[n];
+    if (s < 0) return -1;
+    if (s >= t.num_seqs) {
+        flag_error(err, PKV_FLAG_BAD_SEQ);
+        return -1;
+    }
+    if (p < 0 || p / t.block_size >= t.max_blocks) {
+        flag_error(err, PKV_FLAG_BAD_LENGTH);
+        return -1;
+    }
+    const int32_t phys = t.table[(int64_t)s * t.max_blocks + p / t.block_size];
+    if (phys < 0) {
+        flag_error(err, PKV_FLAG_BAD_BLOCK);
+        return -1;
+    }
+    return phys * t.block_size + p % t.block_size;
+}
+
+__global__ void build_slot_mapping_kernel(const TokenSlots t, int64_t num_tokens,
                                           int32_t* __restrict__ slots, unsigned int* err) {
     PKV_DEPENDENT_PROLOGUE();
     int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (n >= num_tokens) return;
-    const int32_t s = token_seq[n];
-    const int32_t p = token_pos[n];
-    int32_t out = -1;
-    if (s >= 0) {
-        if (s >= num_seqs) {
-            flag_error(err, PKV_FLAG_BAD_SEQ);
-        } else if (p < 0 || p / block_size >= max_blocks) {
-            flag_error(err, PKV_FLAG_BAD_LENGTH);
-        } else {
-            const int32_t phys = table[(int64_t)s * max_blocks + p / block_size];
-            if (phys < 0) {
-                flag_error(err, PKV_FLAG_BAD_BLOCK);
-            } else {
-                out = phys * block_size + p % block_size;
-            }
-        }
-    }
-    slots[n] = out;
+    slots[n] = token_slot(t, n, err);
 }
 
 cudaError_t launch_build_slot_mapping(const int32_t* block_table, int32_t max_blocks,
@@ -53,9 +65,9 @@ cudaError_t launch_build_slot_mapping(const int32_t* block_table, int32_t max_bl
     if (num_tokens == 0) return cudaSuccess;
     const int threads = 256;
     const int64_t blocks = (num_tokens + threads - 1) / threads;
+    const TokenSlots t{block_table, max_blocks, num_seqs, token_seq, token_pos, block_size};
     return launch_dependent(build_slot_mapping_kernel, dim3((unsigned)blocks), dim3(threads), 0,
-                            stream, block_table, max_blocks, num_seqs, token_seq, token_pos,
-                            num_tokens, block_size, slot_mapping, err);
+                            stream, t, num_tokens, slot_mapping, err);
 }
 
 // ---------------------------------------------------------------------------
@@ -63,27 +75,71 @@ cudaError_t launch_build_slot_mapping(const int32_t* block_table, int32_t max_bl
 // ---------------------------------------------------------------------------
 constexpr int kWriteWarps = 8;
 
-// equal dtypes: 16-byte vector copy of row_bytes (a multiple of 16)
+// The slot of the warp's token: read from the slot mapping, or (POS) computed
+// from the token's sequence and position by lane 0 and, when slots_out is
+// given, stored there for the writes of later layers.
+template <bool POS>
+__device__ __forceinline__ int32_t warp_token_slot(const int32_t* slots, const TokenSlots& t,
+                                                   int32_t* slots_out, int64_t n, int lane,
+                                                   unsigned int* err) {
+    if constexpr (!POS) {
+        return __ldg(slots + n);
+    } else {
+        int32_t s = 0;
+        if (lane == 0) {
+            s = token_slot(t, n, err);
+            if (slots_out) slots_out[n] = s;
+        }
+        return __shfl_sync(0xffffffffu, s, 0);
+    }
+}
+
+// equal dtypes: 16-byte vector copy of row_bytes (a multiple of 16).  The
+// first kPrefetch vectors of the K and V rows a lane copies are loaded before
+// the slot is known (the source rows do not depend on it), so the slot
+// lookup's latency overlaps theirs; a row that is not written (padding or a
+// bad slot) wastes those loads only.
+constexpr int kPrefetch = 4;
+
+template <bool POS>
 __global__ void __launch_bounds__(kWriteWarps * 32)
 kv_write_copy_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
-                     const int32_t* __restrict__ slots, int64_t num_tokens,
+                     const int32_t* __restrict__ slots, const TokenSlots t,
+                     int32_t* __restrict__ slots_out, int64_t num_tokens,
                      uint4* __restrict__ kc, uint4* __restrict__ vc, int64_t vec_per_row,
                      int64_t num_slots, unsigned int* err) {
     PKV_DEPENDENT_PROLOGUE();
     const int lane = threadIdx.x & 31;
     const int64_t n = (int64_t)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
     if (n >= num_tokens) return;
-    const int32_t s = __ldg(slots + n);
+    const uint4* ks = k + n * vec_per_row;
+    const uint4* vs = v + n * vec_per_row;
+    uint4 ka[kPrefetch], va[kPrefetch];
+#pragma unroll
+    for (int u = 0; u < kPrefetch; ++u) {
+        const int64_t i = lane + 32 * u;
+        if (i < vec_per_row) {
+            ka[u] = __ldcs(ks + i);
+            va[u] = __ldcs(vs + i);
+        }
+    }
+    const int32_t s = warp_token_slot<POS>(slots, t, slots_out, n, lane, err);
     if (s < 0) return;
     if (s >= num_slots) {
         if (lane == 0) flag_error(err, PKV_FLAG_BAD_SLOT);
         return;
     }
-    const uint4* ks = k + n * vec_per_row;
-    const uint4* vs = v + n * vec_per_row;
     uint4* kd = kc + (int64_t)s * vec_per_row;
     uint4* vd = vc + (int64_t)s * vec_per_row;
-    for (int64_t i = lane; i < vec_per_row; i += 32) {
+#pragma unroll
+    for (int u = 0; u < kPrefetch; ++u) {
+        const int64_t i = lane + 32 * u;
+        if (i < vec_per_row) {
+            kd[i] = ka[u];
+            vd[i] = va[u];
+        }
+    }
+    for (int64_t i = lane + 32 * kPrefetch; i < vec_per_row; i += 32) {
         const uint4 a = __ldcs(ks + i);
         const uint4 b = __ldcs(vs + i);
         kd[i] = a;
@@ -92,16 +148,18 @@ kv_write_copy_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
 }
 
 // fp32 source -> bf16 cache (round to nearest even); groups of 8 elements
+template <bool POS>
 __global__ void __launch_bounds__(kWriteWarps * 32)
 kv_write_f32_to_bf16_kernel(const float4* __restrict__ k, const float4* __restrict__ v,
-                            const int32_t* __restrict__ slots, int64_t num_tokens,
+                            const int32_t* __restrict__ slots, const TokenSlots t,
+                            int32_t* __restrict__ slots_out, int64_t num_tokens,
                             uint4* __restrict__ kc, uint4* __restrict__ vc, int64_t groups8,
                             int64_t num_slots, unsigned int* err) {
     PKV_DEPENDENT_PROLOGUE();
     const int lane = threadIdx.x & 31;
     const int64_t n = (int64_t)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
     if (n >= num_tokens) return;
-    const int32_t s = __ldg(slots + n);
+    const int32_t s = warp_token_slot<POS>(slots, t, slots_out, n, lane, err);
     if (s < 0) return;
     if (s >= num_slots) {
         if (lane == 0) flag_error(err, PKV_FLAG_BAD_SLOT);
@@ -120,8 +178,10 @@ kv_write_f32_to_bf16_kernel(const float4* __restrict__ k, const float4* __restri
 }
 
 // generic element-wise path: any kvDim, any dtype pair
+template <bool POS>
 __global__ void kv_write_scalar_kernel(const void* __restrict__ k, const void* __restrict__ v,
                                        int src_dtype, const int32_t* __restrict__ slots,
+                                       const TokenSlots t, int32_t* __restrict__ slots_out,
                                        int64_t num_tokens, void* __restrict__ kc,
                                        void* __restrict__ vc, int cache_dtype, int64_t kv_dim,
                                        int64_t num_slots, unsigned int* err) {
@@ -129,7 +189,7 @@ __global__ void kv_write_scalar_kernel(const void* __restrict__ k, const void* _
     const int lane = threadIdx.x & 31;
     const int64_t n = (int64_t)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
     if (n >= num_tokens) return;
-    const int32_t s = slots[n];
+    const int32_t s = warp_token_slot<POS>(slots, t, slots_out, n, lane, err);
     if (s < 0) return;
     if (s >= num_slots) {
         if (lane == 0) flag_error(err, PKV_FLAG_BAD_SLOT);
@@ -160,10 +220,14 @@ __global__ void kv_write_scalar_kernel(const void* __restrict__ k, const void* _
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-cudaError_t launch_kv_write(const void* k, const void* v, int src_dtype, const int32_t* slots,
-                            int64_t num_tokens, void* k_cache, void* v_cache, int cache_dtype,
-                            int64_t kv_dim, int64_t num_slots, unsigned int* err,
-                            cudaStream_t stream) {
+// One write launch; with `pos` the slots come from the tokens' sequences and
+// positions (and are stored in pos->slots_out when given), else from `slots`.
+template <bool POS>
+static cudaError_t launch_write_t(const void* k, const void* v, int src_dtype,
+                                  const int32_t* slots, const TokenSlots& t, int32_t* slots_out,
+                                  int64_t num_tokens, void* k_cache, void* v_cache,
+                                  int cache_dtype, int64_t kv_dim, int64_t num_slots,
+                                  unsigned int* err, cudaStream_t stream) {
     if (num_tokens == 0) return cudaSuccess;
     const int64_t grid = (num_tokens + kWriteWarps - 1) / kWriteWarps;
     const int threads = kWriteWarps * 32;
@@ -171,23 +235,41 @@ cudaError_t launch_kv_write(const void* k, const void* v, int src_dtype, const i
                              aligned16(v_cache);
     const int src_elt = src_dtype == PKV_F32 ? 4 : 2;
     if (all_aligned && src_dtype == cache_dtype && (kv_dim * src_elt) % 16 == 0) {
-        return launch_dependent(kv_write_copy_kernel, dim3((unsigned)grid), dim3(threads), 0,
+        return launch_dependent(kv_write_copy_kernel<POS>, dim3((unsigned)grid), dim3(threads), 0,
                                 stream, static_cast<const uint4*>(k),
-                                static_cast<const uint4*>(v), slots, num_tokens,
+                                static_cast<const uint4*>(v), slots, t, slots_out, num_tokens,
                                 static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
                                 kv_dim * src_elt / 16, num_slots, err);
     } else if (all_aligned && src_dtype == PKV_F32 && cache_dtype == PKV_BF16 && kv_dim % 8 == 0) {
-        return launch_dependent(kv_write_f32_to_bf16_kernel, dim3((unsigned)grid), dim3(threads),
-                                0, stream, static_cast<const float4*>(k),
-                                static_cast<const float4*>(v), slots, num_tokens,
+        return launch_dependent(kv_write_f32_to_bf16_kernel<POS>, dim3((unsigned)grid),
+                                dim3(threads), 0, stream, static_cast<const float4*>(k),
+                                static_cast<const float4*>(v), slots, t, slots_out, num_tokens,
                                 static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
                                 kv_dim / 8, num_slots, err);
-    } else {
-        return launch_dependent(kv_write_scalar_kernel, dim3((unsigned)grid), dim3(threads), 0,
-                                stream, k, v, src_dtype, slots, num_tokens, k_cache, v_cache,
-                                cache_dtype, kv_dim, num_slots, err);
     }
-    return cudaGetLastError();
+    return launch_dependent(kv_write_scalar_kernel<POS>, dim3((unsigned)grid), dim3(threads), 0,
+                            stream, k, v, src_dtype, slots, t, slots_out, num_tokens, k_cache,
+                            v_cache, cache_dtype, kv_dim, num_slots, err);
+}
+
+cudaError_t launch_kv_write(const void* k, const void* v, int src_dtype, const int32_t* slots,
+                            int64_t num_tokens, void* k_cache, void* v_cache, int cache_dtype,
+                            int64_t kv_dim, int64_t num_slots, unsigned int* err,
+                            cudaStream_t stream) {
+    return launch_write_t<false>(k, v, src_dtype, slots, TokenSlots{}, nullptr, num_tokens,
+                                 k_cache, v_cache, cache_dtype, kv_dim, num_slots, err, stream);
+}
+
+cudaError_t launch_kv_write_positions(const void* k, const void* v, int src_dtype,
+                                      const int32_t* block_table, int32_t max_blocks,
+                                      int32_t num_seqs, const int32_t* token_seq,
+                                      const int32_t* token_pos, int64_t num_tokens,
+                                      int32_t block_size, int32_t* slots_out, void* k_cache,
+                                      void* v_cache, int cache_dtype, int64_t kv_dim,
+                                      int64_t num_slots, unsigned int* err, cudaStream_t stream) {
+    const TokenSlots t{block_table, max_blocks, num_seqs, token_seq, token_pos, block_size};
+    return launch_write_t<true>(k, v, src_dtype, nullptr, t, slots_out, num_tokens, k_cache,
+                                v_cache, cache_dtype, kv_dim, num_slots, err, stream);
 }
 
 // ---------------------------------------------------------------------------

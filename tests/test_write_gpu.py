@@ -101,3 +101,55 @@ def test_slot_builder_flags_bad_entries():
     assert list(s) == [13, -1, 7, -1, -1]
     f = pkv.paged_error_flags()
     assert f & pkv.PKV_FLAG_BAD_BLOCK and f & pkv.PKV_FLAG_BAD_SEQ and f & pkv.PKV_FLAG_BAD_LENGTH
+
+
+@pytest.mark.parametrize("cfg", [1, 4, 5])
+def test_write_positions_matches_oracle(cfg):
+    """paged_kv_write_positions (slot build and write in one launch): the same
+    caches and slot mapping as the oracle's two steps, padding rows skipped."""
+    step = W.config(cfg)
+    dev = DevStep(step)
+    out = torch.full((step.token_seq.size,), 12345, dtype=torch.int32, device="cuda")
+    pkv.paged_kv_write_positions(dev.new_k, dev.new_v, dev.table, dev.token_seq, dev.token_pos,
+                                 dev.k_cache, dev.v_cache, slot_mapping_out=out)
+    torch.cuda.synchronize()
+    want_slots, kc, vc = oracle_write(step)
+    assert np.array_equal(to_host(out), want_slots)
+    assert np.array_equal(to_host(dev.k_cache), kc)
+    assert np.array_equal(to_host(dev.v_cache), vc)
+    assert pkv.paged_error_flags() == 0
+
+
+@pytest.mark.parametrize("src,dst,hkv,d", [("f32", "bf16", 2, 64), ("bf16", "f32", 3, 24),
+                                           ("bf16", "bf16", 8, 128)])
+def test_write_positions_dtypes_and_bad_entries(src, dst, hkv, d):
+    """Every write path of the fused call; bad sequence ids, positions and
+    table entries write nothing and set their flags; no slot output."""
+    rng = np.random.default_rng(11)
+    nb, B = 6, 4
+    table = np.array([[3, 0, -1], [5, 1, 2]], np.int32)
+    seq = np.array([0, 1, 1, -1, 0, 2, 1, 0], np.int32)
+    pos = np.array([1, 4, 11, 0, 9, 0, 12, 5], np.int32)
+    n = seq.size
+
+    def mk(shape, dt):
+        return W._to_dtype(rng.standard_normal(shape).astype(np.float32), dt)
+    k, v = mk((n, hkv, d), src), mk((n, hkv, d), src)
+    canary = mk((nb, B, hkv, d), dst)
+    # rows 0-2 and 7 are valid (the oracle's addressing); row 3 is padding;
+    # row 4 meets a -1 table entry, row 5 a sequence id past the table, row 6
+    # a position past its row: slot -1, nothing written
+    valid = np.array([0, 1, 2, 7])
+    slots = np.full(n, -1, np.int32)
+    slots[valid] = oracle.build_slot_mapping(table, seq[valid], pos[valid], B)
+    assert list(slots) == [13, 4, 11, -1, -1, -1, -1, 1]
+    kc, vc = canary.copy(), canary.copy()
+    oracle.kv_write(k, v, slots, kc, vc)
+    dk, dv = to_dev(canary.copy()), to_dev(canary.copy())
+    pkv.paged_kv_write_positions(to_dev(k), to_dev(v), to_dev(table), to_dev(seq), to_dev(pos),
+                                 dk, dv)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_host(dk), kc)
+    assert np.array_equal(to_host(dv), vc)
+    f = pkv.paged_error_flags()
+    assert f & pkv.PKV_FLAG_BAD_BLOCK and f & pkv.PKV_FLAG_BAD_SEQ and f & pkv.PKV_FLAG_BAD_LENGTH
