@@ -864,7 +864,8 @@ def run_prefill_packed(args, world, pkv, pstep, pdev, flops, flush, bf16_peak, p
         "roofline": {"bound": "tensor", "kernel": "paged_varlen_prefill (packed)",
                      "achieved": round(tf, 1), "peak": bf16_peak, "unit": "TFLOP/s",
                      "frac": round(tf / bf16_peak, 4), "peak_source": peak_src + " (bf16 burst)",
-                     "traffic": None, "mean_ms": round(mean, 5), "median_ms": round(med, 5)}}
+                     "traffic": traffic_of("chunked_prefill_packed"), "mean_ms": round(mean, 5),
+                     "median_ms": round(med, 5)}}
     line["gpu_launches"] += args.steps
     line["error_flags"] |= pkv.paged_error_flags()
     del kp, vp
@@ -1003,7 +1004,7 @@ def run_mixed_step(args, world, pkv, W, peaks, flush, line):
         "unique_bytes": nbytes,
         "roofline": hbm_roofline("paged_mixed_step (every kernel of the call)", nbytes, mean,
                                  med, hbm_peak, peak_src, "mixed_step")}
-    line["gpu_launches"] += 5 * args.steps
+    line["gpu_launches"] += 4 * args.steps  # write, tensor-core launch, split, combine
     line["error_flags"] |= pkv.paged_error_flags()
     del kc, vc, ws
     torch.cuda.empty_cache()
