@@ -11,11 +11,12 @@
 // GB300 design (HBM-bound: ~1 FMA per K/V byte for GQA group 2):
 //  * Work split.  The keys of every sequence are cut into tiles of R keys
 //    (R divides B, so a tile never crosses a page) and the concatenated tile
-//    list of all sequences is cut into equal contiguous shares, one per CTA
-//    (one CTA per SM).  A CTA therefore covers a piece of one long sequence or
-//    several short ones; each piece yields a partial (m, l, o) state that a
-//    second kernel merges with the same rule.  Load balance is within one tile
-//    whatever the length mix.
+//    list of all sequences is cut into contiguous shares, one per CTA (one
+//    CTA per SM), equal once each sequence start is counted as one tile.  A
+//    CTA therefore covers a piece of one long sequence or several short ones;
+//    each piece yields a partial (m, l, o) state that a second kernel merges
+//    with the same rule.  Load balance is within about one tile whatever the
+//    length mix.
 //  * Data movement.  A producer warp streams each tile of K and V (all KV heads
 //    of the CTA; a tile is contiguous in the pool when the CTA owns every KV
 //    head) into a ring of shared-memory stages with cp.async.bulk, tracked by
@@ -29,7 +30,8 @@
 //    dimensions of q (pre-scaled by scale*log2 e) and of o as fp32 pairs; a
 //    group handles two key rows at a time with packed fp32x2 FMAs (four
 //    independent chains), dot products are reduced with xor shuffles, and each
-//    key updates the state (running max; o rescaled only when the max grows).
+//    pair of keys updates the state as one block (running max of the state and
+//    both scores; o rescaled only when the max grows).
 //    Exponentials are base 2 on log2-scaled scores, which is the same merge.
 //  * The combine kernel (one warp per sequence and head) is launched as a
 //    programmatic dependent of the split kernel, so its launch overlaps the
@@ -107,10 +109,28 @@ struct DecodeArgs {
     int32_t wait_inputs;  // wait for the previous kernel before reading any input
 };
 
-// Tiles of one piece of the split: one CTA's equal share of the tile list
-// (the combine derives the same size).
-__device__ __forceinline__ int32_t piece_tiles(int32_t total, int ctas) {
-    return total > 0 ? (total + ctas - 1) / ctas : 1;
+// The split's shares.  Tile t of sequence b sits at position
+//   u(t) = t + kSeqCost * (b + 1)
+// of a cost line (starting a sequence costs a CTA about kSeqCost tiles: its
+// queries, its partial state, the merge), and the line is cut into equal
+// pieces, one per CTA.  u is increasing, so a piece is a contiguous run of
+// tiles; the combine finds a sequence's pieces from the same formula.
+constexpr int32_t kSeqCost = 1;
+__device__ __forceinline__ int32_t share_cost(int32_t total, int32_t batch, int ctas) {
+    const int32_t u = total + kSeqCost * batch;
+    return u > 0 ? (u + ctas - 1) / ctas : 1;
+}
+// the first tile t with u(t) >= x (total if none)
+__device__ __forceinline__ int32_t first_tile_at(const int32_t* tstart, int batch, int64_t x) {
+    int lo = 0, hi = batch;  // first b whose last tile's position is >= x
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((int64_t)tstart[mid + 1] - 1 + (int64_t)kSeqCost * (mid + 1) >= x) hi = mid;
+        else lo = mid + 1;
+    }
+    if (lo >= batch) return tstart[batch];
+    const int64_t t = x - (int64_t)kSeqCost * (lo + 1);
+    return (int32_t)max((int64_t)tstart[lo], t);
 }
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -239,24 +259,6 @@ __device__ __forceinline__ int seq_of_tile(const int32_t* tstart, int batch, int
     return lo - 1;
 }
 
-// online-softmax update of one head's state with one key row (score s, V pairs)
-__device__ __forceinline__ void online_update(float s, const float2* v, float& m, float& l,
-                                              float2* o) {
-    if (s > m) {  // running max grows: rescale the state
-        const float c = ex2(m - s);
-        l *= c;
-        const float2 c2 = make_float2(c, c);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = fmul2(o[e], c2);
-        m = s;
-    }
-    const float p = ex2(s - m);
-    l += p;
-    const float2 p2 = make_float2(p, p);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = ffma2(p2, v[e], o[e]);
-}
-
 template <int D, bool BF16, int G>
 __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(const DecodeArgs a) {
     constexpr int ELT = BF16 ? 2 : 4;
@@ -316,9 +318,9 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
         }
     }
     // this CTA's share [t0, t1) of the tile list
-    const int32_t chunk = piece_tiles(total, gridDim.x);
-    const int32_t t0 = blockIdx.x * chunk;
-    const int32_t t1 = min(t0 + chunk, total);
+    const int32_t chunk = share_cost(total, a.batch, gridDim.x);
+    const int32_t t0 = first_tile_at(tstart, a.batch, (int64_t)blockIdx.x * chunk);
+    const int32_t t1 = first_tile_at(tstart, a.batch, (int64_t)(blockIdx.x + 1) * chunk);
     if (t0 >= t1) {
         if (holder && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
         return;
@@ -525,13 +527,39 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
                         sb[g] += __shfl_xor_sync(0xffffffffu, sb[g], off);
                     }
                 }
-                if (va) {
+                // both rows in one update (a block of two keys): one max test
+                // and one rescale per pair, the two exponentials independent
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    if (!va) sa[g] = -INFINITY;
+                    if (!vb) sb[g] = -INFINITY;
+                    const float mn = fmax3(m[g], sa[g], sb[g]);
+                    if (mn > m[g]) {  // running max grows: rescale the state
+                        const float c = ex2(m[g] - mn);
+                        l[g] *= c;
+                        const float2 c2 = make_float2(c, c);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o2[g][e] = fmul2(o2[g][e], c2);
+                        m[g] = mn;
+                    }
+                    // (a pair of rows past the tile's end on a fresh state: m = -inf)
+                    const float mr = (m[g] == -INFINITY) ? 0.f : m[g];
+                    const float pa = ex2(sa[g] - mr), pb = ex2(sb[g] - mr);
+                    l[g] += pa + pb;
+                    sa[g] = pa;
+                    sb[g] = pb;
+                }
+                {  // row a (p = 0 when past the end: row 0's values, finite, times 0)
                     const unsigned char* vr = vs + ((size_t)ia * HC + hc) * D * ELT;
                     float2 vx[8];
                     load8_smem<BF16>(vr + dim0 * ELT, &vx[0]);
                     load8_smem<BF16>(vr + dim1 * ELT, &vx[4]);
 #pragma unroll
-                    for (int g = 0; g < G; ++g) online_update(sa[g], vx, m[g], l[g], o2[g]);
+                    for (int g = 0; g < G; ++g) {
+                        const float2 p2 = make_float2(sa[g], sa[g]);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o2[g][e] = ffma2(p2, vx[e], o2[g][e]);
+                    }
                 }
                 if (vb) {
                     const unsigned char* vr = vs + ((size_t)ib * HC + hc) * D * ELT;
@@ -539,7 +567,11 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
                     load8_smem<BF16>(vr + dim0 * ELT, &vx[0]);
                     load8_smem<BF16>(vr + dim1 * ELT, &vx[4]);
 #pragma unroll
-                    for (int g = 0; g < G; ++g) online_update(sb[g], vx, m[g], l[g], o2[g]);
+                    for (int g = 0; g < G; ++g) {
+                        const float2 p2 = make_float2(sb[g], sb[g]);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o2[g][e] = ffma2(p2, vx[e], o2[g][e]);
+                    }
                 }
             }
         }
@@ -785,8 +817,9 @@ decode_combine_kernel(const CombineArgs c) {
     if (!live) return;
     const int32_t total = c.tstart[batch];
     const int32_t tb0 = c.tstart[b], tb1 = c.tstart[b + 1];
-    const int32_t chunk = piece_tiles(total, c.ctas);
-    const int c0 = tb0 / chunk, c1 = tb1 > tb0 ? (tb1 - 1) / chunk : c0 - 1;
+    const int32_t chunk = share_cost(total, batch, c.ctas);
+    const int32_t ub = kSeqCost * (b + 1);  // u(t) - t for this sequence's tiles
+    const int c0 = (tb0 + ub) / chunk, c1 = tb1 > tb0 ? (tb1 - 1 + ub) / chunk : c0 - 1;
     const int64_t xstride = (int64_t)batch * hq;  // one prefix chunk's (sequence, head) count
     for (int x = 0; x < c.x_chunks; ++x) {
         float xo[DPL];
