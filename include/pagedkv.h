@@ -154,9 +154,10 @@ size_t paged_decode_workspace_size(int32_t batch, const pkv_geom* geom);
  * K/V must already have been written with paged_kv_write.
  *   out[b,h,:] = sum_j softmax_j(scale * q[b,h,:] . k_j) v_j  over those keys,
  *   0 when cache_seqlens[b] == 0.
- * The keys of all sequences are cut into equal shares, one per CTA; each CTA
- * keeps the (m, l, o) online-softmax state of its share and a second kernel
- * merges the shares of each sequence with the same rule and normalises.
+ * The keys of all sequences are cut into shares, one per CTA (equal once each
+ * sequence start is counted as one tile of keys); each CTA keeps the (m, l, o)
+ * online-softmax state of its share and a second kernel merges the shares of
+ * each sequence with the same rule and normalises.
  * Supported: head_dim 64 or 128; fp32 or bf16; Hq/Hkv in {1, 2, 4}; Hkv in
  * {1, 2, 4, 8} or a multiple of 8; any block_size >= 1; batch <= 4096.
  * Like its workspace-size call it takes no max_seqlen_k: nothing in the launch
