@@ -26,7 +26,7 @@ sub-object of the JSON line:
 Prints one JSON line.  With torchrun (N > 1) every rank runs its own replica of
 the workload on its own GPU (no collective on the data path; "replicas only"),
 and timing is the max over ranks.  ``--impl reference`` times the CPU oracle (the
-reference arm of this build) on a bounded sample of the same workload.
+reference arm) on a bounded sample of the same workload.
 
 Between timed steps L2 is flushed (untimed): a 256 MiB buffer is written and
 then a 1 GiB buffer is read, so that the dirty lines of the write go back to

@@ -46,7 +46,7 @@ def test_decode_wait_timeout_sets_flag_and_returns(timeout_lib, hq, hkv):
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     out = torch.full_like(dev.q_decode, float("nan"))
     torch.cuda.synchronize()
-    _flags(lib)  # clear this build's error word
+    _flags(lib)  # clear the timeout library's error word
     pkv.paged_error_flags()  # and the default library's
     st = lib.paged_decode(
         ctypes.c_void_p(dev.q_decode.data_ptr()), ctypes.c_void_p(dev.k_cache.data_ptr()),
