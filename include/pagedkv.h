@@ -158,8 +158,10 @@ size_t paged_decode_workspace_size(int32_t batch, const pkv_geom* geom);
  * sequence start is counted as one tile of keys); each CTA keeps the (m, l, o)
  * online-softmax state of its share and a second kernel merges the shares of
  * each sequence with the same rule and normalises.
- * Supported: head_dim 64 or 128; fp32 or bf16; Hq/Hkv in {1, 2, 4}; Hkv in
- * {1, 2, 4, 8} or a multiple of 8; any block_size >= 1; batch <= 4096.
+ * Supported: head_dim 64 or 128; fp32 or bf16; G = Hq/Hkv in {1, 2, 4, 8, 16,
+ * 32} (from 8 up, G/4 warps per KV head, 4 query heads each, share its K/V
+ * tiles); with s = 8 / max(1, G/4) KV heads per CTA, Hkv divides s or is a
+ * multiple of s; any block_size >= 1; batch <= 4096.
  * Like its workspace-size call it takes no max_seqlen_k: nothing in the launch
  * depends on the longest sequence.
  * workspace: device scratch of at least paged_decode_workspace_size(batch, geom)
@@ -248,8 +250,9 @@ int paged_varlen_prefill(const void* q, const void* k_cache, const void* v_cache
  * prefix part is the attention of the group's queries over the prefix keys
  * (one pass over them, on the tensor cores), the rest the decode of each
  * sequence's own keys, merged with §11.2's boxed rule.
- * Supported: bf16, head_dim 64 or 128, Hq/Hkv in {1, 2, 4}, block_size a multiple of
- * 128 or a divisor of 128 (>= 8).  workspace: at least
+ * Supported: bf16, head_dim 64 or 128, Hq/Hkv and Hkv as for paged_decode,
+ * block_size a multiple of 128 or a divisor of 128 (>= 8).
+ * workspace: at least
  * paged_decode_shared_prefix_workspace_size(batch, geom) bytes, 256-byte
  * aligned.  A prefix length that is negative, longer than a member's keys or
  * not a multiple of block_size sets PKV_FLAG_BAD_LENGTH.

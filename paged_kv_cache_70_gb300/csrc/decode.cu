@@ -101,6 +101,8 @@ struct DecodeArgs {
     int32_t hq;
     int32_t hkv;
     int32_t hc;  // KV heads per CTA
+    int32_t gfull;   // query heads per KV head (Hq / Hkv)
+    int32_t gsplit;  // warps (query-head subsets of G each) per KV head and row
     int32_t block_size;
     int32_t rows;  // R
     int32_t stages;
@@ -426,13 +428,17 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
 
     // ------------------------------- consumers --------------------------------
     if constexpr (G >= 4) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs4));
-    const int hc = warp % HC;     // local KV head of this warp
-    const int wrank = warp / HC;  // rank among the warps sharing this head
-    const int WH = kConsumerWarps / HC;
+    // warp -> (local KV head, subset of G query heads, rank among the warps
+    // that share both and split the tile's rows)
+    const int GS = a.gsplit;
+    const int hc = warp % HC;
+    const int gs = (warp / HC) % GS;
+    const int wrank = warp / (HC * GS);
+    const int WH = kConsumerWarps / (HC * GS);
+    const int qh0 = (head0 + hc) * a.gfull + gs * G;  // the warp's first query head
     const int grp = lane / TG, tl = lane % TG;
     const int warp_row0 = wrank * GPW;  // first row of the warp in a tile
     const int row_step = WH * GPW;      // rows between a group's consecutive rows
-    const int kvh = head0 + hc;
     // this lane's dimensions: [tl*8, +8) and [TG*8 + tl*8, +8)
     const int dim0 = tl * 8, dim1 = TG * 8 + tl * 8;
 
@@ -469,7 +475,7 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
             // the queries first: their loads overlap the length lookups
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const int64_t qb = ((int64_t)b * a.hq + (int64_t)kvh * G + g) * D;
+                const int64_t qb = ((int64_t)b * a.hq + qh0 + g) * D;
                 load8_global<BF16>(a.q, qb + dim0, &q2[g][0]);
                 load8_global<BF16>(a.q, qb + dim1, &q2[g][4]);
             }
@@ -627,13 +633,15 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
                 for (int g = 0; g < G; ++g) {
                     float M = -INFINITY;
                     for (int w = 0; w < WH; ++w)
-                        M = fmaxf(M, mscratch[(size_t)(w * HC + hc) * G * (D + 2) + g * (D + 2) + D]);
+                        M = fmaxf(M, mscratch[(size_t)((w * GS + gs) * HC + hc) * G * (D + 2) +
+                                              g * (D + 2) + D]);
                     float lt = 0.f;
                     float2 ot[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) ot[e] = make_float2(0.f, 0.f);
                     for (int w = 0; w < WH; ++w) {
-                        const float* src = mscratch + (size_t)(w * HC + hc) * G * (D + 2) + g * (D + 2);
+                        const float* src = mscratch + (size_t)((w * GS + gs) * HC + hc) * G * (D + 2) +
+                                           g * (D + 2);
                         const float mw = src[D];
                         const float c = (mw == -INFINITY) ? 0.f : ex2(mw - M);
                         lt += src[D + 1] * c;
@@ -660,7 +668,7 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
             const int64_t slot = (int64_t)piece + b;
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const int64_t qh = (int64_t)kvh * G + g;
+                const int64_t qh = qh0 + g;
                 float* dst = a.part_o + (slot * a.hq + qh) * D;
                 *reinterpret_cast<float4*>(dst + dim0) =
                     make_float4(o2[g][0].x, o2[g][0].y, o2[g][1].x, o2[g][1].y);
@@ -889,16 +897,24 @@ bool plan_decode(const DeviceInfo& dev, int32_t batch, int hq, int hkv, int d, i
     if (d != 64 && d != 128) return false;
     if (hkv <= 0 || hq % hkv) return false;
     const int G = hq / hkv;
-    if (G != 1 && G != 2 && G != 4) return false;
+    // groups of 1, 2 and 4, and of 8, 16 and 32: G / 4 warps per KV head, each
+    // with 4 of its query heads, share the K/V tile (G / 4 divides the 8
+    // consumer warps, so every warp has a KV head and a subset)
+    int gsplit = 1;
+    if (G == 1 || G == 2 || G == 4) gsplit = 1;
+    else if (G == 8 || G == 16 || G == 32) gsplit = G / 4;
+    else return false;
+    const int G_warp = G / gsplit;  // query heads a consumer warp holds
     if (batch < 0 || batch > kDecodeMaxBatch) return false;
     if (block_size > (1 << 24)) return false;  // the producer packs slot * 64 + rows
-    int HC;
-    if (hkv <= kConsumerWarps) {
-        if (kConsumerWarps % hkv) return false;
+    int HC;  // KV heads per CTA: gsplit warps each, 8 consumer warps
+    const int head_slots = kConsumerWarps / gsplit;
+    if (hkv <= head_slots) {
+        if (head_slots % hkv) return false;
         HC = hkv;
     } else {
-        if (hkv % kConsumerWarps) return false;
-        HC = kConsumerWarps;
+        if (hkv % head_slots) return false;
+        HC = head_slots;
     }
     const size_t row_bytes = (size_t)HC * d * elt;
     // ~64 KiB of K+V per stage, at most 32 keys
@@ -907,11 +923,12 @@ bool plan_decode(const DeviceInfo& dev, int32_t batch, int hq, int hkv, int d, i
     if (cap_rows > 32) cap_rows = 32;
     const int R = largest_pow2_divisor(block_size, cap_rows);
     const size_t stage = 2 * (size_t)R * row_bytes;
-    const size_t fixed = decode_fixed_smem(G, d, batch);
+    const size_t fixed = decode_fixed_smem(G_warp, d, batch);
     if (dev.max_smem_optin < fixed + 2 * stage) return false;
     int stages = (int)((dev.max_smem_optin - fixed) / stage);
     if (stages > kMaxStages) stages = kMaxStages;
     p->heads_per_cta = HC;
+    p->gsplit = gsplit;
     p->head_groups = hkv / HC;
     p->ctas = dev.num_sms / p->head_groups > 0 ? dev.num_sms / p->head_groups : 1;
     p->rows_per_tile = R;
@@ -988,10 +1005,12 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
     a.hq = hq;
     a.hkv = hkv;
     a.hc = plan.heads_per_cta;
+    a.gfull = hq / hkv;
+    a.gsplit = plan.gsplit;
     a.block_size = block_size;
     a.rows = plan.rows_per_tile;
     a.stages = plan.stages;
-    const int G = hq / hkv;
+    const int G = hq / hkv / plan.gsplit;  // query heads per consumer warp
     const bool bf = dtype == PKV_BF16;
     CombineArgs c = {};
     c.part_o = a.part_o;

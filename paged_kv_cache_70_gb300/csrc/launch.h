@@ -89,6 +89,7 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src,
 // ---- decode -----------------------------------------------------------------
 struct DecodePlan {
     int heads_per_cta;   // KV heads one CTA handles (HC)
+    int gsplit;          // consumer warps per KV head and row (each with Hq/Hkv/gsplit query heads)
     int head_groups;     // grid.y = Hkv / HC
     int ctas;            // grid.x (CTAs along the key axis)
     int rows_per_tile;   // R: keys per pipeline stage (divides block_size)

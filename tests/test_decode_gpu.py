@@ -72,6 +72,12 @@ CASES = [
     ("f32", 32, 16, 128, 16, [40, 300]),            # Hkv > 8: heads split across CTAs
     ("bf16", 2, 2, 128, 3, [0, 0, 0]),              # all empty
     ("bf16", 16, 8, 128, 16, [4096] * 3 + [0] * 500 + [17] * 200),  # many sequences
+    ("bf16", 64, 8, 128, 16, [900, 1, 33, 4000]),   # G = 8: two warps per KV head
+    ("f32", 32, 4, 64, 32, [5, 64, 700]),           # G = 8, fp32, d = 64
+    ("bf16", 8, 1, 128, 64, [129, 2000]),           # G = 8, Hkv = 1 (four warps share rows)
+    ("bf16", 128, 8, 128, 256, [3000, 20000]),      # G = 16: four warps per KV head
+    ("f32", 32, 2, 128, 16, [1, 300, 17]),          # G = 16, Hkv = 2
+    ("bf16", 32, 1, 64, 16, [50, 1000]),            # G = 32: every warp on one KV head
 ]
 
 
@@ -161,6 +167,12 @@ def test_workspace_and_support_errors():
     assert e.value.status == -3
     q = torch.zeros(1, 16, 96, dtype=torch.bfloat16, device="cuda")
     kc = torch.zeros(4, 16, 8, 96, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pkv.PagedKVError) as e:
+        pkv.paged_decode(q, kc, kc, dev.decode_table, dev.cache_seqlens)
+    assert e.value.status == -2
+    # a GQA group of 12 (not 1, 2, 4, 8, 16 or 32)
+    q = torch.zeros(1, 96, 128, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(4, 16, 8, 128, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(pkv.PagedKVError) as e:
         pkv.paged_decode(q, kc, kc, dev.decode_table, dev.cache_seqlens)
     assert e.value.status == -2

@@ -78,7 +78,7 @@ def test_random_decode(seed):
     dtype = str(rng.choice(["bf16", "f32"]))
     d = int(rng.choice([64, 128]))
     hkv = int(rng.choice([1, 2, 4, 8, 16]))
-    hq = hkv * int(rng.choice([1, 2, 4]))
+    hq = hkv * int(rng.choice([1, 2, 4, 8]))
     B = int(rng.choice([1, 3, 16, 32, 48, 256]))
     lens = [int(rng.integers(0, 3000)) for _ in range(int(rng.integers(1, 40)))]
     step = W.make_step(name="rnd", dtype=dtype, hq=hq, hkv=hkv, d=d, block_size=B,
@@ -98,7 +98,7 @@ def test_random_shared_prefix(seed):
     rng = np.random.default_rng(1100 + seed)
     d = int(rng.choice([64, 128]))
     hkv = int(rng.choice([1, 2, 4, 8]))
-    hq = hkv * int(rng.choice([1, 2, 4]))
+    hq = hkv * int(rng.choice([1, 2, 4, 8]))
     B = int(rng.choice([8, 16, 32, 64, 128, 256]))
     ngr = int(rng.integers(1, 5))
     sizes = [int(rng.integers(1, 40)) for _ in range(ngr)]

@@ -105,10 +105,11 @@ def test_prefix_not_a_whole_block_is_flagged():
     assert pkv.paged_error_flags() & pkv.PKV_FLAG_BAD_LENGTH
 
 
-@pytest.mark.parametrize("hq,hkv", [(8, 8), (32, 8), (8, 2)])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (32, 8), (8, 2), (64, 8), (32, 2)])
 def test_group_sizes(hq, hkv):
-    """GQA group 1 (the prefix pass takes one head per work item), 4, and a
-    KV-head count below the decode kernel's warp count."""
+    """GQA group 1 (the prefix pass takes one head per work item), 4, 8 and 16
+    (two and four decode warps per KV head), and a KV-head count below the
+    decode kernel's warp count."""
     rng = np.random.default_rng(hq * 7 + hkv)
     q, kc, vc, table, lens, gcu, plen = build_groups(rng, [6, 9], [256, 512], 200, 32,
                                                      hq=hq, hkv=hkv)
