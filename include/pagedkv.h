@@ -142,7 +142,9 @@ int paged_kv_write_positions(const void* k, const void* v, int32_t kv_dtype,
  * count).  Returns 0 for invalid arguments.  There is no max_seqlen_k
  * argument: the keys of all sequences are cut into one share per CTA, so the
  * scratch holds (CTAs + batch) partial states whatever the lengths are, and
- * the lengths themselves are device data the host need not know.
+ * the lengths themselves are device data the host need not know.  On the
+ * tensor-core path (below) it adds c partial states per (sequence, query
+ * head), c = min(32, ceil(SMs / (batch * Hkv))).
  */
 size_t paged_decode_workspace_size(int32_t batch, const pkv_geom* geom);
 
@@ -158,6 +160,14 @@ size_t paged_decode_workspace_size(int32_t batch, const pkv_geom* geom);
  * sequence start is counted as one tile of keys); each CTA keeps the (m, l, o)
  * online-softmax state of its share and a second kernel merges the shares of
  * each sequence with the same rule and normalises.
+ * Tensor-core path: bf16 with G = Hq/Hkv >= 4 (and dividing 128), and block
+ * sizes the shared-prefix pass takes (multiples of 128, or divisors of 128 of
+ * at least 8).  There the whole pages of each sequence (128-key parts of larger
+ * pages) are attended on the tensor cores, in c chunks of
+ * ceil(max_blocks_per_seq * B / c) keys rounded up to 128, one work item per
+ * (sequence, KV head, chunk) with the G query heads as rows of one MMA tile.
+ * The split takes the keys after the last whole page, and the same second
+ * kernel merges the chunks' states with the split's.
  * Supported: head_dim 64 or 128; fp32 or bf16; G = Hq/Hkv in {1, 2, 4, 8, 16,
  * 32} (from 8 up, G/4 warps per KV head, 4 query heads each, share its K/V
  * tiles); with s = 8 / max(1, G/4) KV heads per CTA, Hkv divides s or is a

@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" entry points of libpagedkv (declared in
 // include/pagedkv.h): argument validation, per-device state (SM count,
 // shared-memory limit, error word) and dispatch to the kernel launchers.
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -128,6 +129,73 @@ int paged_kv_write_positions(const void* k, const void* v, int32_t kv_dtype,
         num_slots, dev.err, stream));
 }
 
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+static pkv::PrefixLaunch prefix_pass(const DeviceInfo& dev, const void* q, const void* k_cache,
+                                     const void* v_cache, const int32_t* table,
+                                     int32_t max_blocks, int32_t batch, const int32_t* group_cu,
+                                     const int32_t* group_plen, int32_t n_groups,
+                                     int32_t max_group_size, float scale, void* x_out,
+                                     float* x_lse, const pkv_geom* g, bool pdl);
+
+// bf16 decode with a GQA group of 4 or more: each sequence's whole pieces
+// (pages, or 128-key parts of larger pages) go through the tensor-core pass
+// as a group of one, in chunks of keys, about one (sequence, KV head, chunk)
+// item per SM; the split takes the keys after the last whole piece, and the
+// combine merges both.  (With 4 or more query heads per KV head the split
+// runs short of issue slots on the CUDA cores; with 2 it streams faster than
+// the tensor-core pass.)  Returns the chunks per sequence, 0 when the
+// CUDA-core split takes the whole decode.
+constexpr int kMaxTcChunks = 32;
+static int tc_chunks(const DeviceInfo& dev, int32_t batch, const pkv_geom* g) {
+    const int G = g->num_heads / g->num_kv_heads;
+    if (g->dtype != PKV_BF16 || G < 4 || 128 % G) return 0;
+    if (g->head_dim != 128 && g->head_dim != 64) return 0;
+    const int B = g->block_size;
+    if (!(B >= 128 ? B % 128 == 0 : (B >= 8 && 128 % B == 0))) return 0;
+    const int64_t units = (int64_t)batch * g->num_kv_heads;
+    if (units <= 0) return 0;
+    const int64_t kc = ((int64_t)dev.num_sms + units - 1) / units;
+    return (int)std::min<int64_t>(std::max<int64_t>(kc, 1), kMaxTcChunks);
+}
+// the chunks' partials: [kc, batch, hq, d] bf16 outputs, [kc, batch, hq] log2-sum-exp
+static size_t tc_extra_bytes(int kc, int32_t batch, const pkv_geom* g) {
+    return align256((size_t)kc * batch * g->num_heads * g->head_dim * 2) +
+           align256((size_t)kc * batch * g->num_heads * 4);
+}
+
+// the decode through the tensor-core pass (tc_chunks > 0), with or without
+// the append
+static int tc_decode(const DeviceInfo& dev, const pkv::DecodePlan& plan, int kc, const void* q,
+                     const void* k_cache, const void* v_cache, const int32_t* block_table,
+                     int32_t max_blocks, const int32_t* cache_seqlens, int32_t batch,
+                     float scale, void* out, void* workspace, const pkv_geom* geom,
+                     const pkv::DecodeAppend* ap, cudaStream_t stream) {
+    unsigned char* x_out = static_cast<unsigned char*>(workspace) + plan.ws_bytes;
+    float* x_lse = reinterpret_cast<float*>(
+        x_out + align256((size_t)kc * batch * geom->num_heads * geom->head_dim * 2));
+    pkv::PrefixLaunch pp = prefix_pass(dev, q, k_cache, v_cache, block_table, max_blocks, batch,
+                                       nullptr, nullptr, batch, 1, scale, x_out, x_lse, geom,
+                                       false);
+    const int64_t cap = (int64_t)max_blocks * geom->block_size;
+    int64_t per = (cap + kc - 1) / kc;
+    per = (per + 127) / 128 * 128;
+    pp.kchunks = kc;
+    pp.seqlens = cache_seqlens;
+    pp.chunk_keys = (int32_t)std::min<int64_t>(std::max<int64_t>(per, 128), 1 << 30);
+    cudaError_t e = pkv::launch_prefix(dev, pp, stream);
+    if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    const int32_t piece = geom->block_size >= 128 ? 128 : geom->block_size;
+    pkv::SharedPrefix sp{nullptr, nullptr, 0, x_out, x_lse, kc, piece};
+    pkv::DecodeChain ch{true};
+    return cuda_status(pkv::launch_decode(plan, q, k_cache, v_cache, block_table, max_blocks,
+                                          cache_seqlens, batch, scale, out, workspace,
+                                          geom->num_heads, geom->num_kv_heads, geom->head_dim,
+                                          geom->block_size, geom->num_blocks, geom->dtype,
+                                          dev.err, stream, &sp, ap, &ch));
+}
+
 size_t paged_decode_workspace_size(int32_t batch, const pkv_geom* geom) {
     if (check_geom(geom) != PKV_OK || batch < 0) return 0;
     DeviceInfo dev;
@@ -136,7 +204,8 @@ size_t paged_decode_workspace_size(int32_t batch, const pkv_geom* geom) {
     if (!pkv::plan_decode(dev, batch, geom->num_heads, geom->num_kv_heads, geom->head_dim,
                           geom->block_size, elt_size(geom->dtype), &plan))
         return 0;
-    return plan.ws_bytes;
+    const int kc = tc_chunks(dev, batch, geom);
+    return plan.ws_bytes + (kc ? tc_extra_bytes(kc, batch, geom) : 0);
 }
 
 int paged_decode(const void* q, const void* k_cache, const void* v_cache,
@@ -158,8 +227,13 @@ int paged_decode(const void* q, const void* k_cache, const void* v_cache,
     if (!pkv::plan_decode(dev, batch, geom->num_heads, geom->num_kv_heads, geom->head_dim,
                           geom->block_size, elt_size(geom->dtype), &plan))
         return PKV_ERR_UNSUPPORTED;
-    if (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256))
+    const int kc = tc_chunks(dev, batch, geom);
+    const size_t need = plan.ws_bytes + (kc ? tc_extra_bytes(kc, batch, geom) : 0);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
         return PKV_ERR_WORKSPACE;
+    if (kc)
+        return tc_decode(dev, plan, kc, q, k_cache, v_cache, block_table, max_blocks_per_seq,
+                         cache_seqlens, batch, scale, out, workspace, geom, nullptr, stream);
     return cuda_status(pkv::launch_decode(plan, q, k_cache, v_cache, block_table,
                                           max_blocks_per_seq, cache_seqlens, batch, scale, out,
                                           workspace, geom->num_heads, geom->num_kv_heads,
@@ -187,9 +261,14 @@ int paged_decode_append(const void* q, const void* k_new, const void* v_new, voi
     if (!pkv::plan_decode(dev, batch, geom->num_heads, geom->num_kv_heads, geom->head_dim,
                           geom->block_size, elt_size(geom->dtype), &plan))
         return PKV_ERR_UNSUPPORTED;
-    if (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256))
+    const int kc = tc_chunks(dev, batch, geom);
+    const size_t need = plan.ws_bytes + (kc ? tc_extra_bytes(kc, batch, geom) : 0);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
         return PKV_ERR_WORKSPACE;
     pkv::DecodeAppend ap{k_new, v_new, k_cache, v_cache};
+    if (kc)
+        return tc_decode(dev, plan, kc, q, k_cache, v_cache, block_table, max_blocks_per_seq,
+                         cache_seqlens, batch, scale, out, workspace, geom, &ap, stream);
     return cuda_status(pkv::launch_decode(plan, q, k_cache, v_cache, block_table,
                                           max_blocks_per_seq, cache_seqlens, batch, scale, out,
                                           workspace, geom->num_heads, geom->num_kv_heads,
@@ -232,8 +311,6 @@ int paged_varlen_prefill(const void* q, const void* k_cache, const void* v_cache
     if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
     return cuda_status(e);
 }
-
-static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // the prefix keys of a group are split into at most this many chunks (work
 // items for the SMs); each chunk leaves its own partial per (sequence, head)

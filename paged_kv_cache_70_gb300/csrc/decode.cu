@@ -109,6 +109,7 @@ struct DecodeArgs {
     int32_t n_groups;
     int32_t wait_prior;  // this grid completes only after the previous kernel has
     int32_t wait_inputs;  // wait for the previous kernel before reading any input
+    int32_t self_piece;   // > 0: each sequence's first L - L % self_piece keys are skipped
 };
 
 // The split's shares.  Tile t of sequence b sits at position
@@ -222,6 +223,8 @@ __device__ void plan_tiles(const DecodeArgs& a, int32_t* tstart, int32_t* sfirst
                 st = st < 0 ? 0 : (st > L ? L : st);
                 st -= st % a.rows;
             }
+        } else if (a.self_piece > 0) {
+            st = L - L % a.self_piece;  // covered by the tensor-core pass
         }
         slen[b] = L;
         sfirst[b] = st;
@@ -828,21 +831,22 @@ decode_combine_kernel(const CombineArgs c) {
     const int32_t chunk = share_cost(total, batch, c.ctas);
     const int32_t ub = kSeqCost * (b + 1);  // u(t) - t for this sequence's tiles
     const int c0 = (tb0 + ub) / chunk, c1 = tb1 > tb0 ? (tb1 - 1 + ub) / chunk : c0 - 1;
+    // the states to merge: the prefix chunks (x < x_chunks), then the split's
+    // pieces c0 .. c1, in rounds of U with every load of a round in flight
     const int64_t xstride = (int64_t)batch * hq;  // one prefix chunk's (sequence, head) count
-    for (int x = 0; x < c.x_chunks; ++x) {
-        float xo[DPL];
-        const float mx = c.x_lse[x * xstride + bh];
-        load_row<true, DPL>(c.x_out, (x * xstride + bh) * D + lane * DPL, xo);
-        merge_state<DPL>(M, L, acc, mx, 1.f, xo);
-    }
-    for (int base = c0; base <= c1; base += U) {
+    const int nx = c.x_chunks, n = nx + (c1 - c0 + 1);
+    for (int base = 0; base < n; base += U) {
         float2 ml[U];
         float o[U][DPL];
 #pragma unroll
         for (int i = 0; i < U; ++i) {
             ml[i] = make_float2(-INFINITY, 0.f);
-            if (base + i <= c1) {
-                const int64_t slot = (int64_t)(base + i) + b;
+            const int j = base + i;
+            if (j < nx) {
+                ml[i] = make_float2(c.x_lse[j * xstride + bh], 1.f);
+                load_row<true, DPL>(c.x_out, (j * xstride + bh) * D + lane * DPL, o[i]);
+            } else if (j < n) {
+                const int64_t slot = (int64_t)(c0 + j - nx) + b;
                 ml[i] = *reinterpret_cast<const float2*>(c.part_ml + (slot * hq + h) * 2);
                 load_row<false, DPL>(c.part_o, (slot * hq + h) * D + lane * DPL, o[i]);
             }
@@ -984,6 +988,7 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
     a.group_cu = sp ? sp->group_cu : nullptr;
     a.group_plen = sp ? sp->group_plen : nullptr;
     a.n_groups = sp ? sp->n_groups : 0;
+    a.self_piece = sp ? sp->self_piece : 0;
 
     a.q = q;
     a.k_cache = static_cast<const unsigned char*>(k_cache);

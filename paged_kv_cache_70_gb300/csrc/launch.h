@@ -104,12 +104,14 @@ constexpr int kDecodeMaxBatch = 4096;
 // attention (normalised output and log2-sum-exp per sequence and head) was
 // computed separately; the decode covers the keys after it and merges.
 struct SharedPrefix {
-    const int32_t* group_cu;    // [n_groups + 1]
+    const int32_t* group_cu;    // [n_groups + 1] (null with self_piece)
     const int32_t* group_plen;  // [n_groups]
     int32_t n_groups;
     const void* x_out;          // [x_chunks, batch, hq, d] bf16
     const float* x_lse;         // [x_chunks, batch, hq]
     int32_t x_chunks;           // prefix partials per (sequence, head)
+    int32_t self_piece;         // > 0: each sequence's own whole pieces of this many keys
+                                // were the prefix; the split takes the keys after them
 };
 
 // In-place append: the new token of every sequence ([batch, hkv, d], the
@@ -152,14 +154,16 @@ struct PrefixLaunch {
     const void* k_cache;
     const void* v_cache;
     const int32_t* table;       // [batch, max_blocks]; a group reads its first member's row
-    const int32_t* group_cu;    // [n_groups + 1]
+    const int32_t* group_cu;    // [n_groups + 1]; null: every sequence is a group of one
     const int32_t* group_plen;  // [n_groups]
+    const int32_t* seqlens;     // groups of one: their prefix is the whole pieces of seqlens[g]
     void* x_out;
     float* x_lse;
     unsigned int* err;
     int64_t num_blocks;
     float scale;
     int32_t max_blocks, batch, hq, hkv, hd, block_size, n_groups, max_group_size, kchunks;
+    int32_t chunk_keys;         // > 0: keys per chunk (a multiple of 128), else prefix / kchunks
     bool pdl;                   // launch as a programmatic dependent of the previous kernel
 };
 

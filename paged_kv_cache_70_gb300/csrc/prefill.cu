@@ -734,8 +734,9 @@ struct PShape {
 };
 
 struct PrefixArgs {
-    const int32_t* group_cu;    // [n_groups + 1]
+    const int32_t* group_cu;    // [n_groups + 1]; null: every sequence its own group
     const int32_t* group_plen;  // [n_groups]
+    const int32_t* seqlens;     // groups of one: the whole pieces of seqlens[g] keys
     const int32_t* table;       // [batch, max_blocks]
     uint16_t* x_out;            // [kchunks, batch, hq, HD] bf16
     float* x_lse;               // [kchunks, batch, hq]
@@ -750,6 +751,7 @@ struct PrefixArgs {
     int32_t piece;       // rows per K/V box = min(B, 128)
     int32_t oob_row;     // a row beyond the pools (zero-filled by TMA)
     int32_t kchunks;
+    int32_t chunk_keys;  // > 0: keys per chunk (a multiple of 128), else prefix / kchunks
     int32_t n_groups;
 };
 
@@ -786,20 +788,29 @@ __device__ __forceinline__ void prefix_cta(const CUtensorMap& tmap_q, const CUte
     const int per_blk = 128 / G;  // members per CTA
     const int kvh = by;
     const int g = bz / a.kchunks, chunk = bz % a.kchunks;
-    const int32_t gm0 = a.group_cu[g], gm1 = a.group_cu[g + 1];
+    const bool own = a.group_cu == nullptr;  // groups of one sequence
+    const int32_t gm0 = own ? g : a.group_cu[g], gm1 = own ? g + 1 : a.group_cu[g + 1];
     const int32_t m0 = gm0 + (int32_t)bx * per_blk;
     if (m0 >= gm1 || m0 >= a.batch || m0 < 0) return;  // no member in this block
     const int32_t m1 = min(min(gm1, m0 + per_blk), a.batch);
     // the prefix: whole pieces only (a piece past the keys arrives zero-filled)
     const int32_t cap = a.max_blocks * a.block_size;
-    int32_t plen = a.group_plen[g];
-    if (plen < 0 || plen > cap || plen % a.block_size) {
-        if (threadIdx.x == 0 && bx == 0 && by == 0)
-            flag_error(a.err, PKV_FLAG_BAD_LENGTH);
+    int32_t plen;
+    if (own) {  // the sequence's whole pieces (its length is checked by the split)
+        plen = a.seqlens[g];
         plen = plen < 0 ? 0 : (plen > cap ? cap : plen);
+    } else {
+        plen = a.group_plen[g];
+        if (plen < 0 || plen > cap || plen % a.block_size) {
+            if (threadIdx.x == 0 && bx == 0 && by == 0)
+                flag_error(a.err, PKV_FLAG_BAD_LENGTH);
+            plen = plen < 0 ? 0 : (plen > cap ? cap : plen);
+        }
     }
     plen -= plen % a.piece;
-    const int32_t per = ((plen + a.kchunks - 1) / a.kchunks + kPBN - 1) / kPBN * kPBN;
+    const int32_t per = a.chunk_keys > 0
+                            ? a.chunk_keys
+                            : ((plen + a.kchunks - 1) / a.kchunks + kPBN - 1) / kPBN * kPBN;
     const int32_t kbase = chunk * per;
     const int32_t klen = max(0, min(per, plen - kbase));
     const int n_tiles = (klen + kPBN - 1) / kPBN;
@@ -1277,6 +1288,8 @@ cudaError_t prepare_prefix(const PrefixLaunch& p, PrefixArgs* a, CUtensorMap* ma
         return cudaErrorInvalidValue;
     a->group_cu = p.group_cu;
     a->group_plen = p.group_plen;
+    a->seqlens = p.seqlens;
+    a->chunk_keys = p.chunk_keys;
     a->table = p.table;
     a->x_out = static_cast<uint16_t*>(p.x_out);
     a->x_lse = p.x_lse;

@@ -87,10 +87,12 @@ def test_position_past_the_table_is_flagged_and_not_written():
 
 
 @pytest.mark.parametrize("dtype,hq,hkv,d,B", [("f32", 8, 2, 64, 1), ("bf16", 32, 8, 128, 48),
-                                              ("f32", 16, 16, 128, 16)])
+                                              ("f32", 16, 16, 128, 16), ("bf16", 64, 8, 128, 16),
+                                              ("bf16", 32, 2, 64, 256)])
 def test_append_shapes(dtype, hq, hkv, d, B):
     """Other dtypes, head sizes, GQA groups and block sizes (B = 1, B not a
-    power of two, Hkv above the decode kernel's warp count)."""
+    power of two, Hkv above the decode kernel's warp count; bf16 groups of 8
+    and 16, whose whole pages go through the tensor-core pass)."""
     lens = [0, 1, B, 3 * B + 1, 700]
     step = W.make_step(name="app", dtype=dtype, hq=hq, hkv=hkv, d=d, block_size=B,
                        decode_lens=lens, seed=sum(lens) + hq + d)

@@ -72,12 +72,15 @@ CASES = [
     ("f32", 32, 16, 128, 16, [40, 300]),            # Hkv > 8: heads split across CTAs
     ("bf16", 2, 2, 128, 3, [0, 0, 0]),              # all empty
     ("bf16", 16, 8, 128, 16, [4096] * 3 + [0] * 500 + [17] * 200),  # many sequences
-    ("bf16", 64, 8, 128, 16, [900, 1, 33, 4000]),   # G = 8: two warps per KV head
-    ("f32", 32, 4, 64, 32, [5, 64, 700]),           # G = 8, fp32, d = 64
-    ("bf16", 8, 1, 128, 64, [129, 2000]),           # G = 8, Hkv = 1 (four warps share rows)
-    ("bf16", 128, 8, 128, 256, [3000, 20000]),      # G = 16: four warps per KV head
-    ("f32", 32, 2, 128, 16, [1, 300, 17]),          # G = 16, Hkv = 2
-    ("bf16", 32, 1, 64, 16, [50, 1000]),            # G = 32: every warp on one KV head
+    ("bf16", 64, 8, 128, 16, [900, 1, 33, 4000]),   # G = 8: pages on the tensor cores
+    ("f32", 32, 4, 64, 32, [5, 64, 700]),           # G = 8, fp32: two split warps per KV head
+    ("bf16", 8, 1, 128, 64, [129, 2000]),           # G = 8, Hkv = 1
+    ("bf16", 128, 8, 128, 256, [3000, 20000]),      # G = 16, long context
+    ("f32", 32, 2, 128, 16, [1, 300, 17]),          # G = 16, fp32: four split warps per KV head
+    ("bf16", 32, 1, 64, 16, [50, 1000]),            # G = 32
+    ("bf16", 64, 8, 128, 48, [47, 48, 49, 3000]),   # G = 8, B = 48: the CUDA-core split alone
+    ("bf16", 64, 8, 64, 128, [127, 128, 129, 0, 5000]),  # G = 8 on the tensor cores, d = 64
+    ("bf16", 16, 1, 128, 8, [1, 7, 8, 9, 1000] * 40),    # G = 16, 200 sequences of pages of 8
 ]
 
 
