@@ -831,22 +831,33 @@ decode_combine_kernel(const CombineArgs c) {
     const int32_t chunk = share_cost(total, batch, c.ctas);
     const int32_t ub = kSeqCost * (b + 1);  // u(t) - t for this sequence's tiles
     const int c0 = (tb0 + ub) / chunk, c1 = tb1 > tb0 ? (tb1 - 1 + ub) / chunk : c0 - 1;
-    // the states to merge: the prefix chunks (x < x_chunks), then the split's
-    // pieces c0 .. c1, in rounds of U with every load of a round in flight
+    // the prefix chunks' states (rounds of UX), then the split's pieces c0 ..
+    // c1 (rounds of U), every load of a round in flight
+    constexpr int UX = U < 8 ? U : 8;
     const int64_t xstride = (int64_t)batch * hq;  // one prefix chunk's (sequence, head) count
-    const int nx = c.x_chunks, n = nx + (c1 - c0 + 1);
-    for (int base = 0; base < n; base += U) {
+    for (int base = 0; base < c.x_chunks; base += UX) {
+        float mx[UX];
+        float xo[UX][DPL];
+#pragma unroll
+        for (int i = 0; i < UX; ++i) {
+            mx[i] = -INFINITY;
+            if (base + i < c.x_chunks) {
+                const int64_t xi = (int64_t)(base + i) * xstride + bh;
+                mx[i] = c.x_lse[xi];
+                load_row<true, DPL>(c.x_out, xi * D + lane * DPL, xo[i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < UX; ++i) merge_state<DPL>(M, L, acc, mx[i], 1.f, xo[i]);
+    }
+    for (int base = c0; base <= c1; base += U) {
         float2 ml[U];
         float o[U][DPL];
 #pragma unroll
         for (int i = 0; i < U; ++i) {
             ml[i] = make_float2(-INFINITY, 0.f);
-            const int j = base + i;
-            if (j < nx) {
-                ml[i] = make_float2(c.x_lse[j * xstride + bh], 1.f);
-                load_row<true, DPL>(c.x_out, (j * xstride + bh) * D + lane * DPL, o[i]);
-            } else if (j < n) {
-                const int64_t slot = (int64_t)(c0 + j - nx) + b;
+            if (base + i <= c1) {
+                const int64_t slot = (int64_t)(base + i) + b;
                 ml[i] = *reinterpret_cast<const float2*>(c.part_ml + (slot * hq + h) * 2);
                 load_row<false, DPL>(c.part_o, (slot * hq + h) * D + lane * DPL, o[i]);
             }
