@@ -162,12 +162,12 @@ size_t paged_decode_workspace_size(int32_t batch, const pkv_geom* geom);
  * each sequence with the same rule and normalises.
  * Tensor-core path: bf16 with G = Hq/Hkv >= 4 (and dividing 128), and block
  * sizes the shared-prefix pass takes (multiples of 128, or divisors of 128 of
- * at least 8).  There the whole pages of each sequence (128-key parts of larger
- * pages) are attended on the tensor cores, in c chunks of
- * ceil(max_blocks_per_seq * B / c) keys rounded up to 128, one work item per
- * (sequence, KV head, chunk) with the G query heads as rows of one MMA tile.
- * The split takes the keys after the last whole page, and the same second
- * kernel merges the chunks' states with the split's.
+ * at least 8).  There the keys of each sequence are attended on the tensor
+ * cores in c chunks of ceil(max_blocks_per_seq * B / c) keys rounded up to
+ * 128, one work item per (sequence, KV head, chunk) with the G query heads as
+ * rows of one MMA tile (keys past the length in the last page are masked, and
+ * their V rows zeroed in shared memory); the same second kernel merges the
+ * chunks' states (two launches, no split).
  * Supported: head_dim 64 or 128; fp32 or bf16; G = Hq/Hkv in {1, 2, 4, 8, 16,
  * 32} (from 8 up, G/4 warps per KV head, 4 query heads each, share its K/V
  * tiles); with s = 8 / max(1, G/4) KV heads per CTA, Hkv divides s or is a

@@ -138,14 +138,13 @@ static pkv::PrefixLaunch prefix_pass(const DeviceInfo& dev, const void* q, const
                                      int32_t max_group_size, float scale, void* x_out,
                                      float* x_lse, const pkv_geom* g, bool pdl);
 
-// bf16 decode with a GQA group of 4 or more: each sequence's whole pieces
-// (pages, or 128-key parts of larger pages) go through the tensor-core pass
-// as a group of one, in chunks of keys, about one (sequence, KV head, chunk)
-// item per SM; the split takes the keys after the last whole piece, and the
-// combine merges both.  (With 4 or more query heads per KV head the split
-// runs short of issue slots on the CUDA cores; with 2 it streams faster than
-// the tensor-core pass.)  Returns the chunks per sequence, 0 when the
-// CUDA-core split takes the whole decode.
+// bf16 decode with a GQA group of 4 or more: every sequence's keys go through
+// the tensor-core pass as a group of one, in chunks of keys, about one
+// (sequence, KV head, chunk) item per SM, and the combine merges the chunks
+// (no split launch).  With 4 or more query heads per KV head the split runs
+// short of issue slots on the CUDA cores; with 2 it streams faster than the
+// tensor-core pass.  Returns the chunks per sequence, 0 when the CUDA-core
+// split takes the decode.
 constexpr int kMaxTcChunks = 32;
 static int tc_chunks(const DeviceInfo& dev, int32_t batch, const pkv_geom* g) {
     const int G = g->num_heads / g->num_kv_heads;
@@ -186,9 +185,8 @@ static int tc_decode(const DeviceInfo& dev, const pkv::DecodePlan& plan, int kc,
     cudaError_t e = pkv::launch_prefix(dev, pp, stream);
     if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return PKV_ERR_CUDA;
-    const int32_t piece = geom->block_size >= 128 ? 128 : geom->block_size;
-    pkv::SharedPrefix sp{nullptr, nullptr, 0, x_out, x_lse, kc, piece};
-    pkv::DecodeChain ch{true};
+    pkv::SharedPrefix sp{nullptr, nullptr, 0, x_out, x_lse, kc};
+    pkv::DecodeChain ch{true, true};
     return cuda_status(pkv::launch_decode(plan, q, k_cache, v_cache, block_table, max_blocks,
                                           cache_seqlens, batch, scale, out, workspace,
                                           geom->num_heads, geom->num_kv_heads, geom->head_dim,

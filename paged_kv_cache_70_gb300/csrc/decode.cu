@@ -109,7 +109,6 @@ struct DecodeArgs {
     int32_t n_groups;
     int32_t wait_prior;  // this grid completes only after the previous kernel has
     int32_t wait_inputs;  // wait for the previous kernel before reading any input
-    int32_t self_piece;   // > 0: each sequence's first L - L % self_piece keys are skipped
 };
 
 // The split's shares.  Tile t of sequence b sits at position
@@ -223,8 +222,6 @@ __device__ void plan_tiles(const DecodeArgs& a, int32_t* tstart, int32_t* sfirst
                 st = st < 0 ? 0 : (st > L ? L : st);
                 st -= st % a.rows;
             }
-        } else if (a.self_piece > 0) {
-            st = L - L % a.self_piece;  // covered by the tensor-core pass
         }
         slen[b] = L;
         sfirst[b] = st;
@@ -695,7 +692,7 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
 struct CombineArgs {
     const float* part_o;
     const float* part_ml;
-    const int32_t* tstart;
+    const int32_t* tstart;  // null: no split pieces (the prefix chunks hold every key)
     int32_t batch;
     int ctas;
     int hq;
@@ -826,8 +823,8 @@ decode_combine_kernel(const CombineArgs c) {
     // wait until the split kernel's partials are complete and visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!live) return;
-    const int32_t total = c.tstart[batch];
-    const int32_t tb0 = c.tstart[b], tb1 = c.tstart[b + 1];
+    const int32_t total = c.tstart ? c.tstart[batch] : 0;
+    const int32_t tb0 = c.tstart ? c.tstart[b] : 0, tb1 = c.tstart ? c.tstart[b + 1] : 0;
     const int32_t chunk = share_cost(total, batch, c.ctas);
     const int32_t ub = kSeqCost * (b + 1);  // u(t) - t for this sequence's tiles
     const int c0 = (tb0 + ub) / chunk, c1 = tb1 > tb0 ? (tb1 - 1 + ub) / chunk : c0 - 1;
@@ -957,14 +954,16 @@ bool plan_decode(const DeviceInfo& dev, int32_t batch, int hq, int hkv, int d, i
 
 template <int D, bool BF16, int G>
 static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a,
-                                   const CombineArgs& c, cudaStream_t stream) {
-    auto kern = decode_split_kernel<D, BF16, G>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)plan.smem_bytes);
-    if (e != cudaSuccess) return e;
-    e = launch_dependent(kern, dim3(plan.ctas, plan.head_groups), dim3(decode_threads<G>()),
-                         plan.smem_bytes, stream, a);
-    if (e != cudaSuccess) return e;
+                                   const CombineArgs& c, bool split, cudaStream_t stream) {
+    if (split) {
+        auto kern = decode_split_kernel<D, BF16, G>;
+        cudaError_t e = cudaFuncSetAttribute(
+            kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem_bytes);
+        if (e != cudaSuccess) return e;
+        e = launch_dependent(kern, dim3(plan.ctas, plan.head_groups),
+                             dim3(decode_threads<G>()), plan.smem_bytes, stream, a);
+        if (e != cudaSuccess) return e;
+    }
     // combine: programmatic dependent of the split kernel, one warp per
     // (sequence, head); 16 pieces in flight per round while every warp of
     // the batch still fits on the GPU at once (4 warps a CTA, 4 CTAs an SM),
@@ -999,7 +998,6 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
     a.group_cu = sp ? sp->group_cu : nullptr;
     a.group_plen = sp ? sp->group_plen : nullptr;
     a.n_groups = sp ? sp->n_groups : 0;
-    a.self_piece = sp ? sp->self_piece : 0;
 
     a.q = q;
     a.k_cache = static_cast<const unsigned char*>(k_cache);
@@ -1031,7 +1029,8 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
     CombineArgs c = {};
     c.part_o = a.part_o;
     c.part_ml = a.part_ml;
-    c.tstart = a.tstart_out;
+    const bool split = !(chain && chain->no_split);
+    c.tstart = split ? a.tstart_out : nullptr;
     c.batch = batch;
     c.ctas = plan.ctas;
     c.hq = hq;
@@ -1058,7 +1057,7 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
     c.err = err;
 #define PKV_DECODE_CASE(DD, BB, GG) \
     if (d == DD && bf == BB && G == GG) \
-        return launch_decode_t<DD, BB, GG>(plan, a, c, stream);
+        return launch_decode_t<DD, BB, GG>(plan, a, c, split, stream);
     PKV_DECODE_CASE(128, true, 1) PKV_DECODE_CASE(128, true, 2) PKV_DECODE_CASE(128, true, 4)
     PKV_DECODE_CASE(128, false, 1) PKV_DECODE_CASE(128, false, 2) PKV_DECODE_CASE(128, false, 4)
     PKV_DECODE_CASE(64, true, 1) PKV_DECODE_CASE(64, true, 2) PKV_DECODE_CASE(64, true, 4)

@@ -104,14 +104,12 @@ constexpr int kDecodeMaxBatch = 4096;
 // attention (normalised output and log2-sum-exp per sequence and head) was
 // computed separately; the decode covers the keys after it and merges.
 struct SharedPrefix {
-    const int32_t* group_cu;    // [n_groups + 1] (null with self_piece)
+    const int32_t* group_cu;    // [n_groups + 1]
     const int32_t* group_plen;  // [n_groups]
     int32_t n_groups;
     const void* x_out;          // [x_chunks, batch, hq, d] bf16
     const float* x_lse;         // [x_chunks, batch, hq]
     int32_t x_chunks;           // prefix partials per (sequence, head)
-    int32_t self_piece;         // > 0: each sequence's own whole pieces of this many keys
-                                // were the prefix; the split takes the keys after them
 };
 
 // In-place append: the new token of every sequence ([batch, hkv, d], the
@@ -128,6 +126,7 @@ struct DecodeAppend {
 // after that kernel has (so the combine, which waits for the split, sees it).
 struct DecodeChain {
     bool pdl_split;
+    bool no_split;  // the prefix chunks hold every key: the combine alone follows them
 };
 
 // Returns false when the geometry is not supported.

@@ -736,7 +736,7 @@ struct PShape {
 struct PrefixArgs {
     const int32_t* group_cu;    // [n_groups + 1]; null: every sequence its own group
     const int32_t* group_plen;  // [n_groups]
-    const int32_t* seqlens;     // groups of one: the whole pieces of seqlens[g] keys
+    const int32_t* seqlens;     // groups of one: all seqlens[g] keys of sequence g
     const int32_t* table;       // [batch, max_blocks]
     uint16_t* x_out;            // [kchunks, batch, hq, HD] bf16
     float* x_lse;               // [kchunks, batch, hq]
@@ -796,9 +796,13 @@ __device__ __forceinline__ void prefix_cta(const CUtensorMap& tmap_q, const CUte
     // the prefix: whole pieces only (a piece past the keys arrives zero-filled)
     const int32_t cap = a.max_blocks * a.block_size;
     int32_t plen;
-    if (own) {  // the sequence's whole pieces (its length is checked by the split)
+    if (own) {  // all of the sequence's keys; the last piece may be partial
         plen = a.seqlens[g];
-        plen = plen < 0 ? 0 : (plen > cap ? cap : plen);
+        if (plen < 0 || plen > cap) {
+            if (threadIdx.x == 0 && bz % a.kchunks == 0 && by == 0)
+                flag_error(a.err, PKV_FLAG_BAD_LENGTH);
+            plen = plen < 0 ? 0 : (plen > cap ? cap : plen);
+        }
     } else {
         plen = a.group_plen[g];
         if (plen < 0 || plen > cap || plen % a.block_size) {
@@ -806,8 +810,8 @@ __device__ __forceinline__ void prefix_cta(const CUtensorMap& tmap_q, const CUte
                 flag_error(a.err, PKV_FLAG_BAD_LENGTH);
             plen = plen < 0 ? 0 : (plen > cap ? cap : plen);
         }
+        plen -= plen % a.piece;
     }
-    plen -= plen % a.piece;
     const int32_t per = a.chunk_keys > 0
                             ? a.chunk_keys
                             : ((plen + a.kchunks - 1) / a.kchunks + kPBN - 1) / kPBN * kPBN;
@@ -1086,6 +1090,20 @@ __device__ __forceinline__ void prefix_cta(const CUtensorMap& tmap_q, const CUte
             l = l * alpha + psum;
             tmem_st32(tm_s, sr);
             tmem_st32(tm_s + 32, sr + 32);
+            if (own && ragged) {
+                // a sequence's last tile may end inside a page: its V rows past
+                // the keys hold whatever the pool holds there; zero them so that
+                // p = 0 never meets a non-finite value
+                const int sv = j % kPSV;
+                if (!warp_wait(&v_full[sv], (j / kPSV) & 1, a.err)) { ok = false; break; }
+                if (t >= lim) {
+                    unsigned char* vs = sm + Sh::OFF_V + sv * kTileBytes;
+#pragma unroll
+                    for (int c = 0; c < HD / 8; ++c)
+                        *reinterpret_cast<uint4*>(vs + swz(t, c)) = make_uint4(0, 0, 0, 0);
+                }
+                fence_async_smem();
+            }
             if (i > 0 && __any_sync(0xffffffffu, resc)) {
                 // S_x(j) complete implies PV_x(j - 2) is: O_x is stable; scale
                 // it before PV_x(j) accumulates

@@ -100,6 +100,32 @@ def test_decode_shapes(dtype, hq, hkv, d, B, lens):
     assert pkv.paged_error_flags() == 0
 
 
+@pytest.mark.parametrize("hq,hkv,B", [(32, 8, 16), (64, 8, 256), (16, 8, 16), (32, 4, 48)])
+def test_nonfinite_pool_past_the_keys_is_ignored(hq, hkv, B):
+    """Every pool row past a sequence's keys holds NaN, in the last page and
+    in every unused block: nothing of it may reach the output.  Groups of 4 and
+    8 with B = 16 or 256 take the tensor-core route (masked scores, zeroed V
+    rows of the partial last page); 16/8 heads and B = 48 take the split."""
+    lens = [1, 15, 17, 130, 1000, 4000]
+    step = W.make_step(name="nan", dtype="bf16", hq=hq, hkv=hkv, d=128, block_size=B,
+                       decode_lens=[L - 1 for L in lens], seed=77 + hq + B)
+    step.cache_seqlens = np.asarray(lens, np.int32)
+    kc, vc = step.k_cache.copy(), step.v_cache.copy()
+    keep = np.zeros(kc.shape[:2], dtype=bool)  # [blocks, B]: rows that hold a key
+    for b, L in enumerate(lens):
+        for p in range(L):
+            keep[step.decode_table[b, p // B], p % B] = True
+    kc[~keep] = 0x7fc0  # bf16 NaN
+    vc[~keep] = 0x7fc0
+    step.k_cache, step.v_cache = kc, vc
+    out = widen(DevStep(step).decode())
+    torch.cuda.synchronize()
+    assert np.all(np.isfinite(out))
+    want = _oracle_decode(step, kc, vc)
+    assert_close(out, want, "bf16", f"nan pool {hq}/{hkv} B{B}")
+    assert pkv.paged_error_flags() == 0
+
+
 def test_single_key_returns_v0():
     step = W.make_step(name="one", dtype="f32", hq=4, hkv=2, d=128, block_size=16,
                        decode_lens=[0, 0], seed=3)
