@@ -715,8 +715,8 @@ def run_qwen3(args, world, pkv, W, peaks, flush, line):
 
 # Decode shapes beyond the workloads: the long-context lengths (8 sequences,
 # U[16384, 40960] keys, block 256) with GQA groups of 4, 8 and 16, head_dim 64,
-# and 4 KV heads.  bf16 groups of 4 and more run their whole pages through the
-# tensor-core pass (three launches: that pass, the split, the combine).
+# and 4 KV heads.  bf16 groups of 4 and more attend through the tensor-core
+# pass (two launches: that pass and the combine; no split).
 SHAPES = {"gqa4_32q_8kv_d128": (32, 8, 128), "d64_16q_8kv": (16, 8, 64),
           "16q_4kv_d128": (16, 4, 128), "gqa8_64q_8kv_d128": (64, 8, 128),
           "gqa16_128q_8kv_d128": (128, 8, 128)}
@@ -733,14 +733,14 @@ def run_shapes(args, world, pkv, W, peaks, flush, line):
         ms_step, per = time_parts([dev.run], args.steps, args.warmup, world, flush)
         nbytes = decode_append_bytes(s)
         tc = hq // hkv >= 4
-        kernels = ("paged_decode_append (tensor-core pass + split + combine)" if tc else
+        kernels = ("paged_decode_append (tensor-core pass + combine)" if tc else
                    "paged_decode_append (split kernel + combine)")
         out[name] = {"value": round(world * nbytes / (ms_step * 1e-3) / 1e9, 2), "unit": "GB/s",
                      "ms_per_step": round(ms_step, 5), "bytes_per_step": nbytes,
                      "path": "tensor cores" if tc else "CUDA cores",
                      "roofline": hbm_roofline(kernels, nbytes, per[0][0], per[0][1], hbm_peak,
                                               peak_src, "decode_" + name)}
-        line["gpu_launches"] += (DecodeStep.launches + (1 if tc else 0)) * args.steps
+        line["gpu_launches"] += DecodeStep.launches * args.steps
         del dev
         torch.cuda.empty_cache()
     line["decode_shapes"] = {
