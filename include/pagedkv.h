@@ -343,10 +343,10 @@ int paged_mixed_step(const pkv_mixed_step* step, void* k_cache, void* v_cache, v
  * device array of PKV_NOALLOC_SCRATCH_BYTES inside the library, which every
  * GPU that loads the library holds until the process exits.
  *   - Same arguments, layouts, results and support matrix as paged_decode,
- *     minus workspace / workspace_bytes.
- *   - Returns PKV_ERR_WORKSPACE when the problem needs more scratch than the
- *     array holds, i.e. when paged_decode_workspace_size(batch, geom) >
- *     PKV_NOALLOC_SCRATCH_BYTES.  That size is about
+ *     minus workspace / workspace_bytes.  It always takes the CUDA-core split
+ *     (never paged_decode's tensor-core path), whose scratch is the array.
+ *   - Returns PKV_ERR_WORKSPACE when the split needs more scratch than the
+ *     array holds.  That scratch is about
  *     (SMs + batch) * Hq * (head_dim + 2) * 4 bytes, so the limit is
  *     batch <= PKV_NOALLOC_SCRATCH_BYTES / (Hq * (head_dim + 2) * 4) - SMs:
  *     about 850 sequences for Hq=16, head_dim=128 on a 152-SM GPU.

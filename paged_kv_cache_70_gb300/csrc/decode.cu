@@ -25,7 +25,12 @@
 //  * Math.  Eight consumer warps; each warp owns one KV head and its G query
 //    heads (the K/V tile is shared across the GQA group).  For G = 4 the CTA
 //    has 12 warps and setmaxnreg moves registers from the producer's
-//    warpgroup to the consumers, which hold 4 heads' q and o.  Within a warp,
+//    warpgroup to the consumers, which hold 4 heads' q and o.  Groups of 8, 16
+//    and 32 run the group-4 kernel with G / 4 warps per KV head, each holding
+//    4 of its query heads.  (bf16 decode with G >= 4 normally attends on the
+//    tensor cores instead, through the shared-prefix pass with every sequence
+//    a group of one; this split then serves fp32, the block sizes that pass
+//    does not take, and the suffixes of shared-prefix steps.)  Within a warp,
 //    groups of D/16 lanes take key rows, every lane holding 16 of the D
 //    dimensions of q (pre-scaled by scale*log2 e) and of o as fp32 pairs; a
 //    group handles two key rows at a time with packed fp32x2 FMAs (four

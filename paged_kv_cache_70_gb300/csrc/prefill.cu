@@ -682,6 +682,11 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tmap_q, const CUt
 // the state (m = lse, l = 1, o = out) that the decode's combine merges with the
 // sequence's own keys by the boxed rule.  A chunk with no keys leaves lse =
 // -inf (the merge skips it).
+// With no group arrays every sequence is a group of one whose "prefix" is all
+// of its seqlens[b] keys, in chunks of chunk_keys: bf16 decode with 4 or more
+// query heads per KV head on the tensor cores.  Its last tile may end inside a
+// page; those scores are masked like any ragged tile's, and the V rows past
+// the keys are zeroed in shared memory before PV.
 //
 // GB300 design.  One CTA per (group, KV head, key chunk, block of members):
 //   - its single 128-row Q tile holds the group's queries of the KV head's G
