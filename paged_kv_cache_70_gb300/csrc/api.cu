@@ -183,7 +183,14 @@ static int tc_decode(const DeviceInfo& dev, const pkv::DecodePlan& plan, int kc,
     pp.seqlens = cache_seqlens;
     pp.chunk_keys = (int32_t)std::min<int64_t>(std::max<int64_t>(per, 128), 1 << 30);
     cudaError_t e = pkv::launch_prefix(dev, pp, stream);
-    if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+    if (e == cudaErrorNotSupported)  // the pass does not take this pool (nothing was
+                                     // launched): the split alone does the decode
+        return cuda_status(pkv::launch_decode(plan, q, k_cache, v_cache, block_table, max_blocks,
+                                              cache_seqlens, batch, scale, out, workspace,
+                                              geom->num_heads, geom->num_kv_heads,
+                                              geom->head_dim, geom->block_size,
+                                              geom->num_blocks, geom->dtype, dev.err, stream,
+                                              nullptr, ap, nullptr));
     if (e != cudaSuccess) return PKV_ERR_CUDA;
     pkv::SharedPrefix sp{nullptr, nullptr, 0, x_out, x_lse, kc};
     pkv::DecodeChain ch{true, true};
