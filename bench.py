@@ -1010,6 +1010,19 @@ def run_mixed_step(args, world, pkv, W, peaks, flush, line):
         "roofline": hbm_roofline("paged_mixed_step (every kernel of the call)", nbytes, mean,
                                  med, hbm_peak, peak_src, "mixed_step")}
     line["gpu_launches"] += 4 * args.steps  # write, tensor-core launch, split, combine
+    # the same step as ONE kernel launch (paged_mixed_step_one_launch)
+    call1 = lambda: pkv.paged_mixed_step(kc, vc, s.scale, prefill=prefill, decode=decode,
+                                         workspace=ws, one_launch=True)
+    _, per1 = time_parts([call1], args.steps, args.warmup, world, flush)
+    mean1, med1 = per1[0]
+    gbs1 = nbytes / (mean1 * 1e-3) / 1e9
+    line["mixed_step"]["one_launch"] = {
+        "value": round(world * gbs1, 1), "unit": "GB/s", "ms_per_step": round(mean1, 5),
+        "call": "paged_mixed_step_one_launch (one kernel: write, tensor-core items, split and "
+                "combine as CTAs of one grid)",
+        "roofline": hbm_roofline("step_one_kernel", nbytes, mean1, med1, hbm_peak, peak_src,
+                                 "mixed_step_one_launch")}
+    line["gpu_launches"] += args.steps
     line["error_flags"] |= pkv.paged_error_flags()
     del kc, vc, ws
     torch.cuda.empty_cache()

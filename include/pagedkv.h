@@ -332,6 +332,23 @@ int paged_mixed_step(const pkv_mixed_step* step, void* k_cache, void* v_cache, v
                      size_t workspace_bytes, const pkv_geom* geom, cudaStream_t stream);
 
 /*
+ * paged_mixed_step_one_launch -- paged_mixed_step's result from ONE kernel
+ * launch (plus a 16-byte memset of its counters): the prefill rows' write, the
+ * shared-prefix and causal-prefill work items on the tensor cores, the decode
+ * split and the combine with the append run as CTAs of one grid, in that
+ * order of block index; a CTA that needs earlier results (a prefill item the
+ * write, a combine CTA the prefix items and the split) waits until their
+ * counters are complete (time-limited: PKV_FLAG_TIMEOUT).  Same arguments,
+ * workspace and errors as paged_mixed_step.  It takes full steps (prefill
+ * rows, prefill requests and grouped decode sequences) in bf16 with 2 query
+ * heads per KV head and at most 8 KV heads; any other step is done by
+ * paged_mixed_step.
+ */
+int paged_mixed_step_one_launch(const pkv_mixed_step* step, void* k_cache, void* v_cache,
+                                void* workspace, size_t workspace_bytes, const pkv_geom* geom,
+                                cudaStream_t stream);
+
+/*
  * paged_decode_noalloc -- paged_decode for callers that cannot allocate device
  * memory.  The pages have no counterpart: this is a deployment variant of
  * paged_decode that takes no workspace.

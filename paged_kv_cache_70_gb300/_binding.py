@@ -53,6 +53,7 @@ EXPORTED = (
     "paged_decode_append",
     "paged_mixed_step_workspace_size",
     "paged_mixed_step",
+    "paged_mixed_step_one_launch",
 )
 PKV_ERR_NO_SPACE = -5
 
@@ -162,6 +163,9 @@ def load_library(path: str | None = None):
         lib.paged_mixed_step_workspace_size.restype = sz
         lib.paged_mixed_step.argtypes = [ctypes.POINTER(MixedStep), vp, vp, vp, sz, gp, vp]
         lib.paged_mixed_step.restype = ctypes.c_int
+        lib.paged_mixed_step_one_launch.argtypes = [ctypes.POINTER(MixedStep), vp, vp, vp, sz, gp,
+                                                    vp]
+        lib.paged_mixed_step_one_launch.restype = ctypes.c_int
         lib.paged_copy_blocks.argtypes = [vp, vp, vp, vp, i32, gp, vp]
         lib.paged_copy_blocks.restype = ctypes.c_int
         lib.paged_status_string.argtypes = [ctypes.c_int]
@@ -575,8 +579,9 @@ def paged_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src: torch.T
 
 def paged_mixed_step(k_cache: torch.Tensor, v_cache: torch.Tensor, scale: float,
                      prefill: dict | None = None, decode: dict | None = None,
-                     workspace: torch.Tensor | None = None):
-    """One continuous-batching step (include/pagedkv.h, paged_mixed_step).
+                     workspace: torch.Tensor | None = None, one_launch: bool = False):
+    """One continuous-batching step (include/pagedkv.h, paged_mixed_step;
+    paged_mixed_step_one_launch with one_launch=True).
 
     prefill: k_new, v_new [N, Hkv, d] and slots [N] (the requests' new rows,
     negative slots skipped), q [total_q, Hq, d], cu_q, cu_k, max_q, max_k,
@@ -636,8 +641,9 @@ def paged_mixed_step(k_cache: torch.Tensor, v_cache: torch.Tensor, scale: float,
         need = int(lib.paged_mixed_step_workspace_size(st.decode_batch, ctypes.byref(g)))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=k_cache.device)
+    fn = lib.paged_mixed_step_one_launch if one_launch else lib.paged_mixed_step
     with torch.cuda.device(k_cache.device):
-        rc = lib.paged_mixed_step(ctypes.byref(st), _ptr(k_cache), _ptr(v_cache), _ptr(workspace),
-                                  workspace.numel(), ctypes.byref(g), _stream(k_cache))
-    _check("paged_mixed_step", rc)
+        rc = fn(ctypes.byref(st), _ptr(k_cache), _ptr(v_cache), _ptr(workspace),
+                workspace.numel(), ctypes.byref(g), _stream(k_cache))
+    _check("paged_mixed_step_one_launch" if one_launch else "paged_mixed_step", rc)
     return pout, dout

@@ -2,8 +2,10 @@
 
 ``python -m paged_kv_cache_70_gb300.build`` (or ``build()``) compiles every
 ``csrc/*.cu`` translation unit in parallel and links them into
-``_build/libpagedkv.so`` next to this file.  The CUDA runtime is linked
-statically, so the library needs only the NVIDIA driver at run time.
+``_build/libpagedkv.so`` next to this file.  ``decode.cu``, ``write.cu`` and
+``prefill.cu`` are not units of their own: ``step.cu`` includes them, so that
+its one-launch step kernel can run their CTA functions.  The CUDA runtime is
+linked statically, so the library needs only the NVIDIA driver at run time.
 """
 from __future__ import annotations
 
@@ -30,8 +32,13 @@ def _nvcc() -> str:
     return cand
 
 
+# sources compiled inside step.cu
+INCLUDED = ("decode.cu", "write.cu", "prefill.cu")
+
+
 def sources() -> list[str]:
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)
+                  if f.endswith(".cu") and f not in INCLUDED)
 
 
 def _stale(target: str, deps: list[str]) -> bool:
@@ -44,7 +51,8 @@ def _stale(target: str, deps: list[str]) -> bool:
 def build(force: bool = False, verbose: bool = False, extra: tuple[str, ...] = ()) -> str:
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
-    headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
+    headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC)
+               if f.endswith((".cuh", ".h")) or f in INCLUDED]
     headers.append(os.path.join(INCLUDE, "pagedkv.h"))
     objs, jobs = [], []
     for src in sources():

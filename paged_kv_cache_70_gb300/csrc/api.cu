@@ -437,10 +437,13 @@ int paged_decode_shared_prefix(const void* q, const void* k_cache, const void* v
                                           geom->dtype, dev.err, stream, &sp, nullptr, &ch));
 }
 
+// The mixed step's workspace: the grouped decode's, then 256 bytes for the
+// one-launch form's counters.
 size_t paged_mixed_step_workspace_size(int32_t decode_batch, const pkv_geom* geom) {
     if (check_geom(geom) != PKV_OK || decode_batch < 0) return 0;
     if (decode_batch == 0) return 256;
-    return paged_decode_shared_prefix_workspace_size(decode_batch, geom);
+    const size_t g = paged_decode_shared_prefix_workspace_size(decode_batch, geom);
+    return g ? g + 256 : 0;
 }
 
 int paged_mixed_step(const pkv_mixed_step* s, void* k_cache, void* v_cache, void* workspace,
@@ -536,6 +539,83 @@ int paged_mixed_step(const pkv_mixed_step* s, void* k_cache, void* v_cache, void
         s->decode_seqlens, s->decode_batch, s->scale, s->decode_out, workspace, geom->num_heads,
         geom->num_kv_heads, geom->head_dim, geom->block_size, geom->num_blocks, geom->dtype,
         dev.err, stream, grp ? &sp : nullptr, &ap, &ch));
+}
+
+int paged_mixed_step_one_launch(const pkv_mixed_step* s, void* k_cache, void* v_cache,
+                                void* workspace, size_t workspace_bytes, const pkv_geom* geom,
+                                cudaStream_t stream) {
+    // the one-launch form takes full steps of its shape; anything else (or an
+    // invalid step, which paged_mixed_step reports) goes the chained way
+    const int st_g = check_geom(geom);
+    if (st_g != PKV_OK || !s || !k_cache || !v_cache) return paged_mixed_step(s, k_cache, v_cache,
+                                                                              workspace,
+                                                                              workspace_bytes,
+                                                                              geom, stream);
+    const bool full = s->prefill_batch > 0 && s->max_seqlen_q > 0 && s->decode_batch > 0 &&
+                      s->n_groups > 0 && s->prefill_new_tokens > 0;
+    if (!full || geom->dtype != PKV_BF16 || geom->num_heads != 2 * geom->num_kv_heads)
+        return paged_mixed_step(s, k_cache, v_cache, workspace, workspace_bytes, geom, stream);
+    if (!s->prefill_k_new || !s->prefill_v_new || !s->prefill_slots || !s->prefill_q ||
+        !s->cu_seqlens_q || !s->cu_seqlens_k || !s->prefill_table || !s->prefill_out ||
+        !s->decode_q || !s->decode_k_new || !s->decode_v_new || !s->decode_table ||
+        !s->decode_seqlens || !s->decode_out || !s->group_cu || !s->group_prefix_len ||
+        s->max_group_size <= 0)
+        return paged_mixed_step(s, k_cache, v_cache, workspace, workspace_bytes, geom, stream);
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(s->prefill_q, 16) ||
+        !aligned(s->prefill_out, 16) || !aligned(s->decode_q, 16) ||
+        !aligned(s->decode_out, 16) || !aligned(s->decode_k_new, 16) ||
+        !aligned(s->decode_v_new, 16) || !aligned(s->prefill_k_new, 16) ||
+        !aligned(s->prefill_v_new, 16))
+        return PKV_ERR_INVALID;
+    DeviceInfo dev;
+    if (pkv::current_device_info(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    pkv::DecodePlan plan;
+    if (!pkv::plan_decode(dev, s->decode_batch, geom->num_heads, geom->num_kv_heads,
+                          geom->head_dim, geom->block_size, elt_size(geom->dtype), &plan))
+        return PKV_ERR_UNSUPPORTED;
+    const size_t grouped = grouped_ws_bytes(plan, s->decode_batch, geom);
+    if (!workspace || workspace_bytes < grouped + 256 || !aligned(workspace, 256))
+        return PKV_ERR_WORKSPACE;
+    unsigned char* x_out = static_cast<unsigned char*>(workspace) + plan.ws_bytes;
+    float* x_lse = reinterpret_cast<float*>(
+        x_out + align256((size_t)kMaxPrefixChunks * s->decode_batch * geom->num_heads *
+                         geom->head_dim * 2));
+    pkv::StepOneLaunch st{};
+    st.prefix = prefix_pass(dev, s->decode_q, k_cache, v_cache, s->decode_table,
+                            s->decode_max_blocks, s->decode_batch, s->group_cu,
+                            s->group_prefix_len, s->n_groups, s->max_group_size, s->scale,
+                            x_out, x_lse, geom, false);
+    st.plan = plan;
+    st.pf_k_new = s->prefill_k_new;
+    st.pf_v_new = s->prefill_v_new;
+    st.pf_slots = s->prefill_slots;
+    st.pf_new_tokens = s->prefill_new_tokens;
+    st.pf_q = s->prefill_q;
+    st.cu_q = s->cu_seqlens_q;
+    st.cu_k = s->cu_seqlens_k;
+    st.pf_batch = s->prefill_batch;
+    st.max_seqlen_q = s->max_seqlen_q;
+    st.pf_max_blocks = s->prefill_max_blocks;
+    st.pf_table = s->prefill_table;
+    st.pf_out = s->prefill_out;
+    st.dec_k_new = s->decode_k_new;
+    st.dec_v_new = s->decode_v_new;
+    st.dec_seqlens = s->decode_seqlens;
+    st.dec_out = s->decode_out;
+    st.k_cache = k_cache;
+    st.v_cache = v_cache;
+    st.workspace = workspace;
+    st.counters = reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(workspace) + grouped);
+    st.scale = s->scale;
+    st.hq = geom->num_heads;
+    st.hkv = geom->num_kv_heads;
+    st.block_size = geom->block_size;
+    st.dtype = geom->dtype;
+    st.num_blocks = geom->num_blocks;
+    const cudaError_t e = pkv::launch_step_one(dev, st, stream);
+    if (e == cudaErrorNotSupported)  // nothing was launched: the chained form
+        return paged_mixed_step(s, k_cache, v_cache, workspace, workspace_bytes, geom, stream);
+    return cuda_status(e);
 }
 
 int paged_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst,

@@ -114,6 +114,9 @@ struct DecodeArgs {
     int32_t n_groups;
     int32_t wait_prior;  // this grid completes only after the previous kernel has
     int32_t wait_inputs;  // wait for the previous kernel before reading any input
+    // one-launch step (else null): each CTA adds 1 here once its partial
+    // states are stored (the combine CTAs of the same grid wait for them)
+    unsigned int* done;
 };
 
 // The split's shares.  Tile t of sequence b sits at position
@@ -266,8 +269,12 @@ __device__ __forceinline__ int seq_of_tile(const int32_t* tstart, int batch, int
     return lo - 1;
 }
 
+// One CTA of the split: share bx of gx along the tile list, KV-head group by.
+// Run by decode_split_kernel, and by the one-launch step kernel with
+// a.done set (there the CTA has 12 warps; warps past the producer leave).
 template <int D, bool BF16, int G>
-__global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(const DecodeArgs a) {
+__device__ __forceinline__ void split_cta(const DecodeArgs& a, const int bx, const int by,
+                                          const int gx) {
     constexpr int ELT = BF16 ? 2 : 4;
     constexpr int TG = D / 16;    // lanes per key row
     constexpr int GPW = 32 / TG;  // key rows processed side by side by a warp
@@ -315,9 +322,9 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
     // Holding the grid open (see DecodeArgs::wait_prior): block (0, 0) does
     // not exit before the kernel launched before this one has completed.
     // Its producer waits after issuing its copies; with no work it waits here.
-    const bool holder = a.wait_prior && blockIdx.x == 0 && blockIdx.y == 0;
+    const bool holder = a.wait_prior && bx == 0 && by == 0;
     const int32_t total = tstart[a.batch];
-    if (blockIdx.x == 0 && blockIdx.y == 0) {
+    if (bx == 0 && by == 0) {
         for (int b = threadIdx.x; b <= a.batch; b += blockDim.x) a.tstart_out[b] = tstart[b];
         for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
             const int32_t L = a.seqlens[b];
@@ -325,20 +332,24 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
         }
     }
     // this CTA's share [t0, t1) of the tile list
-    const int32_t chunk = share_cost(total, a.batch, gridDim.x);
-    const int32_t t0 = first_tile_at(tstart, a.batch, (int64_t)blockIdx.x * chunk);
-    const int32_t t1 = first_tile_at(tstart, a.batch, (int64_t)(blockIdx.x + 1) * chunk);
+    const int32_t chunk = share_cost(total, a.batch, gx);
+    const int32_t t0 = first_tile_at(tstart, a.batch, (int64_t)bx * chunk);
+    const int32_t t1 = first_tile_at(tstart, a.batch, (int64_t)(bx + 1) * chunk);
     if (t0 >= t1) {
         if (holder && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (a.done && threadIdx.x == 0) {  // nothing to store
+            __threadfence();
+            atomicAdd(a.done, 1u);
+        }
         return;
     }
-    const int head0 = blockIdx.y * HC;  // first KV head of this CTA
+    const int head0 = by * HC;  // first KV head of this CTA
 
     if (warp >= kConsumerWarps) {
         if constexpr (G >= 4) {
             asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs4));
-            if (warp > kConsumerWarps) return;  // only completed the producer's warpgroup
         }
+        if (warp > kConsumerWarps) return;  // only complete the warpgroup or the CTA
         // ------------------------------ producer ------------------------------
         // The 32 lanes prepare 32 tiles at a time (sequence, first key, rows,
         // block-table entry: the entries of a batch are read together); lane 0
@@ -354,7 +365,7 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
         bool stop = false;
         {
             // the CTA's piece: its share [t0, t1) of the tile list
-            const int32_t piece = blockIdx.x, pt0 = t0, pt1 = t1;
+            const int32_t piece = bx, pt0 = t0, pt1 = t1;
             for (int32_t tb = pt0; tb < pt1 && !stop; tb += 32) {
                 // lane i: tile tb + i's block-table entry and (first key's slot
                 // in the block) * 64 + rows (rows <= 32); the batch's table
@@ -691,7 +702,20 @@ __global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(co
         }
         fresh = false;  // the next tile starts a new piece
     }
+    if (a.done) {  // every consumer warp has stored its partial states
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atomicAdd(a.done, 1u);
+        }
+    }
 }
+
+template <int D, bool BF16, int G>
+__global__ void __launch_bounds__(decode_threads<G>(), 1) decode_split_kernel(const DecodeArgs a) {
+    split_cta<D, BF16, G>(a, blockIdx.x, blockIdx.y, gridDim.x);
+}
+
 
 // Inputs of the combine kernel.
 struct CombineArgs {
@@ -779,12 +803,14 @@ __device__ __forceinline__ void merge_state(float& M, float& L, float* acc, floa
 // append mode adds the new key (m = its score, l = 1, o = its V row) and the
 // first warp of each KV head writes the new K/V row into the cache (the split
 // kernel, which read only the keys before it, has completed).
+// The combine of (sequence, head) pair w by one warp.  With pdl_wait the warp
+// waits for the split grid (griddepcontrol.wait) after its own loads; without
+// it the caller has already waited for the split's states.
 template <int D, bool BF16, int U>
-__global__ void __launch_bounds__(kCombineWarps * 32, U > 4 ? 4 : 8)
-decode_combine_kernel(const CombineArgs c) {
+__device__ __forceinline__ void combine_warp(const CombineArgs& c, const int64_t w,
+                                             const bool pdl_wait) {
     constexpr int DPL = D / 32;
     const int lane = threadIdx.x & 31;
-    const int64_t w = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
     const int hq = c.hq, batch = c.batch;
     const bool live = w < (int64_t)batch * hq;
     const int b = live ? (int)(w / hq) : 0, h = live ? (int)(w % hq) : 0;
@@ -826,7 +852,7 @@ decode_combine_kernel(const CombineArgs c) {
         merge_state<DPL>(M, L, acc, dot * c.qscale, 1.f, vv);
     }
     // wait until the split kernel's partials are complete and visible
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (pdl_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!live) return;
     const int32_t total = c.tstart ? c.tstart[batch] : 0;
     const int32_t tb0 = c.tstart ? c.tstart[b] : 0, tb1 = c.tstart ? c.tstart[b + 1] : 0;
@@ -898,6 +924,12 @@ decode_combine_kernel(const CombineArgs c) {
                                                    src * ELT + e);
         }
     }
+}
+
+template <int D, bool BF16, int U>
+__global__ void __launch_bounds__(kCombineWarps * 32, U > 4 ? 4 : 8)
+decode_combine_kernel(const CombineArgs c) {
+    combine_warp<D, BF16, U>(c, (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5), true);
 }
 
 // ---------------------------------------------------------------------------
@@ -989,15 +1021,15 @@ static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a,
     return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, BF16, 4>, c);
 }
 
-cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_cache,
-                          const void* v_cache, const int32_t* block_table, int32_t max_blocks,
-                          const int32_t* cache_seqlens, int32_t batch, float scale, void* out,
-                          void* workspace, int hq, int hkv, int d, int block_size,
-                          int64_t num_blocks, int dtype, unsigned int* err, cudaStream_t stream,
-                          const SharedPrefix* sp, const DecodeAppend* ap,
-                          const DecodeChain* chain) {
-    if (batch == 0) return cudaSuccess;
-    DecodeArgs a;
+// The split's and the combine's arguments (workspace carved as the plan sized it).
+static void fill_decode_args(const DecodePlan& plan, const void* q, const void* k_cache,
+                             const void* v_cache, const int32_t* block_table, int32_t max_blocks,
+                             const int32_t* cache_seqlens, int32_t batch, float scale, void* out,
+                             void* workspace, int hq, int hkv, int block_size, int64_t num_blocks,
+                             unsigned int* err, const SharedPrefix* sp, const DecodeAppend* ap,
+                             const DecodeChain* chain, DecodeArgs* pa, CombineArgs* pc) {
+    DecodeArgs& a = *pa;
+    a = DecodeArgs{};
     a.wait_prior = (chain && chain->pdl_split) ? 1 : 0;
     a.wait_inputs = a.wait_prior ? 0 : 1;
     a.group_cu = sp ? sp->group_cu : nullptr;
@@ -1029,9 +1061,8 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
     a.block_size = block_size;
     a.rows = plan.rows_per_tile;
     a.stages = plan.stages;
-    const int G = hq / hkv / plan.gsplit;  // query heads per consumer warp
-    const bool bf = dtype == PKV_BF16;
-    CombineArgs c = {};
+    CombineArgs& c = *pc;
+    c = CombineArgs{};
     c.part_o = a.part_o;
     c.part_ml = a.part_ml;
     const bool split = !(chain && chain->no_split);
@@ -1060,6 +1091,24 @@ cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_c
     c.hkv = hkv;
     c.qscale = a.qscale;
     c.err = err;
+}
+
+cudaError_t launch_decode(const DecodePlan& plan, const void* q, const void* k_cache,
+                          const void* v_cache, const int32_t* block_table, int32_t max_blocks,
+                          const int32_t* cache_seqlens, int32_t batch, float scale, void* out,
+                          void* workspace, int hq, int hkv, int d, int block_size,
+                          int64_t num_blocks, int dtype, unsigned int* err, cudaStream_t stream,
+                          const SharedPrefix* sp, const DecodeAppend* ap,
+                          const DecodeChain* chain) {
+    if (batch == 0) return cudaSuccess;
+    DecodeArgs a;
+    CombineArgs c;
+    fill_decode_args(plan, q, k_cache, v_cache, block_table, max_blocks, cache_seqlens, batch,
+                     scale, out, workspace, hq, hkv, block_size, num_blocks, err, sp, ap, chain,
+                     &a, &c);
+    const bool split = !(chain && chain->no_split);
+    const int G = hq / hkv / plan.gsplit;  // query heads per consumer warp
+    const bool bf = dtype == PKV_BF16;
 #define PKV_DECODE_CASE(DD, BB, GG) \
     if (d == DD && bf == BB && G == GG) \
         return launch_decode_t<DD, BB, GG>(plan, a, c, split, stream);

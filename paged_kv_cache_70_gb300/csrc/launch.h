@@ -168,6 +168,38 @@ struct PrefixLaunch {
 
 cudaError_t launch_prefix(const DeviceInfo& dev, const PrefixLaunch& p, cudaStream_t stream);
 
+// The continuous-batching step in one launch (step.cu): the prefill rows'
+// write, the prefix items and the causal prefill items, the decode split and
+// the combine with the append, as CTAs of one grid ordered by block index and
+// tied by counters.  bf16, 2 query heads per KV head, one KV-head group per
+// split CTA; cudaErrorNotSupported otherwise (before any launch).
+struct StepOneLaunch {
+    PrefixLaunch prefix;        // the decode groups' shared-prefix pass (q, table, groups)
+    DecodePlan plan;            // the decode split's plan
+    const void* pf_k_new;       // [pf_new_tokens, Hkv, d] bf16
+    const void* pf_v_new;
+    const int32_t* pf_slots;    // [pf_new_tokens]
+    int64_t pf_new_tokens;
+    const void* pf_q;           // [total_q, Hq, d]
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    int32_t pf_batch, max_seqlen_q, pf_max_blocks;
+    const int32_t* pf_table;
+    void* pf_out;
+    const void* dec_k_new;      // [decode batch, Hkv, d]
+    const void* dec_v_new;
+    const int32_t* dec_seqlens;
+    void* dec_out;
+    void* k_cache;
+    void* v_cache;
+    void* workspace;            // the decode split's workspace (plan.ws_bytes, then the prefix partials)
+    unsigned int* counters;     // 4 words of device memory
+    float scale;
+    int hq, hkv, block_size, dtype;
+    int64_t num_blocks;
+};
+cudaError_t launch_step_one(const DeviceInfo& dev, const StepOneLaunch& st, cudaStream_t stream);
+
 // A causal varlen prefill (the arguments of launch_prefill) and a
 // shared-prefix pass in ONE launch: the prefill's items wait for the kernel
 // before them, the prefix items start at once, and the SMs take either kind

@@ -63,8 +63,11 @@ def test_head_dim_64_without_groups():
     assert pkv.paged_error_flags() == 0
 
 
-@pytest.mark.parametrize("grouped", [True, False])
-def test_continuous_batching_step(grouped):
+@pytest.mark.parametrize("grouped,one_launch", [(True, False), (False, False), (True, True),
+                                                (False, True)])
+def test_continuous_batching_step(grouped, one_launch):
+    """The whole step against the oracle, chained and in one launch (without
+    groups the one-launch entry hands the step to the chained form)."""
     step = W.config(5)
     dec_rows, pf_rows, slots = split_step(step)
     kc, vc = to_dev(step.k_cache), to_dev(step.v_cache)
@@ -79,7 +82,8 @@ def test_continuous_batching_step(grouped):
                    slots=to_dev(slots[pf_rows]), q=to_dev(step.q_prefill), cu_q=to_dev(step.cu_q),
                    cu_k=to_dev(step.cu_k), max_q=step.max_seqlen_q, max_k=step.max_seqlen_k,
                    table=to_dev(step.prefill_table.copy()))
-    pout, dout = pkv.paged_mixed_step(kc, vc, step.scale, prefill=prefill, decode=decode)
+    pout, dout = pkv.paged_mixed_step(kc, vc, step.scale, prefill=prefill, decode=decode,
+                                      one_launch=one_launch)
     torch.cuda.synchronize()
     _, okc, ovc = oracle_write(step)
     assert np.array_equal(to_host(kc), okc) and np.array_equal(to_host(vc), ovc)
@@ -117,3 +121,30 @@ def test_parts_alone():
                             causal=True, block_table=step.prefill_table,
                             block_size=step.block_size)
     assert_close(widen(pout), want_p, "bf16", "prefill part")
+
+
+def test_one_launch_equals_chained():
+    """The one-launch step runs the same CTA functions on the same partition of
+    the work as the chained launches: its outputs and caches are bit-identical."""
+    step = W.config(5)
+    dec_rows, pf_rows, slots = split_step(step)
+    nd = step.n_decode
+    outs = []
+    for one in (False, True):
+        kc, vc = to_dev(step.k_cache), to_dev(step.v_cache)
+        decode = dict(q=to_dev(step.q_decode), k_new=to_dev(step.new_k[dec_rows]),
+                      v_new=to_dev(step.new_v[dec_rows]), table=to_dev(step.decode_table.copy()),
+                      seqlens=to_dev(step.cache_seqlens - 1),
+                      group_cu=to_dev(np.arange(0, nd + 1, nd // 8, dtype=np.int32)),
+                      group_prefix_len=to_dev(np.full(8, 2048, np.int32)), max_group_size=nd // 8)
+        prefill = dict(k_new=to_dev(step.new_k[pf_rows]), v_new=to_dev(step.new_v[pf_rows]),
+                       slots=to_dev(slots[pf_rows]), q=to_dev(step.q_prefill),
+                       cu_q=to_dev(step.cu_q), cu_k=to_dev(step.cu_k), max_q=step.max_seqlen_q,
+                       max_k=step.max_seqlen_k, table=to_dev(step.prefill_table.copy()))
+        pout, dout = pkv.paged_mixed_step(kc, vc, step.scale, prefill=prefill, decode=decode,
+                                          one_launch=one)
+        torch.cuda.synchronize()
+        outs.append([to_host(t) for t in (pout, dout, kc, vc)])
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+    assert pkv.paged_error_flags() == 0

@@ -6,8 +6,9 @@ word of that build must carry PKV_FLAG_TIMEOUT.  With two KV heads the eight
 consumer warps share heads and merge through time-limited barriers, which must
 not hold any warp after the timeout.
 
-The build compiles decode.cu with the two test defines into its own library
-(_build/test_wait_timeout/); the default library is not changed."""
+The build compiles step.cu (the unit that holds the decode kernels) with the
+two test defines into its own library (_build/test_wait_timeout/); the default
+library is not changed."""
 import ctypes
 
 import numpy as np
@@ -26,7 +27,7 @@ DEFINES = ("-DPKV_WAIT_LIMIT_NS=1000000ull", "-DPKV_TEST_SPLIT_PRODUCER_IDLE")
 
 @pytest.fixture(scope="module")
 def timeout_lib():
-    return pkv.load_library(B.build_variant("test_wait_timeout", DEFINES, ("decode.cu",)))
+    return pkv.load_library(B.build_variant("test_wait_timeout", DEFINES, ("step.cu",)))
 
 
 def _flags(lib, clear=1):
