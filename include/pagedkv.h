@@ -340,9 +340,11 @@ int paged_mixed_step(const pkv_mixed_step* step, void* k_cache, void* v_cache, v
  * write, a combine CTA the prefix items and the split) waits until their
  * counters are complete (time-limited: PKV_FLAG_TIMEOUT).  Same arguments,
  * workspace and errors as paged_mixed_step.  It takes full steps (prefill
- * rows, prefill requests and grouped decode sequences) in bf16 with 2 query
- * heads per KV head and at most 8 KV heads; any other step is done by
- * paged_mixed_step.
+ * rows, prefill requests and grouped decode sequences) in bf16, head_dim 128,
+ * with 2 query heads per KV head and at most 8 KV heads; any other step is done
+ * by paged_mixed_step.  paged_mixed_step is faster on GB300 (each phase keeps
+ * its own CTA shape there); this form is for callers that need a single
+ * kernel launch.
  */
 int paged_mixed_step_one_launch(const pkv_mixed_step* step, void* k_cache, void* v_cache,
                                 void* workspace, size_t workspace_bytes, const pkv_geom* geom,

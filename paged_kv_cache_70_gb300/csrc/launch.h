@@ -171,8 +171,9 @@ cudaError_t launch_prefix(const DeviceInfo& dev, const PrefixLaunch& p, cudaStre
 // The continuous-batching step in one launch (step.cu): the prefill rows'
 // write, the prefix items and the causal prefill items, the decode split and
 // the combine with the append, as CTAs of one grid ordered by block index and
-// tied by counters.  bf16, 2 query heads per KV head, one KV-head group per
-// split CTA; cudaErrorNotSupported otherwise (before any launch).
+// tied by counters.  bf16, head_dim 128, 2 query heads per KV head, one
+// KV-head group per split CTA; cudaErrorNotSupported otherwise (before any
+// launch).
 struct StepOneLaunch {
     PrefixLaunch prefix;        // the decode groups' shared-prefix pass (q, table, groups)
     DecodePlan plan;            // the decode split's plan

@@ -152,7 +152,7 @@ cudaError_t launch_step_one(const DeviceInfo& dev, const StepOneLaunch& st,
                             cudaStream_t stream) {
     const PrefixLaunch& pp = st.prefix;
     const int d = pp.hd;
-    if (st.dtype != PKV_BF16 || (d != 128 && d != 64)) return cudaErrorNotSupported;
+    if (st.dtype != PKV_BF16 || d != 128) return cudaErrorNotSupported;
     if (st.hq / st.hkv != 2 || st.plan.gsplit != 1 || st.plan.head_groups != 1)
         return cudaErrorNotSupported;
     if (st.pf_new_tokens < 0 || ((uintptr_t)st.pf_k_new & 15) || ((uintptr_t)st.pf_v_new & 15))
@@ -204,10 +204,9 @@ cudaError_t launch_step_one(const DeviceInfo& dev, const StepOneLaunch& st,
     const int64_t blocks = (int64_t)s.n_tc + s.n_split;
     if (blocks > 0x7fffffffLL) return cudaErrorNotSupported;
     const size_t smem =
-        std::max({d == 128 ? Shape<128>::kSmemBytes : Shape<64>::kSmemBytes,
-                  d == 128 ? PShape<128>::kSmemBytes : PShape<64>::kSmemBytes, st.plan.smem_bytes});
+        std::max({Shape<128>::kSmemBytes, PShape<128>::kSmemBytes, st.plan.smem_bytes});
     if (dev.max_smem_optin < smem) return cudaErrorNotSupported;
-    auto kern = d == 128 ? step_one_kernel<128> : step_one_kernel<64>;
+    auto kern = step_one_kernel<128>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(st.counters, 0, 4 * sizeof(unsigned int), stream);
