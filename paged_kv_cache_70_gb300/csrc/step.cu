@@ -18,20 +18,21 @@
 //      by the boxed rule, the new K/V row of every decode sequence written.
 //
 // GB300 design.  One grid of 384-thread CTAs in this block order: [prefix
-// items][prefill items][split CTAs].  The SMs take blocks in that order as they
+// items][prefill items][split CTAs][combine CTAs].  The SMs take blocks in that order as they
 // free up, as with the chained launches.  In-grid dependencies replace the
 // launch boundaries: a CTA that feeds later ones adds 1 to a counter once its
 // results are stored, and a CTA that needs them waits, time-limited, until the
 // count is complete.  The first wave (the first n_write = min(SMs, items)
 // tensor-core items, all dispatched at once) first writes the prefill rows, a
 // warp per row, and counts its shares; the prefill items wait for all of them.
-// The split CTAs then do the combine: once
-// every prefix item and split CTA has counted, their 12 warps take the
-// (sequence, head) pairs in turn.  Every CTA of one launch has the largest
-// item's resources (one CTA per SM), so separate combine CTAs would run in
-// waves of 152; the split CTAs are all resident by then.  A CTA waits only for
-// blocks placed before it or resident beside it.  The counters live in the
-// workspace and are zeroed on the stream before the launch.
+// The combine CTAs (at most one per split CTA)
+// wait until every prefix item and split CTA has counted, and their 12 warps
+// then take the (sequence, head) pairs in turn.  Every CTA of one launch has
+// the largest item's resources (one CTA per SM), so the combine is cut into
+// as many CTAs as there are split CTAs, not one per 12 pairs, which would run
+// in waves.  A CTA waits only for blocks placed before it, which in-order
+// dispatch has made resident or finished.  The counters live in the workspace
+// and are zeroed on the stream before the launch.
 #include "decode.cu"
 #include "write.cu"
 #include "prefill.cu"
@@ -52,6 +53,7 @@ struct StepOne {
     int32_t n_tc;       // tensor-core items: g.n_prefix prefix items, then prefill items
     int32_t n_write;    // the first n_write items write the prefill rows
     int32_t n_split;    // split CTAs
+    int32_t n_combine;  // combine CTAs
     unsigned int* counters;  // [0] row shares written, [1] prefix items, [2] split CTAs done
     unsigned int* err;
 };
@@ -133,8 +135,11 @@ step_one_kernel(const __grid_constant__ CUtensorMap fq, const __grid_constant__ 
         return;
     }
     item -= s.n_tc;
-    split_cta<HD, true, 2>(da, item, 0, s.n_split);  // counts itself in da.done
-    __syncthreads();  // every warp is back (split_cta uses no CTA barrier after its plan)
+    if (item < s.n_split) {
+        split_cta<HD, true, 2>(da, item, 0, s.n_split);  // counts itself in da.done
+        return;
+    }
+    item -= s.n_split;
     if (threadIdx.x == 0) {
         wait_count(s.counters + 1, (unsigned)g.n_prefix, s.err);
         wait_count(s.counters + 2, (unsigned)s.n_split, s.err);
@@ -142,7 +147,7 @@ step_one_kernel(const __grid_constant__ CUtensorMap fq, const __grid_constant__ 
     __syncthreads();
     const int64_t pairs = (int64_t)ca.batch * ca.hq;
     for (int64_t w = (int64_t)item * kStepWarps + warp; w < pairs;
-         w += (int64_t)s.n_split * kStepWarps)
+         w += (int64_t)s.n_combine * kStepWarps)
         combine_warp<HD, true, 4>(ca, w, false);
 }
 
@@ -199,9 +204,10 @@ cudaError_t launch_step_one(const DeviceInfo& dev, const StepOneLaunch& st,
     s.n_split = st.plan.ctas;
     s.counters = st.counters;
     s.err = dev.err;
-    (void)warps;
     s.n_write = (int32_t)std::min<int64_t>(dev.num_sms, nf + np);
-    const int64_t blocks = (int64_t)s.n_tc + s.n_split;
+    s.n_combine = (int32_t)std::max<int64_t>(
+        1, std::min<int64_t>(s.n_split, (warps + kStepWarps - 1) / kStepWarps));
+    const int64_t blocks = (int64_t)s.n_tc + s.n_split + s.n_combine;
     if (blocks > 0x7fffffffLL) return cudaErrorNotSupported;
     const size_t smem =
         std::max({Shape<128>::kSmemBytes, PShape<128>::kSmemBytes, st.plan.smem_bytes});
