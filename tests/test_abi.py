@@ -101,3 +101,17 @@ def test_host_side_checks_of_the_step_calls(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not found"):
         pkv.load_library(str(tmp_path / "missing.so"))
+
+
+def test_every_source_is_compiled_once():
+    """Every csrc/*.cu is either a translation unit of its own or included by
+    step.cu (which compiles decode.cu, write.cu and prefill.cu together), never
+    both: a source compiled twice would define its kernels twice."""
+    csrc = build.CSRC
+    step = open(os.path.join(csrc, "step.cu")).read()
+    included = set(re.findall(r'^#include "(\w+\.cu)"', step, flags=re.M))
+    assert included == set(build.INCLUDED)
+    units = {os.path.basename(p) for p in build.sources()}
+    every = {f for f in os.listdir(csrc) if f.endswith(".cu")}
+    assert units | included == every
+    assert not units & included
