@@ -927,7 +927,7 @@ __device__ __forceinline__ void combine_warp(const CombineArgs& c, const int64_t
 }
 
 template <int D, bool BF16, int U>
-__global__ void __launch_bounds__(kCombineWarps * 32, U > 4 ? 4 : 8)
+__global__ void __launch_bounds__(kCombineWarps * 32, U > 8 ? 4 : (U > 4 ? 7 : 8))
 decode_combine_kernel(const CombineArgs c) {
     combine_warp<D, BF16, U>(c, (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5), true);
 }
@@ -1002,9 +1002,13 @@ static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a,
         if (e != cudaSuccess) return e;
     }
     // combine: programmatic dependent of the split kernel, one warp per
-    // (sequence, head); 16 pieces in flight per round while every warp of
-    // the batch still fits on the GPU at once (4 warps a CTA, 4 CTAs an SM),
-    // else 4
+    // (sequence, head).  Pieces in flight per round:
+    //  - 8 when a sequence has few pieces (about ctas / batch + 2 <= 8) and
+    //    every warp fits beside the split's CTAs while they run (72 registers:
+    //    two 4-warp CTAs per SM next to a split CTA), so all start early;
+    //  - 16 while every warp of the batch fits on the GPU at once (4 warps a
+    //    CTA, 4 CTAs an SM);
+    //  - else 4.
     cudaLaunchConfig_t cfg = {};
     const int64_t warps = (int64_t)a.batch * a.hq;
     cfg.gridDim = dim3((unsigned)((warps + kCombineWarps - 1) / kCombineWarps));
@@ -1016,6 +1020,9 @@ static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if ((int64_t)plan.ctas / (a.batch > 0 ? a.batch : 1) + 2 <= 8 &&
+        warps <= (int64_t)plan.ctas * plan.head_groups * 2 * kCombineWarps)
+        return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, BF16, 8>, c);
     if (warps <= (int64_t)plan.ctas * plan.head_groups * 4 * kCombineWarps)
         return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, BF16, 16>, c);
     return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, BF16, 4>, c);
