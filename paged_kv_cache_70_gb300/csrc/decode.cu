@@ -315,7 +315,10 @@ __device__ __forceinline__ void split_cta(const DecodeArgs& a, const int bx, con
     // Kernels launched after this one may be scheduled now (the combine waits
     // for this grid's results).  After the wait above, so that one that does
     // not wait would still start only after everything before this grid.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Block (0, 0) lets them start only once it has stored the tile starts
+    // (below), which the combine reads before its wait.
+    const bool first_cta = bx == 0 && by == 0;
+    if (!first_cta) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     plan_tiles(a, tstart, sfirst, slen);
     __syncthreads();
 
@@ -324,12 +327,15 @@ __device__ __forceinline__ void split_cta(const DecodeArgs& a, const int bx, con
     // Its producer waits after issuing its copies; with no work it waits here.
     const bool holder = a.wait_prior && bx == 0 && by == 0;
     const int32_t total = tstart[a.batch];
-    if (bx == 0 && by == 0) {
+    if (first_cta) {
         for (int b = threadIdx.x; b <= a.batch; b += blockDim.x) a.tstart_out[b] = tstart[b];
         for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
             const int32_t L = a.seqlens[b];
             if (L < 0 || L > cap) flag_error(a.err, PKV_FLAG_BAD_LENGTH);
         }
+        __threadfence();
+        __syncthreads();
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
     // this CTA's share [t0, t1) of the tile list
     const int32_t chunk = share_cost(total, a.batch, gx);
@@ -795,8 +801,8 @@ __device__ __forceinline__ void merge_state(float& M, float& L, float* acc, floa
 // per (sequence, head); lane i owns dims [i*D/32, (i+1)*D/32).  Each state
 // joins a running (M, L, acc) by the boxed rule as it arrives, so the loads of
 // U split pieces (and, first, of the prefix chunks and the new key) are in
-// flight together: a sequence with up to U pieces costs two dependent memory
-// round trips after the split (the tile starts, then everything else).  U is
+// flight together: a sequence with up to U pieces costs one memory round trip
+// after the split (the tile starts are read before the wait).  U is
 // 16 for batches of few sequences (long contexts, many pieces each) and 4 for
 // large batches, whose warps must all fit on the GPU at once.  Shared-prefix
 // mode adds the prefix chunks, each as the state (m = lse, l = 1, o = out);
@@ -851,11 +857,18 @@ __device__ __forceinline__ void combine_warp(const CombineArgs& c, const int64_t
         for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
         merge_state<DPL>(M, L, acc, dot * c.qscale, 1.f, vv);
     }
+    // The split's tile starts: stored (and fenced) by its first block before
+    // any of its blocks let this kernel start, so they are read before the
+    // wait, from L2.
+    int32_t total = 0, tb0 = 0, tb1 = 0;
+    if (c.tstart && live) {
+        total = __ldcg(c.tstart + batch);
+        tb0 = __ldcg(c.tstart + b);
+        tb1 = __ldcg(c.tstart + b + 1);
+    }
     // wait until the split kernel's partials are complete and visible
     if (pdl_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!live) return;
-    const int32_t total = c.tstart ? c.tstart[batch] : 0;
-    const int32_t tb0 = c.tstart ? c.tstart[b] : 0, tb1 = c.tstart ? c.tstart[b + 1] : 0;
     const int32_t chunk = share_cost(total, batch, c.ctas);
     const int32_t ub = kSeqCost * (b + 1);  // u(t) - t for this sequence's tiles
     const int c0 = (tb0 + ub) / chunk, c1 = tb1 > tb0 ? (tb1 - 1 + ub) / chunk : c0 - 1;
