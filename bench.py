@@ -370,6 +370,13 @@ def time_parts(parts, steps: int, warmup: int, world: int, flush=None):
     torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)]
            for _ in range(steps)]
+    # Keep the GPU busy while the first timed pass is enqueued, so that no
+    # host launch latency lands inside a timed region (later passes are
+    # queued behind the previous ones).
+    if flush is not None:
+        flush(steps)
+    else:
+        torch.cuda._sleep(2_000_000)
     for i in range(steps):
         if flush is not None:
             flush(i)
@@ -380,7 +387,9 @@ def time_parts(parts, steps: int, warmup: int, world: int, flush=None):
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    total = max_over_ranks(float(np.mean([e[0].elapsed_time(e[-1]) for e in evs])), world)
+    steps_ms = [e[0].elapsed_time(e[-1]) for e in evs]
+    total = max_over_ranks(float(np.mean(steps_ms)), world)
+    print("steps (us):", " ".join(f"{1e3 * x:.1f}" for x in steps_ms), file=sys.stderr, flush=True)
     per = []
     for j in range(len(parts)):
         ms = [e[j].elapsed_time(e[j + 1]) for e in evs]
