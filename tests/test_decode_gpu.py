@@ -1,5 +1,6 @@
 """GPU parity of paged decode (block-table reads + online-softmax merge +
 split-KV combine) against the fp64 oracle, through the C ABI."""
+import ctypes
 import json
 import os
 
@@ -228,3 +229,30 @@ def test_split_points_vary_with_the_batch():
         outs.append(out[0])
     assert_close(outs[1], outs[0].astype(np.float64), "bf16", "split vs alone")
     assert_close(outs[2], outs[0].astype(np.float64), "bf16", "split vs alone")
+
+
+@pytest.mark.gpu
+def test_one_workspace_across_calls_with_different_tile_starts():
+    """Calls that reuse one workspace but cut their keys differently (other
+    tile starts, pieces and partial-state slots) each match the oracle: a
+    call reads only its own tile starts and partial states, never what the
+    call before left in the workspace."""
+    full = [3000, 17, 40000, 5, 12000, 800, 25000, 64]
+    step = W.make_step(name="reuse", dtype="bf16", hq=16, hkv=8, d=128, block_size=64,
+                       decode_lens=[L - 1 for L in full], seed=91)
+    dev = DevStep(step)
+    g = pkv.geom_of(dev.k_cache, step.hq)
+    need = int(pkv._binding.load_library().paged_decode_workspace_size(len(full), ctypes.byref(g)))
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    pkv.paged_error_flags()  # clear
+    variants = [full, [L // 3 + 1 for L in full], [0 if i % 2 else L for i, L in enumerate(full)],
+                full[:1] + [1] * (len(full) - 1), full]
+    for lens in variants:
+        lens = np.array(lens, np.int32)
+        dev.cache_seqlens = to_dev(lens)
+        out = widen(dev.decode(workspace=ws))
+        torch.cuda.synchronize()
+        want = oracle.decode(step.q_decode, step.k_cache, step.v_cache, step.decode_table, lens,
+                             step.scale)
+        assert_close(out, want, "bf16", f"lengths {lens.tolist()}")
+    assert pkv.paged_error_flags() == 0
