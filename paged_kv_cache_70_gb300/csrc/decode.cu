@@ -812,9 +812,14 @@ __device__ __forceinline__ void merge_state(float& M, float& L, float* acc, floa
 // The combine of (sequence, head) pair w by one warp.  With pdl_wait the warp
 // waits for the split grid (griddepcontrol.wait) after its own loads; without
 // it the caller has already waited for the split's states.
-template <int D, bool BF16, int U>
+// With H = 2, two warps share pair w: warp `half` merges its half of the
+// split's pieces, and half 1 hands its state to half 0 through xch (shared
+// memory, 32 * (D / 32 + 2) floats) at named barrier bar_id (64 threads);
+// half 0 alone takes the prefix chunks and the appended key, and stores.
+template <int D, bool BF16, int U, int H = 1>
 __device__ __forceinline__ void combine_warp(const CombineArgs& c, const int64_t w,
-                                             const bool pdl_wait) {
+                                             const bool pdl_wait, const int half = 0,
+                                             float* xch = nullptr, const int bar_id = 0) {
     constexpr int DPL = D / 32;
     const int lane = threadIdx.x & 31;
     const int hq = c.hq, batch = c.batch;
@@ -830,7 +835,7 @@ __device__ __forceinline__ void combine_warp(const CombineArgs& c, const int64_t
 #pragma unroll
     for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
     int64_t new_slot = -1;  // the appended row's slot, when this warp writes it
-    if (c.k_new && live) {  // the appended key: score q . k_new in log2 units
+    if (c.k_new && live && (H == 1 || half == 0)) {  // the appended key: q . k_new, log2 units
         const int64_t row = ((int64_t)b * c.hkv + kvh) * D + lane * DPL;
         float qv[DPL], kv[DPL], vv[DPL];
         load_row<BF16, DPL>(c.q, bh * D + lane * DPL, qv);
@@ -871,12 +876,17 @@ __device__ __forceinline__ void combine_warp(const CombineArgs& c, const int64_t
     if (!live) return;
     const int32_t chunk = share_cost(total, batch, c.ctas);
     const int32_t ub = kSeqCost * (b + 1);  // u(t) - t for this sequence's tiles
-    const int c0 = (tb0 + ub) / chunk, c1 = tb1 > tb0 ? (tb1 - 1 + ub) / chunk : c0 - 1;
+    int c0 = (tb0 + ub) / chunk, c1 = tb1 > tb0 ? (tb1 - 1 + ub) / chunk : c0 - 1;
+    if constexpr (H == 2) {  // this warp's half of the pieces
+        const int mid = c0 + (c1 - c0 + 2) / 2;
+        if (half == 0) c1 = mid - 1;
+        else c0 = mid;
+    }
     // the prefix chunks' states (rounds of UX), then the split's pieces c0 ..
     // c1 (rounds of U), every load of a round in flight
     constexpr int UX = U < 8 ? U : 8;
     const int64_t xstride = (int64_t)batch * hq;  // one prefix chunk's (sequence, head) count
-    for (int base = 0; base < c.x_chunks; base += UX) {
+    for (int base = 0; (H == 1 || half == 0) && base < c.x_chunks; base += UX) {
         float mx[UX];
         float xo[UX][DPL];
 #pragma unroll
@@ -905,6 +915,21 @@ __device__ __forceinline__ void combine_warp(const CombineArgs& c, const int64_t
         }
 #pragma unroll
         for (int i = 0; i < U; ++i) merge_state<DPL>(M, L, acc, ml[i].x, ml[i].y, o[i]);
+    }
+    if constexpr (H == 2) {  // half 1's state joins half 0's
+        float* x = xch + lane * (DPL + 2);
+        if (half == 1) {
+            x[0] = M;
+            x[1] = L;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) x[2 + e] = acc[e];
+        }
+        asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
+        if (half == 1) return;
+        float o1[DPL];
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o1[e] = x[2 + e];
+        merge_state<DPL>(M, L, acc, x[0], x[1], o1);
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     const int64_t oi = bh * D + lane * DPL;
@@ -943,6 +968,16 @@ template <int D, bool BF16, int U>
 __global__ void __launch_bounds__(kCombineWarps * 32, U > 8 ? 4 : (U > 4 ? 7 : 8))
 decode_combine_kernel(const CombineArgs c) {
     combine_warp<D, BF16, U>(c, (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5), true);
+}
+
+// Two warps per (sequence, head): for few sequences with more pieces each
+// than one round holds, so that every piece is loaded in one round.
+template <int D, bool BF16, int U>
+__global__ void __launch_bounds__(kCombineWarps * 32, 4) decode_combine2_kernel(const CombineArgs c) {
+    __shared__ float xch[kCombineWarps / 2][32 * (D / 32 + 2)];
+    const int warp = threadIdx.x >> 5, p = warp >> 1;
+    combine_warp<D, BF16, U, 2>(c, (int64_t)blockIdx.x * (kCombineWarps / 2) + p, true, warp & 1,
+                                xch[p], 1 + p);
 }
 
 // ---------------------------------------------------------------------------
@@ -1015,7 +1050,9 @@ static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a,
         if (e != cudaSuccess) return e;
     }
     // combine: programmatic dependent of the split kernel, one warp per
-    // (sequence, head).  Pieces in flight per round:
+    // (sequence, head), or two when a sequence has more pieces than a round
+    // of 16 and the warps fit beside the split's CTAs (one round each, up to
+    // 32 pieces).  Pieces in flight per round:
     //  - 8 when a sequence has few pieces (about ctas / batch + 2 <= 8) and
     //    every warp fits beside the split's CTAs while they run (72 registers:
     //    two 4-warp CTAs per SM next to a split CTA), so all start early;
@@ -1033,8 +1070,13 @@ static cudaError_t launch_decode_t(const DecodePlan& plan, const DecodeArgs& a,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((int64_t)plan.ctas / (a.batch > 0 ? a.batch : 1) + 2 <= 8 &&
-        warps <= (int64_t)plan.ctas * plan.head_groups * 2 * kCombineWarps)
+    const int64_t per_seq = (int64_t)plan.ctas / (a.batch > 0 ? a.batch : 1) + 2;
+    if (c.tstart && per_seq > 16 && per_seq <= 32 &&
+        2 * warps <= (int64_t)plan.ctas * plan.head_groups * kCombineWarps) {
+        cfg.gridDim = dim3((unsigned)((warps + kCombineWarps / 2 - 1) / (kCombineWarps / 2)));
+        return cudaLaunchKernelEx(&cfg, decode_combine2_kernel<D, BF16, 16>, c);
+    }
+    if (per_seq <= 8 && warps <= (int64_t)plan.ctas * plan.head_groups * 2 * kCombineWarps)
         return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, BF16, 8>, c);
     if (warps <= (int64_t)plan.ctas * plan.head_groups * 4 * kCombineWarps)
         return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, BF16, 16>, c);
